@@ -1,0 +1,351 @@
+"""Benchmark of the fused attention forward pass (tensorized online softmax) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--all]
+
+One step = one pass of the whole hot path (one fat_attn_fwd call) over the
+workload; the default workload is the long-sequence causal shape
+B2 H16 N8192 d128 (bf16, X = 128).  Prints ONE JSON line (rank 0).
+
+Metric: attention forward TFLOP/s, FLOPs = 4 B H N^2 d (halved when causal),
+and the fraction of the measured dense bf16 tensor peak.  Inputs are seeded
+synthetic N(0,1) tensors resident in HBM; L2 is flushed (256 MiB write)
+before every timed step; each step is timed with CUDA events on the stream
+the kernel is launched on.
+
+--impl reference times the CPU oracle (plain double-precision definition) on
+the host cores, each step a bounded sample (one head, 1/8 of its rows).
+With N > 1 ranks every rank runs its own replica (weak scaling; attention
+heads are independent, there is no data-path collective).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "b2h16n8192d128_causal"
+METRIC = "attn fwd TFLOPS on 1 GB300 (bf16/fp8, causal+full) and % of dense tensor peak"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return {"bf16_tflops": float(pk["bf16_tflops"]),
+                "bf16_tflops_sustained": float(pk.get("bf16_tflops_sustained", pk["bf16_tflops"])),
+                "hbm_gbs": float(pk["hbm_gbs"]), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0,
+                "source": "fallback"}
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks / throttle reasons while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def cpu_oracle_sample(w, inp, budget_s: float = 10.0):
+    """Time the oracle as it stands on this host's cores over whole heads of
+    the workload until about ``budget_s`` seconds of work have run."""
+    import oracle
+    from tensorized_online_softmax_gb300 import inputs as gen
+
+    q64, k64, v64 = (gen.widened(inp, n) for n in ("q", "k", "v"))
+    flops_head = w.flops / (w.B * w.H)
+    done, t_total, heads = 0.0, 0.0, 0
+    for b in range(w.B):
+        for h in range(w.H):
+            qs, ks, vs = (t[b:b + 1, h:h + 1].numpy() for t in (q64, k64, v64))
+            t0 = time.perf_counter()
+            oracle.attn_fwd(qs, ks, vs, w.causal, w.scale)
+            t_total += time.perf_counter() - t0
+            done += flops_head
+            heads += 1
+            if t_total >= budget_s:
+                break
+        if t_total >= budget_s:
+            break
+    return {"value": done / t_total / 1e12, "unit": "TFLOP/s", "cores": oracle.available_cores(),
+            "kind": "oracle",
+            "sample": f"{heads} of {w.B * w.H} heads of {w.name}, all rows, float64 "
+                      f"({t_total:.1f} s)"}
+
+
+def run_reference(args, w):
+    """The CPU oracle as the reference arm (rank 0 only)."""
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    import oracle
+    from tensorized_online_softmax_gb300 import inputs as gen
+
+    inp = gen.make_inputs(w)
+    q64, k64, v64 = (gen.widened(inp, n) for n in ("q", "k", "v"))
+    per_step, flops = [], 0.0
+    for step in range(args.warmup + args.steps):
+        b, h = step % w.B, (step // w.B) % w.H
+        r0 = step % 8
+        qs, ks, vs = (t[b:b + 1, h:h + 1].numpy() for t in (q64, k64, v64))
+        rows = range(r0, w.N, 8)
+        step_flops = sum(4.0 * w.d * ((r + 1) if w.causal else w.N) for r in rows)
+        t0 = time.perf_counter()
+        oracle.attn_fwd(qs, ks, vs, w.causal, w.scale, rows=slice(r0, w.N, 8))
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            per_step.append(dt)
+            flops += step_flops
+    total = sum(per_step)
+    value = flops / total / 1e12
+    cores = oracle.available_cores()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / len(per_step), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_dict(w, "oracle"),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step: 1/8 of the rows of one head of {w.name}"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(w, variant):
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+            "X": w.X, "dtype": w.dtype, "variant": variant,
+            "l2": "flushed before every timed step (256 MiB write)"}
+
+
+def time_variant(fat, torch, w, dev, args, variant, flush, stream):
+    """Device time (ms) of each of args.steps launches, L2 flushed before each."""
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    out = (torch.empty((w.B, w.H, w.N, w.d), dtype=torch.float32, device=dev["q"].device),
+           torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev["q"].device))
+
+    def call():
+        if w.dtype == "e4m3":
+            fat.attn_fwd_fp8(dev["q"], dev["k"], dev["v"], dev["q_descale"], dev["k_descale"],
+                             dev["v_descale"], w.causal, w.scale, w.X, out=out, stream=stream)
+        else:
+            fat.attn_fwd(dev["q"], dev["k"], dev["v"], w.causal, w.scale, w.X, variant=variant,
+                         out=out, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            call()
+        stream.synchronize()
+        yield "start"
+        for i in range(args.steps):
+            flush.zero_()
+            starts[i].record(stream)
+            call()
+            ends[i].record(stream)
+        stream.synchronize()
+    yield [s.elapsed_time(e) for s, e in zip(starts, ends)]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-ablation", action="store_true", help="skip timing the vec variant")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from tensorized_online_softmax_gb300 import inputs as gen
+
+    w = gen.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+        return
+
+    import torch
+
+    import tensorized_online_softmax_gb300 as fat
+
+    world, rank, local = dist_setup()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=device)
+        pg = dist
+
+    inp = gen.make_inputs(w)
+    dev = {k: (v.to(device) if isinstance(v, torch.Tensor) and k in ("q", "k", "v") else v)
+           for k, v in inp.items()}
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    stream = torch.cuda.Stream(device)
+    peaks = load_peaks()
+
+    def timed(variant, sample_clocks):
+        gen_ = time_variant(fat, torch, w, dev, args, variant, flush, stream)
+        next(gen_)  # warm-up done
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize(device)
+        sampler = ClockSampler(local) if sample_clocks else None
+        if sampler:
+            sampler.start()
+        t0 = time.perf_counter()
+        times = next(gen_)
+        torch.cuda.synchronize(device)
+        wall = time.perf_counter() - t0
+        if pg:
+            pg.barrier()
+        clocks = sampler.stop() if sampler else None
+        return times, wall, clocks
+
+    times, wall, clocks = timed("tensor", True)
+    if fat.check_device_error(stream) != fat.FAT_OK:
+        raise SystemExit("device error word set during the timed run")
+    total_ms = sum(times)
+    if pg:
+        t = torch.tensor([total_ms], device=device)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * w.flops * args.steps / (total_ms * 1e-3) / 1e12
+    avg_ms = total_ms / args.steps
+    achieved = w.flops / (avg_ms * 1e-3) / 1e12
+
+    ablation = None
+    if not args.no_ablation and w.dtype == "bf16":
+        vt, _, _ = timed("vec", False)
+        v_avg = sum(vt) / len(vt)
+        ablation = {"vec_value": w.flops / (v_avg * 1e-3) / 1e12, "vec_ms_per_step": v_avg,
+                    "tensor_speedup_vs_vec": v_avg / avg_ms}
+
+    # end to end through the public API with host buffers: H2D of q, k, v from
+    # pinned memory, the call, D2H of o and lse, every step
+    e2e = None
+    if args.e2e_steps > 0:
+        host = {n: inp[n].pin_memory() for n in ("q", "k", "v")}
+        o_host = torch.empty((w.B, w.H, w.N, w.d), dtype=torch.float32).pin_memory()
+        l_host = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = o_host.numel() * 4 + l_host.numel() * 4
+        with torch.cuda.stream(stream):
+            e_s = torch.cuda.Event(enable_timing=True)
+            e_e = torch.cuda.Event(enable_timing=True)
+            for i in range(2 + args.e2e_steps):
+                if i == 2:
+                    stream.synchronize()
+                    e_s.record(stream)
+                qd, kd, vd = (host[n].to(device, non_blocking=True) for n in ("q", "k", "v"))
+                o, lse = fat.attn_fwd(qd, kd, vd, w.causal, w.scale, w.X, stream=stream)
+                o_host.copy_(o, non_blocking=True)
+                l_host.copy_(lse, non_blocking=True)
+            e_e.record(stream)
+            stream.synchronize()
+        e2e_ms = e_s.elapsed_time(e_e) / args.e2e_steps
+        e2e = {"value": w.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_oracle_sample(w, inp)
+
+    if rank == 0:
+        peak = peaks["bf16_tflops"]
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": avg_ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": w.dtype, "data": "synthetic", "config": config_dict(w, "tensor"),
+            "pct_of_peak": 100.0 * achieved / peak,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "peak_source": f"{peaks['source']} bf16 dense (burst)"},
+            "ablation": ablation, "e2e": e2e, "cpu_baseline": cpu,
+            "gpu_launches": args.steps, "clocks": clocks,
+            "wall_s_timed_region": wall,
+        }
+        print(json.dumps(line), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

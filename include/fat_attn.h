@@ -1,0 +1,132 @@
+/*
+ * fat_attn.h -- C ABI of the GB300 (sm_103a) fused attention forward pass with
+ * the tensorized online softmax.
+ *
+ * Operation (every entry point): for each batch b, head h and query row i,
+ *
+ *     O[b,h,i,:] = sum_j softmax_j(scale * Q[b,h,i,:] . K[b,h,j,:]) V[b,h,j,:]
+ *     LSE[b,h,i] = ln sum_j exp(scale * Q[b,h,i,:] . K[b,h,j,:])
+ *
+ * over keys j = 0..N-1, or j = 0..i with the causal mask.  This is the fused
+ * attention flow of "FlashAttention-T: Towards Fully Tensorized Attention by
+ * Exploiting Tensor-Vector Parallelism" (papercache.org summary, section A3,
+ * Fig. 2: one output row block per worker, S and P kept on chip), with the
+ * tensorized online softmax of its section A2 (surrogate maximum over X-row
+ * tiles, the equation defining m_hat; Algorithm 1 steps 1-7).
+ *
+ * Conventions shared by all entry points
+ *  - Pointers are DEVICE pointers owned by the caller; the library never
+ *    allocates, frees or keeps them.  Tensors are contiguous row-major:
+ *    q, k, v [B, H, N, d] (bf16, or e4m3 for the fp8 entry point); o fp32
+ *    [B, H, N, d]; lse fp32 [B, H, N] (natural log, in units of the scaled
+ *    logits).  q, k, v, o and lse must be 16-byte aligned.
+ *  - d is 64 or 128; X (rows sharing one surrogate maximum) is 16, 32, 64 or
+ *    128; B, H, N >= 1 (any N: a ragged last tile is masked).
+ *  - Arguments are validated before anything is launched; on failure nothing
+ *    runs and a negative fat_status is returned.
+ *  - The work is enqueued asynchronously on `stream` (0 = legacy default
+ *    stream).  The library never synchronises, except in
+ *    fat_check_device_error().
+ *  - Device-side waits are bounded.  A wait that runs out stops the kernel,
+ *    leaves o/lse unspecified and records FAT_ERR_DEVICE_TIMEOUT in a device
+ *    error word that fat_check_device_error() reports.
+ *  - Calls are re-entrant; the only library state is a per-device cache of
+ *    the driver's tensor-map encoder and kernel attributes.
+ */
+#ifndef FAT_ATTN_H_
+#define FAT_ATTN_H_
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FAT_OK = 0,
+  FAT_ERR_INVALID_ARG = -1,    /* null pointer, bad size, bad d / X, bad scale */
+  FAT_ERR_UNSUPPORTED = -2,    /* a valid request this build does not implement */
+  FAT_ERR_ALIGNMENT = -3,      /* a tensor is not 16-byte aligned */
+  FAT_ERR_LAUNCH = -4,         /* CUDA reported an error while setting up or launching */
+  FAT_ERR_DEVICE_TIMEOUT = -5, /* a bounded device wait ran out (see fat_check_device_error) */
+  FAT_ERR_ARCH = -6            /* the current device is not sm_103 */
+} fat_status;
+
+typedef enum { FAT_VARIANT_TENSOR = 0, FAT_VARIANT_VEC = 1 } fat_variant;
+typedef enum { FAT_DTYPE_BF16 = 0, FAT_DTYPE_E4M3 = 1 } fat_dtype;
+
+/*
+ * Tensorized online softmax (section A2 of the page above).
+ *   - m_hat: per X-row tile, the maximum of the row maxima seen so far
+ *     (Algorithm 1 step 1), kept as an integer number of binades so that the
+ *     rescale factor exp(m_hat_old - m_hat) of steps 2-3 is an exact power of
+ *     two shared by the tile;
+ *   - Z = log2(e) * scale * S - m_hat, P~ = exp2(Z) (steps 4-6);
+ *   - the row sum l of step 7 is produced on the tensor pipe (P~ times a block
+ *     of ones);
+ *   - rows whose surrogate maximum exceeds their exact maximum by more than
+ *     the underflow threshold (default 64 binades), or whose sum is zero,
+ *     are recomputed with the exact per-row maximum (the optional fallback of
+ *     the all-underflow discussion).
+ * q, k, v: bf16.  Returns a fat_status.
+ */
+int fat_attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse, int B, int H,
+                 int N, int d, int causal, float scale, int X, cudaStream_t stream);
+
+/*
+ * Vector-softmax ablation baseline (the "FA2" arm of the page's Fig. 10
+ * ablation): exact per-row maximum, per-row rescale of O whenever a row
+ * maximum grows, row sum accumulated on the vector units.  Same pipeline,
+ * tiling and signature as fat_attn_fwd; X is validated but unused.
+ */
+int fat_attn_fwd_vec(const void* q, const void* k, const void* v, float* o, float* lse, int B,
+                     int H, int N, int d, int causal, float scale, int X, cudaStream_t stream);
+
+/*
+ * FP8 (e4m3) inputs with per-tensor fp32 descales (real value = code * descale),
+ * fp32 accumulation, the tensorized softmax of fat_attn_fwd.  (The page
+ * evaluates FP8-FP32 attention in its section A4.)
+ */
+int fat_attn_fwd_fp8(const void* q, const void* k, const void* v, float q_descale,
+                     float k_descale, float v_descale, float* o, float* lse, int B, int H, int N,
+                     int d, int causal, float scale, int X, cudaStream_t stream);
+
+/* Every knob of the entry points above in one struct (tests and ablations). */
+typedef struct fat_params {
+  const void* q;
+  const void* k;
+  const void* v;
+  float* o;
+  float* lse;
+  int B, H, N, d;
+  int causal;
+  float scale;
+  int X;
+  int variant;                        /* fat_variant */
+  int dtype;                          /* fat_dtype */
+  float q_descale, k_descale, v_descale; /* e4m3 only; ignored for bf16 */
+  float underflow_log2_threshold;     /* <= 0: default (64 binades for bf16 P, 6 for e4m3 P) */
+  int* fallback_rows;                 /* nullable device int: += number of rows recomputed */
+  unsigned long long wait_poll_limit; /* 0: no cap on polls of one device wait */
+  unsigned long long wait_timeout_ns; /* 0: default of 4 s per device wait */
+  cudaStream_t stream;
+} fat_params;
+
+int fat_attn_fwd_ex(const fat_params* p);
+
+/* Human-readable name of a fat_status value (static string). */
+const char* fat_status_string(int status);
+
+/*
+ * Synchronises `stream`, then reads and clears the device error word of the
+ * current device.  Returns FAT_ERR_DEVICE_TIMEOUT if a kernel of this library
+ * stopped on a bounded wait since the last check, FAT_ERR_LAUNCH if the
+ * synchronisation itself failed, FAT_OK otherwise.
+ */
+int fat_check_device_error(cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FAT_ATTN_H_ */

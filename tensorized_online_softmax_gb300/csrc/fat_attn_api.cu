@@ -1,0 +1,230 @@
+// Host side of the C ABI declared in include/fat_attn.h: argument validation,
+// TMA tensor-map encoding, kernel selection and launch.  Nothing here
+// allocates device memory or synchronises (except fat_check_device_error).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/fat_attn.h"
+#include "fat_fwd_kernel.cuh"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceCache {
+  std::once_flag once;
+  int arch_ok = 0;  // 1: sm_103
+  int smem_set[4] = {0, 0, 0, 0};
+};
+DeviceCache g_dev[kMaxDevices];
+
+std::once_flag g_encoder_once;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+  std::call_once(g_encoder_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+// [B*H, N, d] view of a contiguous [B, H, N, d] tensor, boxes of 128 rows x
+// 128 bytes, 128-byte swizzle (the layout the tcgen05 descriptors expect).
+// Rows past N read as zero.
+bool encode_qkv_map(CUtensorMap* tm, const void* ptr, int d, int N, int BH, int elt_bytes) {
+  auto enc = encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * elt_bytes,
+                                 static_cast<cuuint64_t>(N) * d * elt_bytes};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elt_bytes), 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt =
+      elt_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  return enc(tm, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <int D, bool kTensor>
+int launch(const fat::FwdParams& fp, int dev, int slot, int grid, cudaStream_t stream) {
+  auto kern = fat::fat_fwd_kernel<D, kTensor>;
+  const int smem = fat::Smem<D>::kAlloc;
+  if (!g_dev[dev].smem_set[slot]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return FAT_ERR_LAUNCH;
+    g_dev[dev].smem_set[slot] = 1;
+  }
+  kern<<<grid, fat::kNumThreads, smem, stream>>>(fp);
+  return cudaGetLastError() == cudaSuccess ? FAT_OK : FAT_ERR_LAUNCH;
+}
+
+int check_device(int* dev_out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FAT_ERR_LAUNCH;
+  DeviceCache& c = g_dev[dev];
+  std::call_once(c.once, [&] {
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    c.arch_ok = (major == 10 && minor == 3) ? 1 : 0;
+  });
+  *dev_out = dev;
+  return c.arch_ok ? FAT_OK : FAT_ERR_ARCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* fat_status_string(int status) {
+  switch (status) {
+    case FAT_OK: return "FAT_OK";
+    case FAT_ERR_INVALID_ARG: return "FAT_ERR_INVALID_ARG";
+    case FAT_ERR_UNSUPPORTED: return "FAT_ERR_UNSUPPORTED";
+    case FAT_ERR_ALIGNMENT: return "FAT_ERR_ALIGNMENT";
+    case FAT_ERR_LAUNCH: return "FAT_ERR_LAUNCH";
+    case FAT_ERR_DEVICE_TIMEOUT: return "FAT_ERR_DEVICE_TIMEOUT";
+    case FAT_ERR_ARCH: return "FAT_ERR_ARCH";
+    default: return "FAT_ERR_UNKNOWN";
+  }
+}
+
+int fat_attn_fwd_ex(const fat_params* p) {
+  if (!p) return FAT_ERR_INVALID_ARG;
+  // ---- synchronous validation: nothing is launched on failure ----
+  if (!p->q || !p->k || !p->v || !p->o || !p->lse) return FAT_ERR_INVALID_ARG;
+  if (p->B < 1 || p->H < 1 || p->N < 1) return FAT_ERR_INVALID_ARG;
+  if (p->d != 64 && p->d != 128) return FAT_ERR_INVALID_ARG;
+  if (p->X != 16 && p->X != 32 && p->X != 64 && p->X != 128) return FAT_ERR_INVALID_ARG;
+  if (!(p->scale > 0.f) || !std::isfinite(p->scale)) return FAT_ERR_INVALID_ARG;
+  if (p->variant != FAT_VARIANT_TENSOR && p->variant != FAT_VARIANT_VEC) return FAT_ERR_INVALID_ARG;
+  if (p->dtype != FAT_DTYPE_BF16 && p->dtype != FAT_DTYPE_E4M3) return FAT_ERR_INVALID_ARG;
+  const long long BH = static_cast<long long>(p->B) * p->H;
+  const long long n_mblocks = (p->N + fat::kRowsPerCta - 1) / fat::kRowsPerCta;
+  if (BH > (1ll << 30) || BH * n_mblocks > 0x7fffffffll) return FAT_ERR_INVALID_ARG;
+  if (!aligned16(p->q) || !aligned16(p->k) || !aligned16(p->v) || !aligned16(p->o) ||
+      !aligned16(p->lse))
+    return FAT_ERR_ALIGNMENT;
+  if (p->dtype == FAT_DTYPE_E4M3) return FAT_ERR_UNSUPPORTED;
+
+  int dev = 0;
+  const int arch = check_device(&dev);
+  if (arch != FAT_OK) return arch;
+
+  fat::FwdParams fp;
+  const int elt = 2;
+  if (!encode_qkv_map(&fp.tm_q, p->q, p->d, p->N, static_cast<int>(BH), elt) ||
+      !encode_qkv_map(&fp.tm_k, p->k, p->d, p->N, static_cast<int>(BH), elt) ||
+      !encode_qkv_map(&fp.tm_v, p->v, p->d, p->N, static_cast<int>(BH), elt))
+    return FAT_ERR_LAUNCH;
+  fp.o = p->o;
+  fp.lse = p->lse;
+  fp.fallback_rows = p->fallback_rows;
+  fp.B = p->B;
+  fp.H = p->H;
+  fp.N = p->N;
+  fp.causal = p->causal ? 1 : 0;
+  fp.X = p->X;
+  fp.n_mblocks = static_cast<int>(n_mblocks);
+  fp.scale = p->scale;
+  fp.c = p->scale * fat::kLog2e;
+  fp.underflow_thresh = p->underflow_log2_threshold > 0.f ? p->underflow_log2_threshold : 64.f;
+  fp.poll_limit = p->wait_poll_limit;
+  fp.timeout_ns = p->wait_timeout_ns ? p->wait_timeout_ns : 4000000000ull;
+
+  const int grid = static_cast<int>(BH * n_mblocks);
+  const bool tensor = p->variant == FAT_VARIANT_TENSOR;
+  if (p->d == 128)
+    return tensor ? launch<128, true>(fp, dev, 0, grid, p->stream)
+                  : launch<128, false>(fp, dev, 1, grid, p->stream);
+  return tensor ? launch<64, true>(fp, dev, 2, grid, p->stream)
+                : launch<64, false>(fp, dev, 3, grid, p->stream);
+}
+
+static int fwd_common(const void* q, const void* k, const void* v, float* o, float* lse, int B,
+                      int H, int N, int d, int causal, float scale, int X, cudaStream_t stream,
+                      int variant) {
+  fat_params p = {};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.d = d;
+  p.causal = causal;
+  p.scale = scale;
+  p.X = X;
+  p.variant = variant;
+  p.dtype = FAT_DTYPE_BF16;
+  p.stream = stream;
+  return fat_attn_fwd_ex(&p);
+}
+
+int fat_attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse, int B, int H,
+                 int N, int d, int causal, float scale, int X, cudaStream_t stream) {
+  return fwd_common(q, k, v, o, lse, B, H, N, d, causal, scale, X, stream, FAT_VARIANT_TENSOR);
+}
+
+int fat_attn_fwd_vec(const void* q, const void* k, const void* v, float* o, float* lse, int B,
+                     int H, int N, int d, int causal, float scale, int X, cudaStream_t stream) {
+  return fwd_common(q, k, v, o, lse, B, H, N, d, causal, scale, X, stream, FAT_VARIANT_VEC);
+}
+
+int fat_attn_fwd_fp8(const void* q, const void* k, const void* v, float q_descale,
+                     float k_descale, float v_descale, float* o, float* lse, int B, int H, int N,
+                     int d, int causal, float scale, int X, cudaStream_t stream) {
+  fat_params p = {};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.H = H;
+  p.N = N;
+  p.d = d;
+  p.causal = causal;
+  p.scale = scale;
+  p.X = X;
+  p.variant = FAT_VARIANT_TENSOR;
+  p.dtype = FAT_DTYPE_E4M3;
+  p.q_descale = q_descale;
+  p.k_descale = k_descale;
+  p.v_descale = v_descale;
+  p.stream = stream;
+  return fat_attn_fwd_ex(&p);
+}
+
+int fat_check_device_error(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FAT_ERR_LAUNCH;
+  unsigned int word = 0;
+  if (cudaMemcpyFromSymbol(&word, fat::g_fat_error_word, sizeof(word)) != cudaSuccess)
+    return FAT_ERR_LAUNCH;
+  if (word != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(fat::g_fat_error_word, &zero, sizeof(zero)) != cudaSuccess)
+      return FAT_ERR_LAUNCH;
+    return FAT_ERR_DEVICE_TIMEOUT;
+  }
+  return FAT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,509 @@
+// Fused attention forward pass for sm_103a with the tensorized online softmax
+// of "FlashAttention-T: Towards Fully Tensorized Attention by Exploiting
+// Tensor-Vector Parallelism" (papercache.org summary, section A2, Algorithm 1)
+// and its vector-softmax ablation (the FA2 arm of the page's Fig. 10).
+//
+// One CTA computes 256 query rows of one (batch, head) as two 128-row tiles
+// (t = 0, 1) that ping-pong on the tensor pipe, the fused flow of the page's
+// section A3 / Fig. 2 (one output row block per worker, S and P on chip):
+//
+//   warp 9      TMA producer: Q0, Q1 once; K_j, V_j through an mbarrier ring.
+//   warp 8      MMA issuer (one thread): S_t = Q_t K_j^T into TMEM,
+//               O_t += P_t V_j from TMEM, and (tensorized) l_t = P_t 1.
+//   warps 0-7   softmax, warpgroup t owns tile t, thread i owns row i
+//               (TMEM lane i): row max, X-row tile max, O rescale, P = exp2(Z).
+//
+// TMEM (512 columns x 128 lanes, fp32): S_0 [0,128), S_1 [128,256),
+// O_0 [256, 256+D), O_1 [256+D, 256+2D).  P_t is written as packed bf16 over
+// S_t columns [0,64); the tensorized row sum lands in S_t column 64.
+#pragma once
+
+#include <cuda.h>
+
+#include "sm103_ptx.cuh"
+
+namespace fat {
+
+constexpr int kBlockM = 128;  // query rows per tile (= TMEM lanes)
+constexpr int kBlockN = 128;  // keys per K/V tile
+constexpr int kRowsPerCta = 2 * kBlockM;
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr int kNumThreads = 320;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Device error word: bit 0 = a bounded wait ran out.
+__device__ unsigned int g_fat_error_word = 0;
+
+struct FwdParams {
+  CUtensorMap tm_q;
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  float* o;
+  float* lse;
+  int* fallback_rows;
+  int B, H, N;
+  int causal;
+  int X;
+  int n_mblocks;           // ceil(N / 256)
+  float scale;             // softmax scale as received
+  float c;                 // log2(e) * scale (times q/k descales for e4m3)
+  float underflow_thresh;  // binades between surrogate and exact row maximum
+  unsigned long long poll_limit;
+  unsigned long long timeout_ns;
+};
+
+template <int D>
+struct Smem {
+  static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr int kTile = kBlockM * D * 2;  // bytes of one 128 x D bf16 tile
+  static constexpr int kAtoms = D / 64;          // 128-byte-wide column slabs per tile
+  static constexpr int kQ = 0;                   // Q_t at kQ + t * kTile
+  static constexpr int kK = 2 * kTile;           // K ring
+  static constexpr int kV = kK + kStages * kTile;  // V ring
+  static constexpr int kOnes = kV + kStages * kTile;  // 16 x 64 bf16 ones (2 KB)
+  static constexpr int kBars = kOnes + 2048;
+  // barrier slots
+  static constexpr int bQFull = 0;
+  static constexpr int bKFull = 1;
+  static constexpr int bKEmpty = bKFull + kStages;
+  static constexpr int bVFull = bKEmpty + kStages;
+  static constexpr int bVEmpty = bVFull + kStages;
+  static constexpr int bSFull = bVEmpty + kStages;  // [2]
+  static constexpr int bPFull = bSFull + 2;         // [2]
+  static constexpr int bRsFull = bPFull + 2;        // [2]
+  static constexpr int bLFree = bRsFull + 2;        // [2]
+  static constexpr int bRed = bLFree + 2;           // [2] tile-max exchange
+  static constexpr int bOFinal = bRed + 2;
+  static constexpr int bDrain = bOFinal + 1;
+  static constexpr int kNumBars = bDrain + 1;
+  static constexpr int kRed = kBars + 8 * kNumBars;  // float [2 tiles][2 parity][4 warps]
+  static constexpr int kMisc = kRed + 64;            // u32: tmem base, abort, redo
+  static constexpr int kBytes = kMisc + 64;
+  static constexpr int kAlloc = kBytes + 1024;       // slack for 1024-byte alignment
+  static_assert(kK % 1024 == 0 && kV % 1024 == 0 && kOnes % 1024 == 0, "tiles 1 KB aligned");
+  static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+};
+
+// ---------------------------------------------------------------------------
+// bounded waits
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const FwdParams& p,
+                                             volatile uint32_t* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint64_t polls = 1;
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    ++polls;
+    if (*abort_flag) break;
+    if (p.poll_limit != 0 && polls >= p.poll_limit) break;
+    if ((polls & 63) == 0 && globaltimer_ns() - t0 > p.timeout_ns) break;
+  }
+  atomicOr(&g_fat_error_word, 1u);
+  *abort_flag = 1u;
+  return false;
+}
+
+// Waits used only to drain work already in flight after an abort: they never
+// look at the abort flag and use a fixed one-second limit.
+__device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > 1000000000ull) return;
+  }
+}
+
+__device__ __forceinline__ float bf16_round(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+template <int D, bool kTensor>
+__global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using L = Smem<D>;
+  constexpr int S = L::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + L::kMisc);
+  volatile uint32_t* abort_flag = misc + 1;
+  auto bar = [&](int i) -> uint32_t { return sb + L::kBars + 8 * i; };
+
+  // work item: heaviest query blocks first (causal), then (b, h)
+  const int BH = p.B * p.H;
+  const int mblock = p.n_mblocks - 1 - static_cast<int>(blockIdx.x) / BH;
+  const int bh = static_cast<int>(blockIdx.x) % BH;
+  const int m0 = mblock * kRowsPerCta;
+  const int n_kv_all = (p.N + kBlockN - 1) / kBlockN;
+  const int n_kv = p.causal ? min(n_kv_all, (m0 + kRowsPerCta) / kBlockN) : n_kv_all;
+
+  // ---- set-up --------------------------------------------------------------
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::bQFull), 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(bar(L::bKFull + s), 1);
+      mbar_init(bar(L::bKEmpty + s), 1);
+      mbar_init(bar(L::bVFull + s), 1);
+      mbar_init(bar(L::bVEmpty + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(L::bSFull + t), 1);
+      mbar_init(bar(L::bPFull + t), 4);
+      mbar_init(bar(L::bRsFull + t), 1);
+      mbar_init(bar(L::bLFree + t), 4);
+      mbar_init(bar(L::bRed + t), 4);
+    }
+    mbar_init(bar(L::bOFinal), 1);
+    mbar_init(bar(L::bDrain), 1);
+    misc[1] = 0;
+    misc[2] = 0;
+    fence_mbar_init();
+  }
+  if (threadIdx.x < 256) {  // the ones tile used as B of the row-sum MMA
+    reinterpret_cast<uint2*>(smem + L::kOnes)[threadIdx.x] = make_uint2(0x3F803F80u, 0x3F803F80u);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(sb + L::kMisc, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+
+  for (int pass = 0; pass < 2; ++pass) {
+    const bool tensor_pass = kTensor && pass == 0;
+    const int it0 = pass * n_kv;
+
+    if (warp == kLoadWarp) {
+      // =================== TMA producer ===================
+      if (lane == 0) {
+        int k_issued = 0, v_issued = 0;
+        if (pass == 0) {
+          tma_prefetch_desc(&p.tm_q);
+          tma_prefetch_desc(&p.tm_k);
+          tma_prefetch_desc(&p.tm_v);
+          mbar_arrive_expect_tx(bar(L::bQFull), 2 * L::kTile);
+          for (int t = 0; t < 2; ++t)
+            for (int a = 0; a < L::kAtoms; ++a)
+              tma_load_3d(sb + L::kQ + t * L::kTile + a * 16384, &p.tm_q, bar(L::bQFull), a * 64,
+                          m0 + t * kBlockM, bh);
+        }
+        for (int j = 0; j < n_kv; ++j) {
+          const int it = it0 + j, st = it % S;
+          const uint32_t ph = (it / S) & 1;
+          if (!wait_bounded(bar(L::bKEmpty + st), ph ^ 1, p, abort_flag)) break;
+          mbar_arrive_expect_tx(bar(L::bKFull + st), L::kTile);
+          for (int a = 0; a < L::kAtoms; ++a)
+            tma_load_3d(sb + L::kK + st * L::kTile + a * 16384, &p.tm_k, bar(L::bKFull + st),
+                        a * 64, j * kBlockN, bh);
+          k_issued = j + 1;
+          if (!wait_bounded(bar(L::bVEmpty + st), ph ^ 1, p, abort_flag)) break;
+          mbar_arrive_expect_tx(bar(L::bVFull + st), L::kTile);
+          for (int a = 0; a < L::kAtoms; ++a)
+            tma_load_3d(sb + L::kV + st * L::kTile + a * 16384, &p.tm_v, bar(L::bVFull + st),
+                        a * 64, j * kBlockN, bh);
+          v_issued = j + 1;
+        }
+        if (*abort_flag) {
+          // let every copy already issued land before the CTA can exit
+          if (pass == 0) wait_drain(bar(L::bQFull), 0);
+          for (int j = max(0, k_issued - S); j < k_issued; ++j)
+            wait_drain(bar(L::bKFull + (it0 + j) % S), ((it0 + j) / S) & 1);
+          for (int j = max(0, v_issued - S); j < v_issued; ++j)
+            wait_drain(bar(L::bVFull + (it0 + j) % S), ((it0 + j) / S) & 1);
+        }
+      }
+      __syncwarp();
+    } else if (warp == kMmaWarp) {
+      // =================== MMA issuer ===================
+      if (lane == 0) {
+        constexpr uint32_t idesc_s = idesc_f32acc<false>(kBlockM, kBlockN, false);
+        constexpr uint32_t idesc_pv = idesc_f32acc<false>(kBlockM, D, true);
+        constexpr uint32_t idesc_rs = idesc_f32acc<false>(kBlockM, 16, false);
+        const uint64_t ones_desc = sdesc_sw128(sb + L::kOnes, 16, 1024);
+        bool ok = true;
+        auto issue_s = [&](int t, int st) {
+          const uint32_t qa = sb + L::kQ + t * L::kTile, ka = sb + L::kK + st * L::kTile;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_ss<false>(tmem + t * kBlockN, sdesc_sw128(qa + off, 16, 1024),
+                          sdesc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
+          }
+        };
+        auto issue_pv = [&](int t, int st, bool acc) {
+          const uint32_t va = sb + L::kV + st * L::kTile;
+#pragma unroll
+          for (int kk = 0; kk < kBlockN / 16; ++kk)
+            mma_ts<false>(tmem + 2 * kBlockN + t * D, tmem + t * kBlockN + kk * 8,
+                          sdesc_sw128(va + kk * 2048, 16384, 1024), idesc_pv, acc || kk > 0);
+        };
+        auto issue_rs = [&](int t) {
+#pragma unroll
+          for (int kk = 0; kk < kBlockN / 16; ++kk)
+            mma_ts<false>(tmem + t * kBlockN + 64, tmem + t * kBlockN + kk * 8, ones_desc, idesc_rs,
+                          kk > 0);
+        };
+
+        if (pass == 0) ok = wait_bounded(bar(L::bQFull), 0, p, abort_flag);
+        if (ok) {
+          const int st = it0 % S;
+          ok = wait_bounded(bar(L::bKFull + st), (it0 / S) & 1, p, abort_flag);
+          if (ok) {
+            tc_fence_after();
+            issue_s(0, st);
+            mma_commit(bar(L::bSFull + 0));
+            issue_s(1, st);
+            mma_commit(bar(L::bSFull + 1));
+            mma_commit(bar(L::bKEmpty + st));
+          }
+        }
+        for (int j = 0; ok && j < n_kv; ++j) {
+          const int it = it0 + j, st = it % S;
+          const uint32_t ph = (it / S) & 1, par = it & 1;
+          const bool more = j + 1 < n_kv;
+          const int st1 = (it + 1) % S;
+          const uint32_t ph1 = ((it + 1) / S) & 1;
+          if (!(ok = wait_bounded(bar(L::bVFull + st), ph, p, abort_flag))) break;
+          // tile 0
+          if (!(ok = wait_bounded(bar(L::bPFull + 0), par, p, abort_flag))) break;
+          tc_fence_after();
+          if (tensor_pass) {
+            issue_rs(0);
+            mma_commit(bar(L::bRsFull + 0));
+          }
+          issue_pv(0, st, j > 0);
+          if (more) {
+            if (!(ok = wait_bounded(bar(L::bKFull + st1), ph1, p, abort_flag))) break;
+            if (tensor_pass && !(ok = wait_bounded(bar(L::bLFree + 0), par, p, abort_flag))) break;
+            tc_fence_after();
+            issue_s(0, st1);
+            mma_commit(bar(L::bSFull + 0));
+          }
+          // tile 1
+          if (!(ok = wait_bounded(bar(L::bPFull + 1), par, p, abort_flag))) break;
+          tc_fence_after();
+          if (tensor_pass) {
+            issue_rs(1);
+            mma_commit(bar(L::bRsFull + 1));
+          }
+          issue_pv(1, st, j > 0);
+          mma_commit(bar(L::bVEmpty + st));
+          if (more) {
+            if (tensor_pass && !(ok = wait_bounded(bar(L::bLFree + 1), par, p, abort_flag))) break;
+            tc_fence_after();
+            issue_s(1, st1);
+            mma_commit(bar(L::bSFull + 1));
+            mma_commit(bar(L::bKEmpty + st1));
+          }
+        }
+        if (ok) {
+          mma_commit(bar(L::bOFinal));
+        } else {
+          // every MMA issued so far must finish before TMEM can be released
+          mma_commit(bar(L::bDrain));
+          wait_drain(bar(L::bDrain), 0);
+        }
+      }
+      __syncwarp();
+    } else {
+      // =================== softmax warpgroups ===================
+      const int t = warp >> 2;        // tile
+      const int wq = warp & 3;        // quarter of the tile (TMEM lanes 32*wq ..)
+      const int r = wq * 32 + lane;   // row within the tile
+      const int row_g = m0 + t * kBlockM + r;
+      const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+      const uint32_t s_taddr = tmem + lane_base + t * kBlockN;
+      const uint32_t o_taddr = tmem + lane_base + 2 * kBlockN + t * D;
+      const float c = p.c;
+      const int X = p.X;
+      float* red = reinterpret_cast<float*>(smem + L::kRed);
+
+      float M = -INFINITY;      // offset of the exponent, binades (exact row max * c in vec mode)
+      float m_row = -INFINITY;  // exact running row maximum, raw logits
+      float l = 0.f;            // running row sum
+      float delta = 0.f;        // tensorized: rounding of each tile's dominant term
+      bool ok = true;
+
+      for (int j = 0; j < n_kv; ++j) {
+        const int it = it0 + j;
+        const uint32_t par = it & 1;
+        ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bSFull + t), par, p, abort_flag));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t s[4][32];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) tmem_ld32(s_taddr + 32 * k, s[k]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) tmem_wait_ld(s[k]);
+
+        // mask: keys >= N, keys after the query (causal), padding rows
+        const int kv0 = j * kBlockN;
+        int limit = (row_g < p.N) ? (p.causal ? min(p.N, row_g + 1) : p.N) - kv0 : 0;
+        if (limit < kBlockN) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (32 * k + i >= limit) s[k][i] = __float_as_uint(-INFINITY);
+        }
+        float rowmax = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) rowmax = fmaxf(rowmax, __uint_as_float(s[k][i]));
+        m_row = fmaxf(m_row, rowmax);
+
+        float M_new;
+        if (tensor_pass) {
+          // Algorithm 1 step 1: maximum of the row maxima over the X-row tile
+          float tmax = rowmax;
+          const int xw = X < 32 ? X : 32;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1)
+            if (o < xw) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+          if (X > 32) {
+            float* slot = red + (t * 2 + par) * 4;
+            if (lane == 0) slot[wq] = tmax;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(L::bRed + t));
+            ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bRed + t), par, p, abort_flag));
+            if (!ok) break;
+            const int g0 = (X == 64) ? (wq & 2) : 0, gn = X / 32;
+            for (int w = 0; w < gn; ++w) tmax = fmaxf(tmax, slot[g0 + w]);
+          }
+          // the surrogate maximum is kept as a whole number of binades so the
+          // rescale factor of steps 2-3 is an exact power of two
+          const float Mc = (tmax == -INFINITY) ? -INFINITY : ceilf(tmax * c);
+          M_new = fmaxf(M, Mc);
+        } else {
+          M_new = (m_row == -INFINITY) ? -INFINITY : m_row * c;
+        }
+
+        // Algorithm 1 steps 2-3 factor: exp(m_old - m_new), one exact power
+        // of two per X-row tile (exact per-row factor in the vector variant).
+        const bool grow = j > 0 && M_new > M;
+        const float alpha = (M_new == -INFINITY) ? 1.f : ex2_approx(M - M_new);
+        if (j > 0) {
+          l *= alpha;
+          delta *= alpha;
+        }
+        M = M_new;
+        const float neg_M = (M == -INFINITY) ? 0.f : -M;
+
+        // steps 4-6: Z = c S - m_hat, P~ = exp2(Z), stored as bf16 over S
+        float rowsum = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(s[k][2 * i]), c, neg_M));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(s[k][2 * i + 1]), c, neg_M));
+            if (!tensor_pass) rowsum += p0 + p1;
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16(s_taddr + 16 * k, pk);
+        }
+        // steps 2-3: O <- alpha O in TMEM.  PV_{j-1} has completed (it was
+        // issued before S_j, whose completion we waited for) and PV_j waits
+        // for this warpgroup's P-full signal below.
+        if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+          for (int k = 0; k < D / 32; ++k) {
+            uint32_t ov[32];
+            tmem_ld32(o_taddr + 32 * k, ov);
+            tmem_wait_ld(ov);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            tmem_st32(o_taddr + 32 * k, ov);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::bPFull + t));
+
+        if (tensor_pass) {
+          // step 7: the row sum comes from the tensor pipe (P~ times ones);
+          // the LSE also gets back the bf16 rounding of the dominant term.
+          if (rowmax != -INFINITY) {
+            const float pm = ex2_approx(fmaf(rowmax, c, neg_M));
+            delta += pm - bf16_round(pm);
+          }
+          ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bRsFull + t), par, p, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+          uint32_t lt;
+          tmem_ld1(s_taddr + 64, lt);
+          tmem_wait_ld1(lt);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(L::bLFree + t));
+          l += __uint_as_float(lt);
+        } else {
+          l += rowsum;
+        }
+      }
+
+      if (ok) ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bOFinal), pass & 1, p, abort_flag));
+      if (ok) {
+        tc_fence_after();
+        // detector for the all-underflow case: surrogate far above the exact
+        // maximum, or nothing left of the row sum
+        if (tensor_pass) {
+          const bool flagged =
+              row_g < p.N && (!(l > 0.f) || (M - m_row * c) > p.underflow_thresh);
+          const uint32_t ball = __ballot_sync(0xffffffffu, flagged);
+          if (ball != 0 && lane == 0) {
+            atomicOr(const_cast<uint32_t*>(misc + 2), 1u);
+            if (p.fallback_rows) atomicAdd(p.fallback_rows, __popc(ball));
+          }
+        }
+        // epilogue: O / l and LSE
+        const float inv_l = 1.f / l;
+        float* orow = p.o + (static_cast<size_t>(bh) * p.N + row_g) * D;
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k) {
+          uint32_t ov[32];
+          tmem_ld32(o_taddr + 32 * k, ov);
+          tmem_wait_ld(ov);
+          if (row_g < p.N) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              float4 v4 = make_float4(__uint_as_float(ov[i]) * inv_l, __uint_as_float(ov[i + 1]) * inv_l,
+                                      __uint_as_float(ov[i + 2]) * inv_l, __uint_as_float(ov[i + 3]) * inv_l);
+              *reinterpret_cast<float4*>(orow + 32 * k + i) = v4;
+            }
+          }
+        }
+        if (row_g < p.N) {
+          const float lsum = tensor_pass ? l + delta : l;
+          p.lse[static_cast<size_t>(bh) * p.N + row_g] = (M + __log2f(lsum)) * kLn2;
+        }
+      }
+      tc_fence_before();
+    }
+
+    __syncthreads();
+    if (!kTensor || misc[2] == 0u || *abort_flag != 0u) break;
+    // some row of this CTA was flagged: recompute the block with the exact
+    // per-row maximum (the optional vector fallback of the page's
+    // all-underflow discussion)
+  }
+
+  tc_fence_after();
+  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace fat

@@ -1,0 +1,89 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the C ABI,
+run the oracle on the same seeded inputs (whole tensors or sampled rows), and
+compare with the accuracy bars of the fused-attention forward pass."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import tensorized_online_softmax_gb300 as fat
+from tensorized_online_softmax_gb300 import inputs as gen
+
+# acceptance bars (max-abs / mean-abs on O, max-abs on LSE)
+TOL = {
+    "bf16": dict(o_max=2e-2, o_mean=2e-3, lse_max=1e-3),
+    "e4m3": dict(o_max=6e-2, o_mean=6e-3, lse_max=1e-3),
+}
+
+
+def to_dev(inputs, device="cuda"):
+    return {k: (v.to(device) if isinstance(v, torch.Tensor) and k in ("q", "k", "v") else v)
+            for k, v in inputs.items()}
+
+
+def run_cuda(w: gen.Workload, dev_inputs, variant="tensor", **kw):
+    q, k, v = dev_inputs["q"], dev_inputs["k"], dev_inputs["v"]
+    if w.dtype == "e4m3":
+        o, lse = fat.attn_fwd_fp8(q, k, v, dev_inputs["q_descale"], dev_inputs["k_descale"],
+                                  dev_inputs["v_descale"], causal=w.causal, scale=w.scale, X=w.X,
+                                  **kw)
+    else:
+        o, lse = fat.attn_fwd(q, k, v, causal=w.causal, scale=w.scale, X=w.X, variant=variant,
+                              **kw)
+    torch.cuda.synchronize()
+    return o, lse
+
+
+def oracle_full(w: gen.Workload, inputs):
+    return oracle.attn_fwd(gen.widened(inputs, "q"), gen.widened(inputs, "k"),
+                           gen.widened(inputs, "v"), w.causal, w.scale)
+
+
+def sample_rows(N: int, n_random: int, seed: int):
+    """Rows on tile edges (0, 127, 128, 255, 256, N-1) plus random rows."""
+    rng = np.random.default_rng(seed)
+    fixed = [r for r in (0, 1, 127, 128, 255, 256, 383, N // 2, N - 2, N - 1) if 0 <= r < N]
+    rnd = rng.choice(N, size=min(n_random, N), replace=False).tolist()
+    return sorted(set(fixed + rnd))
+
+
+def oracle_sampled(w: gen.Workload, inputs, heads, rows):
+    """Oracle O/LSE for the given (b, h) heads and query rows only."""
+    out = {}
+    q64 = gen.widened(inputs, "q")
+    k64 = gen.widened(inputs, "k")
+    v64 = gen.widened(inputs, "v")
+    for (b, h) in heads:
+        qs = q64[b:b + 1, h:h + 1].numpy()
+        ks = k64[b:b + 1, h:h + 1].numpy()
+        vs = v64[b:b + 1, h:h + 1].numpy()
+        for r in rows:
+            o, lse = oracle.attn_fwd(qs, ks, vs, w.causal, w.scale, rows=slice(r, r + 1))
+            out[(b, h, r)] = (o[0, 0, r], lse[0, 0, r])
+    return out
+
+
+def compare(o_gpu, lse_gpu, o_ref, lse_ref, dtype="bf16", what=""):
+    """Element-by-element comparison against the bars; returns the error stats."""
+    tol = TOL[dtype]
+    o_gpu = np.asarray(o_gpu, dtype=np.float64)
+    lse_gpu = np.asarray(lse_gpu, dtype=np.float64)
+    assert np.isfinite(o_gpu).all(), f"{what}: non-finite O"
+    assert np.isfinite(lse_gpu).all(), f"{what}: non-finite LSE"
+    err = np.abs(o_gpu - o_ref)
+    lerr = np.abs(lse_gpu - lse_ref)
+    stats = dict(o_max=float(err.max()), o_mean=float(err.mean()), lse_max=float(lerr.max()))
+    assert stats["o_max"] <= tol["o_max"], f"{what}: {stats}"
+    assert stats["o_mean"] <= tol["o_mean"], f"{what}: {stats}"
+    assert stats["lse_max"] <= tol["lse_max"], f"{what}: {stats}"
+    return stats
+
+
+def compare_sampled(o_gpu, lse_gpu, ref: dict, dtype="bf16", what=""):
+    keys = sorted(ref)
+    og = np.stack([o_gpu[b, h, r].double().cpu().numpy() for (b, h, r) in keys])
+    lg = np.array([float(lse_gpu[b, h, r]) for (b, h, r) in keys])
+    orf = np.stack([ref[key][0] for key in keys])
+    lrf = np.array([ref[key][1] for key in keys])
+    return compare(og, lg, orf, lrf, dtype, what)

@@ -1,0 +1,101 @@
+"""The C ABI library builds, loads, exports every entry point of
+include/fat_attn.h, and rejects bad arguments before touching a GPU.
+No compute call is made here (no GPU in this environment)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import tensorized_online_softmax_gb300 as fat
+from tensorized_online_softmax_gb300 import _build
+
+HEADER = os.path.join(_build.ROOT, "include", "fat_attn.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(fat_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if _build.nvcc_path() is None and not os.path.exists(_build.LIB_PATH):
+        pytest.skip("no nvcc and no prebuilt library")
+    return fat.load_library()
+
+
+def test_header_declares_the_abi():
+    assert declared_functions() == sorted(fat.ABI_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", _build.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    for name in declared_functions():
+        assert re.search(rf"\bT {name}$", out, flags=re.M), name
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "FAT_OK"), (-1, "FAT_ERR_INVALID_ARG"), (-2, "FAT_ERR_UNSUPPORTED"),
+                       (-3, "FAT_ERR_ALIGNMENT"), (-4, "FAT_ERR_LAUNCH"),
+                       (-5, "FAT_ERR_DEVICE_TIMEOUT"), (-6, "FAT_ERR_ARCH")]:
+        assert lib.fat_status_string(code).decode() == name
+
+
+def _fwd(lib, q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000, B=1, H=1, N=128, d=64,
+         causal=0, scale=0.125, X=16, fn="fat_attn_fwd"):
+    return getattr(lib, fn)(q, k, v, o, lse, B, H, N, d, causal, scale, X, None)
+
+
+@pytest.mark.parametrize("fn", ["fat_attn_fwd", "fat_attn_fwd_vec"])
+def test_validation_before_launch(lib, fn):
+    assert _fwd(lib, q=None, fn=fn) == fat.FAT_ERR_INVALID_ARG
+    assert _fwd(lib, lse=None, fn=fn) == fat.FAT_ERR_INVALID_ARG
+    assert _fwd(lib, d=96, fn=fn) == fat.FAT_ERR_INVALID_ARG
+    assert _fwd(lib, d=256, fn=fn) == fat.FAT_ERR_INVALID_ARG
+    assert _fwd(lib, X=8, fn=fn) == fat.FAT_ERR_INVALID_ARG
+    assert _fwd(lib, X=48, fn=fn) == fat.FAT_ERR_INVALID_ARG
+    assert _fwd(lib, N=0, fn=fn) == fat.FAT_ERR_INVALID_ARG
+    assert _fwd(lib, B=0, fn=fn) == fat.FAT_ERR_INVALID_ARG
+    assert _fwd(lib, H=-1, fn=fn) == fat.FAT_ERR_INVALID_ARG
+    assert _fwd(lib, scale=0.0, fn=fn) == fat.FAT_ERR_INVALID_ARG
+    assert _fwd(lib, scale=float("nan"), fn=fn) == fat.FAT_ERR_INVALID_ARG
+    assert _fwd(lib, scale=-1.0, fn=fn) == fat.FAT_ERR_INVALID_ARG
+    assert _fwd(lib, q=0x1001, fn=fn) == fat.FAT_ERR_ALIGNMENT
+    assert _fwd(lib, o=0x4008, fn=fn) == fat.FAT_ERR_ALIGNMENT
+    assert _fwd(lib, lse=0x5004, fn=fn) == fat.FAT_ERR_ALIGNMENT
+
+
+def test_ex_validation(lib):
+    assert lib.fat_attn_fwd_ex(None) == fat.FAT_ERR_INVALID_ARG
+    p = fat.FatParams(q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000, B=1, H=1, N=128, d=64,
+                      causal=0, scale=0.125, X=16, variant=7, dtype=0)
+    assert lib.fat_attn_fwd_ex(ctypes.byref(p)) == fat.FAT_ERR_INVALID_ARG
+    p.variant, p.dtype = 0, 9
+    assert lib.fat_attn_fwd_ex(ctypes.byref(p)) == fat.FAT_ERR_INVALID_ARG
+
+
+def test_params_struct_layout_matches_header(tmp_path):
+    """ctypes mirror of fat_params has the C compiler's size and offsets."""
+    cuda_inc = "/usr/local/cuda/include"
+    if not os.path.exists(os.path.join(cuda_inc, "cuda_runtime_api.h")):
+        pytest.skip("CUDA headers not found")
+    fields = [f[0] for f in fat.FatParams._fields_]
+    src = ['#include <stdio.h>', '#include <stddef.h>', f'#include "{HEADER}"', "int main(void){",
+           'printf("%zu\\n", sizeof(fat_params));']
+    src += [f'printf("%zu\\n", offsetof(fat_params, {f}));' for f in fields]
+    src += ["return 0;}"]
+    c = tmp_path / "layout.c"
+    c.write_text("\n".join(src))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-I", cuda_inc, "-o", str(exe), str(c)], check=True)
+    vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True,
+                                           check=True).stdout.split()]
+    assert vals[0] == ctypes.sizeof(fat.FatParams)
+    for f, off in zip(fields, vals[1:]):
+        assert getattr(fat.FatParams, f).offset == off, f
