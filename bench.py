@@ -189,7 +189,7 @@ def config_dict(w, variant):
             "l2": "flushed before every timed step (256 MiB write)"}
 
 
-def time_variant(fat, torch, w, dev, args, variant, flush, stream):
+def time_variant(fat, torch, w, dev, args, variant, flush, stream, l_mode="vector"):
     """Device time (ms) of each of args.steps launches, L2 flushed before each."""
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -202,7 +202,7 @@ def time_variant(fat, torch, w, dev, args, variant, flush, stream):
                              dev["v_descale"], w.causal, w.scale, w.X, out=out, stream=stream)
         else:
             fat.attn_fwd(dev["q"], dev["k"], dev["v"], w.causal, w.scale, w.X, variant=variant,
-                         out=out, stream=stream)
+                         out=out, stream=stream, l_mode=l_mode)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -260,8 +260,8 @@ def main():
     stream = torch.cuda.Stream(device)
     peaks = load_peaks()
 
-    def timed(variant, sample_clocks):
-        gen_ = time_variant(fat, torch, w, dev, args, variant, flush, stream)
+    def timed(variant, sample_clocks, l_mode="vector"):
+        gen_ = time_variant(fat, torch, w, dev, args, variant, flush, stream, l_mode)
         next(gen_)  # warm-up done
         if pg:
             pg.barrier()
@@ -293,9 +293,13 @@ def main():
     ablation = None
     if not args.no_ablation and w.dtype == "bf16":
         vt, _, _ = timed("vec", False)
+        lt, _, _ = timed("tensor", False, "tensor")
         v_avg = sum(vt) / len(vt)
+        l_avg = sum(lt) / len(lt)
         ablation = {"vec_value": w.flops / (v_avg * 1e-3) / 1e12, "vec_ms_per_step": v_avg,
-                    "tensor_speedup_vs_vec": v_avg / avg_ms}
+                    "tensor_speedup_vs_vec": v_avg / avg_ms,
+                    "tensor_lsum_value": w.flops / (l_avg * 1e-3) / 1e12,
+                    "tensor_lsum_ms_per_step": l_avg}
 
     # end to end through the public API with host buffers: H2D of q, k, v from
     # pinned memory, the call, D2H of o and lse, every step

@@ -56,14 +56,27 @@ typedef enum { FAT_VARIANT_TENSOR = 0, FAT_VARIANT_VEC = 1 } fat_variant;
 typedef enum { FAT_DTYPE_BF16 = 0, FAT_DTYPE_E4M3 = 1 } fat_dtype;
 
 /*
+ * Where the row sum l of Algorithm 1 step 7 is formed in the tensorized
+ * variant.  FAT_LMODE_VECTOR (default): fp32 sum of the unrounded P~ on the
+ * vector units (packed f32x2 adds).  FAT_LMODE_TENSOR: on the tensor pipe as
+ * the bf16-rounded P~ times a block of ones, plus a per-tile correction of
+ * the dominant term's rounding; O stays consistent with l, but LSE can then
+ * be off by up to ~2^-9 when a few comparable terms dominate a row.
+ */
+typedef enum { FAT_LMODE_VECTOR = 0, FAT_LMODE_TENSOR = 1 } fat_lmode;
+
+/*
  * Tensorized online softmax (section A2 of the page above).
  *   - m_hat: per X-row tile, the maximum of the row maxima seen so far
  *     (Algorithm 1 step 1), kept as an integer number of binades so that the
  *     rescale factor exp(m_hat_old - m_hat) of steps 2-3 is an exact power of
  *     two shared by the tile;
  *   - Z = log2(e) * scale * S - m_hat, P~ = exp2(Z) (steps 4-6);
- *   - the row sum l of step 7 is produced on the tensor pipe (P~ times a block
- *     of ones);
+ *   - with X = 128 the factor 2^-k is applied by the tensor pipe inside the
+ *     next O += P~ V (the MMA's input-scaling operand); otherwise O is
+ *     rescaled in tensor memory by the vector units, and only when m_hat grew;
+ *   - the row sum l of step 7 is an fp32 sum on the vector units (see
+ *     fat_lmode for the tensor-pipe alternative);
  *   - rows whose surrogate maximum exceeds their exact maximum by more than
  *     the underflow threshold (default 64 binades), or whose sum is zero,
  *     are recomputed with the exact per-row maximum (the optional fallback of
@@ -104,6 +117,7 @@ typedef struct fat_params {
   int X;
   int variant;                        /* fat_variant */
   int dtype;                          /* fat_dtype */
+  int l_mode;                         /* fat_lmode (tensorized variant only) */
   float q_descale, k_descale, v_descale; /* e4m3 only; ignored for bf16 */
   float underflow_log2_threshold;     /* <= 0: default (64 binades for bf16 P, 6 for e4m3 P) */
   int* fallback_rows;                 /* nullable device int: += number of rows recomputed */

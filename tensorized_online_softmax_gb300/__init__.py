@@ -36,6 +36,7 @@ FAT_ERR_ARCH = -6
 
 VARIANTS = {"tensor": 0, "vec": 1}
 DTYPES = {"bf16": 0, "e4m3": 1}
+LMODES = {"vector": 0, "tensor": 1}
 
 # every extern "C" entry point declared in include/fat_attn.h
 ABI_SYMBOLS = (
@@ -58,7 +59,7 @@ class FatParams(ctypes.Structure):
         ("o", ctypes.c_void_p), ("lse", ctypes.c_void_p),
         ("B", ctypes.c_int), ("H", ctypes.c_int), ("N", ctypes.c_int), ("d", ctypes.c_int),
         ("causal", ctypes.c_int), ("scale", ctypes.c_float), ("X", ctypes.c_int),
-        ("variant", ctypes.c_int), ("dtype", ctypes.c_int),
+        ("variant", ctypes.c_int), ("dtype", ctypes.c_int), ("l_mode", ctypes.c_int),
         ("q_descale", ctypes.c_float), ("k_descale", ctypes.c_float),
         ("v_descale", ctypes.c_float),
         ("underflow_log2_threshold", ctypes.c_float),
@@ -141,13 +142,16 @@ def _check_inputs(q, k, v, dtypes):
 def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, X: int = 64,
              variant: str = "tensor", *, out=None, stream=None, fallback_rows=None,
              underflow_log2_threshold: float = 0.0, wait_poll_limit: int = 0,
-             wait_timeout_ns: int = 0, dtype: str = "bf16", descales=(1.0, 1.0, 1.0)):
+             wait_timeout_ns: int = 0, dtype: str = "bf16", descales=(1.0, 1.0, 1.0),
+             l_mode: str = "vector"):
     """Fused attention forward.  Returns ``(o, lse)`` (fp32 [B,H,N,d], fp32 [B,H,N]).
 
     ``q, k, v``: contiguous CUDA tensors [B, H, N, d] (bf16, or float8_e4m3fn
     with ``dtype="e4m3"`` and per-tensor ``descales``).  ``scale`` defaults to
     1/sqrt(d).  ``fallback_rows`` is an optional int32 CUDA tensor of one
     element that the kernel increments by the number of rows it recomputed.
+    ``l_mode="tensor"`` forms the row sum on the tensor pipe (see fat_lmode in
+    include/fat_attn.h for its accuracy).
     The call is asynchronous on ``stream`` (default: torch's current stream).
     """
     import torch
@@ -172,6 +176,7 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, X: int =
     p.X = int(X)
     p.variant = VARIANTS[variant]
     p.dtype = DTYPES[dtype]
+    p.l_mode = LMODES[l_mode]
     p.q_descale, p.k_descale, p.v_descale = (float(x) for x in descales)
     p.underflow_log2_threshold = float(underflow_log2_threshold)
     p.fallback_rows = fallback_rows.data_ptr() if fallback_rows is not None else None

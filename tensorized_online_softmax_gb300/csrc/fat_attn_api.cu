@@ -19,7 +19,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceCache {
   std::once_flag once;
   int arch_ok = 0;  // 1: sm_103
-  int smem_set[4] = {0, 0, 0, 0};
+  int smem_set[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 };
 DeviceCache g_dev[kMaxDevices];
 
@@ -59,9 +59,9 @@ bool encode_qkv_map(CUtensorMap* tm, const void* ptr, int d, int N, int BH, int 
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-template <int D, bool kTensor>
+template <int D, bool kTensor, bool kLTensor>
 int launch(const fat::FwdParams& fp, int dev, int slot, int grid, cudaStream_t stream) {
-  auto kern = fat::fat_fwd_kernel<D, kTensor>;
+  auto kern = fat::fat_fwd_kernel<D, kTensor, kLTensor>;
   const int smem = fat::Smem<D>::kAlloc;
   if (!g_dev[dev].smem_set[slot]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
@@ -114,6 +114,7 @@ int fat_attn_fwd_ex(const fat_params* p) {
   if (!(p->scale > 0.f) || !std::isfinite(p->scale)) return FAT_ERR_INVALID_ARG;
   if (p->variant != FAT_VARIANT_TENSOR && p->variant != FAT_VARIANT_VEC) return FAT_ERR_INVALID_ARG;
   if (p->dtype != FAT_DTYPE_BF16 && p->dtype != FAT_DTYPE_E4M3) return FAT_ERR_INVALID_ARG;
+  if (p->l_mode != FAT_LMODE_VECTOR && p->l_mode != FAT_LMODE_TENSOR) return FAT_ERR_INVALID_ARG;
   const long long BH = static_cast<long long>(p->B) * p->H;
   const long long n_mblocks = (p->N + fat::kRowsPerCta - 1) / fat::kRowsPerCta;
   if (BH > (1ll << 30) || BH * n_mblocks > 0x7fffffffll) return FAT_ERR_INVALID_ARG;
@@ -149,11 +150,15 @@ int fat_attn_fwd_ex(const fat_params* p) {
 
   const int grid = static_cast<int>(BH * n_mblocks);
   const bool tensor = p->variant == FAT_VARIANT_TENSOR;
-  if (p->d == 128)
-    return tensor ? launch<128, true>(fp, dev, 0, grid, p->stream)
-                  : launch<128, false>(fp, dev, 1, grid, p->stream);
-  return tensor ? launch<64, true>(fp, dev, 2, grid, p->stream)
-                : launch<64, false>(fp, dev, 3, grid, p->stream);
+  const bool l_tensor = p->l_mode == FAT_LMODE_TENSOR;
+  if (p->d == 128) {
+    if (!tensor) return launch<128, false, false>(fp, dev, 0, grid, p->stream);
+    return l_tensor ? launch<128, true, true>(fp, dev, 1, grid, p->stream)
+                    : launch<128, true, false>(fp, dev, 2, grid, p->stream);
+  }
+  if (!tensor) return launch<64, false, false>(fp, dev, 3, grid, p->stream);
+  return l_tensor ? launch<64, true, true>(fp, dev, 4, grid, p->stream)
+                  : launch<64, true, false>(fp, dev, 5, grid, p->stream);
 }
 
 static int fwd_common(const void* q, const void* k, const void* v, float* o, float* lse, int B,

@@ -80,7 +80,7 @@ struct Smem {
   static constexpr int bDrain = bOFinal + 1;
   static constexpr int kNumBars = bDrain + 1;
   static constexpr int kRed = kBars + 8 * kNumBars;  // float [2 tiles][2 parity][4 warps]
-  static constexpr int kMisc = kRed + 64;            // u32: tmem base, abort, redo
+  static constexpr int kMisc = kRed + 64;  // u32: tmem base, abort, redo, -, pv scale[2]
   static constexpr int kBytes = kMisc + 64;
   static constexpr int kAlloc = kBytes + 1024;       // slack for 1024-byte alignment
   static_assert(kK % 1024 == 0 && kV % 1024 == 0 && kOnes % 1024 == 0, "tiles 1 KB aligned");
@@ -123,7 +123,12 @@ __device__ __forceinline__ float bf16_round(float x) {
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-template <int D, bool kTensor>
+// kTensor:  surrogate maximum over X-row tiles (Algorithm 1); otherwise the
+//           exact per-row maximum (vector-softmax ablation).
+// kLTensor: (kTensor only) the row sum of step 7 on the tensor pipe as
+//           P~ (bf16) times a block of ones; otherwise an fp32 sum of the
+//           unrounded P~ on the vector units.
+template <int D, bool kTensor, bool kLTensor>
 __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = Smem<D>;
   constexpr int S = L::kStages;
@@ -165,6 +170,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
     mbar_init(bar(L::bDrain), 1);
     misc[1] = 0;
     misc[2] = 0;
+    misc[4] = 0;
+    misc[5] = 0;
     fence_mbar_init();
   }
   if (threadIdx.x < 256) {  // the ones tile used as B of the row-sum MMA
@@ -241,13 +248,21 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
                           sdesc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
           }
         };
-        auto issue_pv = [&](int t, int st, bool acc) {
+        // O_t (+)= P_t V; with kscale > 0 the first K step also applies the
+        // uniform rescale O_t <- 2^-kscale O_t of Algorithm 1 steps 2-3.
+        auto issue_pv = [&](int t, int st, bool acc, int kscale) {
           const uint32_t va = sb + L::kV + st * L::kTile;
 #pragma unroll
-          for (int kk = 0; kk < kBlockN / 16; ++kk)
-            mma_ts<false>(tmem + 2 * kBlockN + t * D, tmem + t * kBlockN + kk * 8,
-                          sdesc_sw128(va + kk * 2048, 16384, 1024), idesc_pv, acc || kk > 0);
+          for (int kk = 0; kk < kBlockN / 16; ++kk) {
+            const uint32_t d_t = tmem + 2 * kBlockN + t * D, a_t = tmem + t * kBlockN + kk * 8;
+            const uint64_t bd = sdesc_sw128(va + kk * 2048, 16384, 1024);
+            if (kk == 0 && acc && kscale > 0)
+              mma_ts_scale_rt(d_t, a_t, bd, idesc_pv, kscale);
+            else
+              mma_ts<false>(d_t, a_t, bd, idesc_pv, acc || kk > 0);
+          }
         };
+        volatile uint32_t* pv_scale = misc + 4;
         auto issue_rs = [&](int t) {
 #pragma unroll
           for (int kk = 0; kk < kBlockN / 16; ++kk)
@@ -278,14 +293,15 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
           // tile 0
           if (!(ok = wait_bounded(bar(L::bPFull + 0), par, p, abort_flag))) break;
           tc_fence_after();
-          if (tensor_pass) {
+          if (kLTensor && tensor_pass) {
             issue_rs(0);
             mma_commit(bar(L::bRsFull + 0));
           }
-          issue_pv(0, st, j > 0);
+          issue_pv(0, st, j > 0, tensor_pass ? static_cast<int>(pv_scale[0]) : 0);
           if (more) {
             if (!(ok = wait_bounded(bar(L::bKFull + st1), ph1, p, abort_flag))) break;
-            if (tensor_pass && !(ok = wait_bounded(bar(L::bLFree + 0), par, p, abort_flag))) break;
+            if (kLTensor && tensor_pass && !(ok = wait_bounded(bar(L::bLFree + 0), par, p, abort_flag)))
+              break;
             tc_fence_after();
             issue_s(0, st1);
             mma_commit(bar(L::bSFull + 0));
@@ -293,14 +309,15 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
           // tile 1
           if (!(ok = wait_bounded(bar(L::bPFull + 1), par, p, abort_flag))) break;
           tc_fence_after();
-          if (tensor_pass) {
+          if (kLTensor && tensor_pass) {
             issue_rs(1);
             mma_commit(bar(L::bRsFull + 1));
           }
-          issue_pv(1, st, j > 0);
+          issue_pv(1, st, j > 0, tensor_pass ? static_cast<int>(pv_scale[1]) : 0);
           mma_commit(bar(L::bVEmpty + st));
           if (more) {
-            if (tensor_pass && !(ok = wait_bounded(bar(L::bLFree + 1), par, p, abort_flag))) break;
+            if (kLTensor && tensor_pass && !(ok = wait_bounded(bar(L::bLFree + 1), par, p, abort_flag)))
+              break;
             tc_fence_after();
             issue_s(1, st1);
             mma_commit(bar(L::bSFull + 1));
@@ -361,7 +378,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
 #pragma unroll
         for (int k = 0; k < 4; ++k)
 #pragma unroll
-          for (int i = 0; i < 32; ++i) rowmax = fmaxf(rowmax, __uint_as_float(s[k][i]));
+          for (int i = 0; i < 32; i += 2)
+            rowmax = fmax3(rowmax, __uint_as_float(s[k][i]), __uint_as_float(s[k][i + 1]));
         m_row = fmaxf(m_row, rowmax);
 
         float M_new;
@@ -396,36 +414,59 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
         const float alpha = (M_new == -INFINITY) ? 1.f : ex2_approx(M - M_new);
         if (j > 0) {
           l *= alpha;
-          delta *= alpha;
+          if (kLTensor) delta *= alpha;
+        }
+        // With X = 128 the whole 128-row tile shares the factor 2^-k, and the
+        // tensor pipe applies it inside the next O += P V (scale-input-d);
+        // other cases rescale O in TMEM from the vector side below.
+        bool vec_rescale = grow;
+        if (tensor_pass && X == 128) {
+          int kscale = 0;
+          if (grow && M_new - M <= 15.f) {
+            kscale = static_cast<int>(M_new - M);
+            vec_rescale = false;
+          }
+          if (wq == 0 && lane == 0) misc[4 + t] = static_cast<uint32_t>(kscale);
         }
         M = M_new;
         const float neg_M = (M == -INFINITY) ? 0.f : -M;
 
         // steps 4-6: Z = c S - m_hat, P~ = exp2(Z), stored as bf16 over S
-        float rowsum = 0.f;
+        const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(neg_M, neg_M);
+        uint64_t acc2 = f2_pack(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(s[k][2 * i]), c, neg_M));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(s[k][2 * i + 1]), c, neg_M));
-            if (!tensor_pass) rowsum += p0 + p1;
+            const uint64_t z = f2_fma(f2_pack(__uint_as_float(s[k][2 * i]),
+                                              __uint_as_float(s[k][2 * i + 1])), c2, nm2);
+            float z0, z1;
+            f2_unpack(z, z0, z1);
+            const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
+            if (!(kLTensor && tensor_pass)) acc2 = f2_add(acc2, f2_pack(p0, p1));
             pk[i] = pack_bf16x2(p0, p1);
           }
           tmem_st16(s_taddr + 16 * k, pk);
         }
-        // steps 2-3: O <- alpha O in TMEM.  PV_{j-1} has completed (it was
-        // issued before S_j, whose completion we waited for) and PV_j waits
-        // for this warpgroup's P-full signal below.
-        if (__any_sync(0xffffffffu, grow)) {
+        // steps 2-3 on the vector side: O <- alpha O in TMEM.  PV_{j-1} has
+        // completed (issued before S_j, whose completion we waited for) and
+        // PV_j waits for this warpgroup's P-full signal below.
+        if (__any_sync(0xffffffffu, vec_rescale)) {
+          const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
           for (int k = 0; k < D / 32; ++k) {
             uint32_t ov[32];
             tmem_ld32(o_taddr + 32 * k, ov);
             tmem_wait_ld(ov);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+            for (int i = 0; i < 32; i += 2) {
+              float o0, o1;
+              f2_unpack(f2_mul(f2_pack(__uint_as_float(ov[i]), __uint_as_float(ov[i + 1])), a2),
+                        o0, o1);
+              ov[i] = __float_as_uint(o0);
+              ov[i + 1] = __float_as_uint(o1);
+            }
             tmem_st32(o_taddr + 32 * k, ov);
           }
         }
@@ -434,7 +475,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(L::bPFull + t));
 
-        if (tensor_pass) {
+        if (kLTensor && tensor_pass) {
           // step 7: the row sum comes from the tensor pipe (P~ times ones);
           // the LSE also gets back the bf16 rounding of the dominant term.
           if (rowmax != -INFINITY) {
@@ -452,7 +493,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
           if (lane == 0) mbar_arrive(bar(L::bLFree + t));
           l += __uint_as_float(lt);
         } else {
-          l += rowsum;
+          float r0, r1;
+          f2_unpack(acc2, r0, r1);
+          l += r0 + r1;
         }
       }
 
@@ -488,7 +531,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
           }
         }
         if (row_g < p.N) {
-          const float lsum = tensor_pass ? l + delta : l;
+          const float lsum = (kLTensor && tensor_pass) ? l + delta : l;
           p.lse[static_cast<size_t>(bh) * p.N + row_g] = (M + __log2f(lsum)) * kLn2;
         }
       }

@@ -161,6 +161,32 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
   }
 }
 
+// D[tmem] = A[tmem] * B[smem]^T + 2^-kScale * D[tmem]   (kind::f16 only; the
+// optional scale-input-d operand, 1 <= kScale <= 15)
+template <int kScale>
+__device__ __forceinline__ void mma_ts_scaled(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                              uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, 1, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p, %4;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "n"(kScale)
+      : "memory");
+}
+
+// Runtime-selected scale 1..15 (a jump table over the immediates).
+__device__ __forceinline__ void mma_ts_scale_rt(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                                uint32_t idesc, int k) {
+  switch (k) {
+#define FAT_SCALE_CASE(n) \
+  case n: mma_ts_scaled<n>(d_tmem, a_tmem, bdesc, idesc); break;
+    FAT_SCALE_CASE(1) FAT_SCALE_CASE(2) FAT_SCALE_CASE(3) FAT_SCALE_CASE(4) FAT_SCALE_CASE(5)
+    FAT_SCALE_CASE(6) FAT_SCALE_CASE(7) FAT_SCALE_CASE(8) FAT_SCALE_CASE(9) FAT_SCALE_CASE(10)
+    FAT_SCALE_CASE(11) FAT_SCALE_CASE(12) FAT_SCALE_CASE(13) FAT_SCALE_CASE(14) FAT_SCALE_CASE(15)
+#undef FAT_SCALE_CASE
+    default: break;
+  }
+}
+
 // Arrive (once) on an mbarrier when every tcgen05 operation this thread issued
 // before has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -239,6 +265,37 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Packed fp32 pairs (Blackwell f32x2 ALU forms).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// max of three floats in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
