@@ -64,6 +64,12 @@ int launch(const fat::FwdParams& fp, int dev, int slot, int grid, cudaStream_t s
   auto kern = fat::fat_fwd_kernel<D, kTensor, kLTensor>;
   const int smem = fat::Smem<D>::kAlloc;
   if (!g_dev[dev].smem_set[slot]) {
+    // The warpgroup register split inside the kernel assumes exactly
+    // kLaunchRegs registers per thread at launch; anything else could make
+    // the register increase wait forever, so refuse to launch.
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs != fat::kLaunchRegs)
+      return FAT_ERR_LAUNCH;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
         cudaSuccess)
       return FAT_ERR_LAUNCH;

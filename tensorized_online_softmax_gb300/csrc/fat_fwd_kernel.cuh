@@ -28,8 +28,16 @@ constexpr int kBlockM = 128;  // query rows per tile (= TMEM lanes)
 constexpr int kBlockN = 128;  // keys per K/V tile
 constexpr int kRowsPerCta = 2 * kBlockM;
 constexpr int kMmaWarp = 8;
-constexpr int kLoadWarp = 9;
-constexpr int kNumThreads = 320;
+constexpr int kLoadWarp = 9;   // warps 10, 11 complete the third warpgroup
+constexpr int kNumThreads = 384;
+// Register budget: 384 threads launch with kLaunchRegs each; the MMA/TMA
+// warpgroup drops to kCtrlRegs and the two softmax warpgroups rise to
+// kSoftmaxRegs.  256 * kSoftmaxRegs + 128 * kCtrlRegs <= 384 * kLaunchRegs.
+constexpr int kLaunchRegs = 168;
+constexpr int kCtrlRegs = 64;
+constexpr int kSoftmaxRegs = 216;
+static_assert(256 * kSoftmaxRegs + 128 * kCtrlRegs <= kNumThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -121,6 +129,267 @@ __device__ __forceinline__ float bf16_round(float x) {
 }
 
 // ---------------------------------------------------------------------------
+// softmax warpgroups: warpgroup t owns query tile t; thread i owns row i
+// (TMEM lane i).  kTensorPass selects the tensorized online softmax (surrogate
+// maximum over X-row tiles); otherwise the exact per-row maximum.
+// ---------------------------------------------------------------------------
+template <int D, bool kTensorPass, bool kLTensor>
+__device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, uint32_t sb,
+                                             uint32_t tmem, volatile uint32_t* misc, int warp,
+                                             int lane, int m0, int bh, int n_kv, int it0,
+                                             int pass) {
+  using L = Smem<D>;
+  constexpr bool tensor_pass = kTensorPass;
+  volatile uint32_t* abort_flag = misc + 1;
+  auto bar = [&](int i) -> uint32_t { return sb + L::kBars + 8 * i; };
+    const int t = warp >> 2;        // tile
+    const int wq = warp & 3;        // quarter of the tile (TMEM lanes 32*wq ..)
+    const int r = wq * 32 + lane;   // row within the tile
+    const int row_g = m0 + t * kBlockM + r;
+    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+    const uint32_t s_taddr = tmem + lane_base + t * kBlockN;
+    const uint32_t o_taddr = tmem + lane_base + 2 * kBlockN + t * D;
+    const float c = p.c;
+    const int X = p.X;
+    float* red = reinterpret_cast<float*>(smem + L::kRed);
+
+    float M = -INFINITY;      // offset of the exponent, binades (exact row max * c in vec mode)
+    float m_row = -INFINITY;  // exact running row maximum, raw logits
+    float l = 0.f;            // running row sum
+    float delta = 0.f;        // tensorized: rounding of each tile's dominant term
+    // A warp whose bounded wait ran out turns "dead": it stops touching TMEM
+    // and barriers of the pipeline, but keeps joining the named barrier of
+    // its X-row group every iteration, so no other warp can be left waiting
+    // there; the OR on that barrier spreads the abort to the whole group.
+    bool dead = false;
+    const bool group_exchange = tensor_pass && X > 32;
+    const uint32_t gbar_id = 1 + 4 * t + (X == 64 ? (wq >> 1) : 0);
+    const uint32_t gbar_n = X == 64 ? 64 : 128;
+
+    for (int j = 0; j < n_kv; ++j) {
+      const int it = it0 + j;
+      const uint32_t par = it & 1;
+      if (!dead)
+        dead = !__all_sync(0xffffffffu, wait_bounded(bar(L::bSFull + t), par, p, abort_flag));
+      uint32_t s[4][32];
+      float rowmax = -INFINITY, tmax = -INFINITY;
+      if (!dead) {
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) tmem_ld32(s_taddr + 32 * k, s[k]);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) tmem_wait_ld(s[k]);
+
+        // mask: keys >= N, keys after the query (causal), padding rows
+        const int kv0 = j * kBlockN;
+        const int limit = (row_g < p.N) ? (p.causal ? min(p.N, row_g + 1) : p.N) - kv0 : 0;
+        if (limit < kBlockN) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (32 * k + i >= limit) s[k][i] = __float_as_uint(-INFINITY);
+        }
+        // row maximum as a tree of independent 3-input maxima
+        float mx[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a)
+          mx[a] = fmax3(__uint_as_float(s[a >> 1][(a & 1) * 16]),
+                        __uint_as_float(s[a >> 1][(a & 1) * 16 + 1]),
+                        __uint_as_float(s[a >> 1][(a & 1) * 16 + 2]));
+#pragma unroll
+        for (int a = 0; a < 8; ++a) {
+          const int k = a >> 1, b = (a & 1) * 16;
+#pragma unroll
+          for (int i = 3; i < 15; i += 2)
+            mx[a] = fmax3(mx[a], __uint_as_float(s[k][b + i]), __uint_as_float(s[k][b + i + 1]));
+          mx[a] = fmaxf(mx[a], __uint_as_float(s[k][b + 15]));
+        }
+        rowmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7])));
+        m_row = fmaxf(m_row, rowmax);
+        if (tensor_pass) {
+          // Algorithm 1 step 1, within the warp: max of the row maxima over
+          // the X-row tile (X = 16: half warps; X >= 32: the whole warp)
+          if (X == 16) {
+            tmax = rowmax;
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+          } else {
+            tmax = warp_max(rowmax);
+          }
+        }
+      }
+      if (group_exchange) {
+        // X = 64 / 128: combine the warps of the X-row group
+        float* slot = red + (t * 2 + par) * 4;
+        if (lane == 0) slot[wq] = tmax;
+        dead = named_bar_or(gbar_id, gbar_n, dead);
+        if (!dead) {
+          const int g0 = (X == 64) ? (wq & 2) : 0;
+          tmax = fmaxf(tmax, fmaxf(slot[g0], slot[g0 + 1]));
+          if (X == 128) tmax = fmaxf(tmax, fmaxf(slot[2], slot[3]));
+        }
+      }
+      if (dead) {
+        if (group_exchange) continue;
+        break;
+      }
+
+      float M_new;
+      if (tensor_pass) {
+        // the surrogate maximum is kept as a whole number of binades so the
+        // rescale factor of steps 2-3 is an exact power of two
+        const float Mc = (tmax == -INFINITY) ? -INFINITY : ceilf(tmax * c);
+        M_new = fmaxf(M, Mc);
+      } else {
+        M_new = (m_row == -INFINITY) ? -INFINITY : m_row * c;
+      }
+
+      // Algorithm 1 steps 2-3 factor: exp(m_old - m_new), one exact power
+      // of two per X-row tile (exact per-row factor in the vector variant).
+      const bool grow = j > 0 && M_new > M;
+      const float alpha = (M_new == -INFINITY) ? 1.f : ex2_approx(M - M_new);
+      if (j > 0) {
+        l *= alpha;
+        if (kLTensor) delta *= alpha;
+      }
+      // With X = 128 the whole 128-row tile shares the factor 2^-k, and the
+      // tensor pipe applies it inside the next O += P V (scale-input-d);
+      // other cases rescale O in TMEM from the vector side below.
+      bool vec_rescale = grow;
+      if (tensor_pass && X == 128) {
+        int kscale = 0;
+        if (grow && M_new - M <= 15.f) {
+          kscale = static_cast<int>(M_new - M);
+          vec_rescale = false;
+        }
+        if (wq == 0 && lane == 0) misc[4 + t] = static_cast<uint32_t>(kscale);
+      }
+      M = M_new;
+      const float neg_M = (M == -INFINITY) ? 0.f : -M;
+
+      // steps 4-6: Z = c S - m_hat, P~ = exp2(Z), stored as bf16 over S
+      const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(neg_M, neg_M);
+      uint64_t acc2[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) acc2[a] = f2_pack(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint64_t z = f2_fma(f2_pack(__uint_as_float(s[k][2 * i]),
+                                            __uint_as_float(s[k][2 * i + 1])), c2, nm2);
+          float z0, z1;
+          f2_unpack(z, z0, z1);
+          const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
+          if (!(kLTensor && tensor_pass)) acc2[i & 3] = f2_add(acc2[i & 3], f2_pack(p0, p1));
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(s_taddr + 16 * k, pk);
+      }
+      // steps 2-3 on the vector side: O <- alpha O in TMEM.  PV_{j-1} has
+      // completed (issued before S_j, whose completion we waited for) and
+      // PV_j waits for this warpgroup's P-full signal below.
+      if (__any_sync(0xffffffffu, vec_rescale)) {
+        const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k) {
+          uint32_t ov[32];
+          tmem_ld32(o_taddr + 32 * k, ov);
+          tmem_wait_ld(ov);
+#pragma unroll
+          for (int i = 0; i < 32; i += 2) {
+            float o0, o1;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(ov[i]), __uint_as_float(ov[i + 1])), a2),
+                      o0, o1);
+            ov[i] = __float_as_uint(o0);
+            ov[i + 1] = __float_as_uint(o1);
+          }
+          tmem_st32(o_taddr + 32 * k, ov);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::bPFull + t));
+
+      if (kLTensor && tensor_pass) {
+        // step 7: the row sum comes from the tensor pipe (P~ times ones);
+        // the LSE also gets back the bf16 rounding of the dominant term.
+        if (rowmax != -INFINITY) {
+          const float pm = ex2_approx(fmaf(rowmax, c, neg_M));
+          delta += pm - bf16_round(pm);
+        }
+        dead = !__all_sync(0xffffffffu, wait_bounded(bar(L::bRsFull + t), par, p, abort_flag));
+        if (dead) continue;
+        tc_fence_after();
+        uint32_t lt;
+        tmem_ld1(s_taddr + 64, lt);
+        tmem_wait_ld1(lt);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(L::bLFree + t));
+        l += __uint_as_float(lt);
+      } else {
+        float r0, r1;
+        f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), r0, r1);
+        l += r0 + r1;
+      }
+    }
+    bool ok = !dead;
+
+    if (ok) ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bOFinal), pass & 1, p, abort_flag));
+    if (ok) {
+      tc_fence_after();
+      // detector for the all-underflow case: surrogate far above the exact
+      // maximum, or nothing left of the row sum
+      if (tensor_pass) {
+        const bool flagged =
+            row_g < p.N && (!(l > 0.f) || (M - m_row * c) > p.underflow_thresh);
+        const uint32_t ball = __ballot_sync(0xffffffffu, flagged);
+        if (ball != 0 && lane == 0) {
+          atomicOr(const_cast<uint32_t*>(misc + 2), 1u);
+          if (p.fallback_rows) atomicAdd(p.fallback_rows, __popc(ball));
+        }
+      }
+      // epilogue: O / l and LSE
+      const float inv_l = 1.f / l;
+      float* orow = p.o + (static_cast<size_t>(bh) * p.N + row_g) * D;
+#pragma unroll
+      for (int k = 0; k < D / 32; ++k) {
+        uint32_t ov[32];
+        tmem_ld32(o_taddr + 32 * k, ov);
+        tmem_wait_ld(ov);
+        if (row_g < p.N) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            float4 v4 = make_float4(__uint_as_float(ov[i]) * inv_l, __uint_as_float(ov[i + 1]) * inv_l,
+                                    __uint_as_float(ov[i + 2]) * inv_l, __uint_as_float(ov[i + 3]) * inv_l);
+            *reinterpret_cast<float4*>(orow + 32 * k + i) = v4;
+          }
+        }
+      }
+      if (row_g < p.N) {
+        const float lsum = (kLTensor && tensor_pass) ? l + delta : l;
+        p.lse[static_cast<size_t>(bh) * p.N + row_g] = (M + __log2f(lsum)) * kLn2;
+      }
+    }
+    tc_fence_before();
+}
+
+// The exact-maximum recomputation that follows a flagged tensorized pass is
+// rare; as a separate (not inlined) function its registers do not weigh on
+// the hot tensorized loop.
+template <int D>
+__device__ __noinline__ void softmax_role_fallback(const FwdParams& p, uint8_t* smem, uint32_t sb,
+                                                   uint32_t tmem, volatile uint32_t* misc,
+                                                   int warp, int lane, int m0, int bh, int n_kv,
+                                                   int it0, int pass) {
+  softmax_role<D, false, false>(p, smem, sb, tmem, misc, warp, lane, m0, bh, n_kv, it0, pass);
+}
+
+// ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
 // kTensor:  surrogate maximum over X-row tiles (Algorithm 1); otherwise the
@@ -187,366 +456,185 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
   tc_fence_after();
   const uint32_t tmem = misc[0];
 
-  for (int pass = 0; pass < 2; ++pass) {
-    const bool tensor_pass = kTensor && pass == 0;
-    const int it0 = pass * n_kv;
-
-    if (warp == kLoadWarp) {
-      // =================== TMA producer ===================
-      if (lane == 0) {
-        int k_issued = 0, v_issued = 0;
-        if (pass == 0) {
-          tma_prefetch_desc(&p.tm_q);
-          tma_prefetch_desc(&p.tm_k);
-          tma_prefetch_desc(&p.tm_v);
-          mbar_arrive_expect_tx(bar(L::bQFull), 2 * L::kTile);
-          for (int t = 0; t < 2; ++t)
+  // Registers: the control warpgroup (TMA, MMA) gives registers back and the
+  // softmax warpgroups take them.  Each role runs its own loop over the
+  // passes so that no code is shared between the two register budgets.
+  if (warp >= kMmaWarp) {
+    regs_dec<kCtrlRegs>();
+    for (int pass = 0; pass < 2; ++pass) {
+      const bool tensor_pass = kTensor && pass == 0;
+      const int it0 = pass * n_kv;
+      if (warp == kLoadWarp) {
+        // =================== TMA producer ===================
+        if (lane == 0) {
+          int k_issued = 0, v_issued = 0;
+          if (pass == 0) {
+            tma_prefetch_desc(&p.tm_q);
+            tma_prefetch_desc(&p.tm_k);
+            tma_prefetch_desc(&p.tm_v);
+            mbar_arrive_expect_tx(bar(L::bQFull), 2 * L::kTile);
+            for (int t = 0; t < 2; ++t)
+              for (int a = 0; a < L::kAtoms; ++a)
+                tma_load_3d(sb + L::kQ + t * L::kTile + a * 16384, &p.tm_q, bar(L::bQFull), a * 64,
+                            m0 + t * kBlockM, bh);
+          }
+          for (int j = 0; j < n_kv; ++j) {
+            const int it = it0 + j, st = it % S;
+            const uint32_t ph = (it / S) & 1;
+            if (!wait_bounded(bar(L::bKEmpty + st), ph ^ 1, p, abort_flag)) break;
+            mbar_arrive_expect_tx(bar(L::bKFull + st), L::kTile);
             for (int a = 0; a < L::kAtoms; ++a)
-              tma_load_3d(sb + L::kQ + t * L::kTile + a * 16384, &p.tm_q, bar(L::bQFull), a * 64,
-                          m0 + t * kBlockM, bh);
-        }
-        for (int j = 0; j < n_kv; ++j) {
-          const int it = it0 + j, st = it % S;
-          const uint32_t ph = (it / S) & 1;
-          if (!wait_bounded(bar(L::bKEmpty + st), ph ^ 1, p, abort_flag)) break;
-          mbar_arrive_expect_tx(bar(L::bKFull + st), L::kTile);
-          for (int a = 0; a < L::kAtoms; ++a)
-            tma_load_3d(sb + L::kK + st * L::kTile + a * 16384, &p.tm_k, bar(L::bKFull + st),
-                        a * 64, j * kBlockN, bh);
-          k_issued = j + 1;
-          if (!wait_bounded(bar(L::bVEmpty + st), ph ^ 1, p, abort_flag)) break;
-          mbar_arrive_expect_tx(bar(L::bVFull + st), L::kTile);
-          for (int a = 0; a < L::kAtoms; ++a)
-            tma_load_3d(sb + L::kV + st * L::kTile + a * 16384, &p.tm_v, bar(L::bVFull + st),
-                        a * 64, j * kBlockN, bh);
-          v_issued = j + 1;
-        }
-        if (*abort_flag) {
-          // let every copy already issued land before the CTA can exit
-          if (pass == 0) wait_drain(bar(L::bQFull), 0);
-          for (int j = max(0, k_issued - S); j < k_issued; ++j)
-            wait_drain(bar(L::bKFull + (it0 + j) % S), ((it0 + j) / S) & 1);
-          for (int j = max(0, v_issued - S); j < v_issued; ++j)
-            wait_drain(bar(L::bVFull + (it0 + j) % S), ((it0 + j) / S) & 1);
-        }
-      }
-      __syncwarp();
-    } else if (warp == kMmaWarp) {
-      // =================== MMA issuer ===================
-      if (lane == 0) {
-        constexpr uint32_t idesc_s = idesc_f32acc<false>(kBlockM, kBlockN, false);
-        constexpr uint32_t idesc_pv = idesc_f32acc<false>(kBlockM, D, true);
-        constexpr uint32_t idesc_rs = idesc_f32acc<false>(kBlockM, 16, false);
-        const uint64_t ones_desc = sdesc_sw128(sb + L::kOnes, 16, 1024);
-        bool ok = true;
-        auto issue_s = [&](int t, int st) {
-          const uint32_t qa = sb + L::kQ + t * L::kTile, ka = sb + L::kK + st * L::kTile;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_ss<false>(tmem + t * kBlockN, sdesc_sw128(qa + off, 16, 1024),
-                          sdesc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
+              tma_load_3d(sb + L::kK + st * L::kTile + a * 16384, &p.tm_k, bar(L::bKFull + st),
+                          a * 64, j * kBlockN, bh);
+            k_issued = j + 1;
+            if (!wait_bounded(bar(L::bVEmpty + st), ph ^ 1, p, abort_flag)) break;
+            mbar_arrive_expect_tx(bar(L::bVFull + st), L::kTile);
+            for (int a = 0; a < L::kAtoms; ++a)
+              tma_load_3d(sb + L::kV + st * L::kTile + a * 16384, &p.tm_v, bar(L::bVFull + st),
+                          a * 64, j * kBlockN, bh);
+            v_issued = j + 1;
           }
-        };
-        // O_t (+)= P_t V; with kscale > 0 the first K step also applies the
-        // uniform rescale O_t <- 2^-kscale O_t of Algorithm 1 steps 2-3.
-        auto issue_pv = [&](int t, int st, bool acc, int kscale) {
-          const uint32_t va = sb + L::kV + st * L::kTile;
-#pragma unroll
-          for (int kk = 0; kk < kBlockN / 16; ++kk) {
-            const uint32_t d_t = tmem + 2 * kBlockN + t * D, a_t = tmem + t * kBlockN + kk * 8;
-            const uint64_t bd = sdesc_sw128(va + kk * 2048, 16384, 1024);
-            if (kk == 0 && acc && kscale > 0)
-              mma_ts_scale_rt(d_t, a_t, bd, idesc_pv, kscale);
-            else
-              mma_ts<false>(d_t, a_t, bd, idesc_pv, acc || kk > 0);
-          }
-        };
-        volatile uint32_t* pv_scale = misc + 4;
-        auto issue_rs = [&](int t) {
-#pragma unroll
-          for (int kk = 0; kk < kBlockN / 16; ++kk)
-            mma_ts<false>(tmem + t * kBlockN + 64, tmem + t * kBlockN + kk * 8, ones_desc, idesc_rs,
-                          kk > 0);
-        };
-
-        if (pass == 0) ok = wait_bounded(bar(L::bQFull), 0, p, abort_flag);
-        if (ok) {
-          const int st = it0 % S;
-          ok = wait_bounded(bar(L::bKFull + st), (it0 / S) & 1, p, abort_flag);
-          if (ok) {
-            tc_fence_after();
-            issue_s(0, st);
-            mma_commit(bar(L::bSFull + 0));
-            issue_s(1, st);
-            mma_commit(bar(L::bSFull + 1));
-            mma_commit(bar(L::bKEmpty + st));
+          if (*abort_flag) {
+            // let every copy already issued land before the CTA can exit
+            if (pass == 0) wait_drain(bar(L::bQFull), 0);
+            for (int j = max(0, k_issued - S); j < k_issued; ++j)
+              wait_drain(bar(L::bKFull + (it0 + j) % S), ((it0 + j) / S) & 1);
+            for (int j = max(0, v_issued - S); j < v_issued; ++j)
+              wait_drain(bar(L::bVFull + (it0 + j) % S), ((it0 + j) / S) & 1);
           }
         }
-        for (int j = 0; ok && j < n_kv; ++j) {
-          const int it = it0 + j, st = it % S;
-          const uint32_t ph = (it / S) & 1, par = it & 1;
-          const bool more = j + 1 < n_kv;
-          const int st1 = (it + 1) % S;
-          const uint32_t ph1 = ((it + 1) / S) & 1;
-          if (!(ok = wait_bounded(bar(L::bVFull + st), ph, p, abort_flag))) break;
-          // tile 0
-          if (!(ok = wait_bounded(bar(L::bPFull + 0), par, p, abort_flag))) break;
-          tc_fence_after();
-          if (kLTensor && tensor_pass) {
-            issue_rs(0);
-            mma_commit(bar(L::bRsFull + 0));
-          }
-          issue_pv(0, st, j > 0, tensor_pass ? static_cast<int>(pv_scale[0]) : 0);
-          if (more) {
-            if (!(ok = wait_bounded(bar(L::bKFull + st1), ph1, p, abort_flag))) break;
-            if (kLTensor && tensor_pass && !(ok = wait_bounded(bar(L::bLFree + 0), par, p, abort_flag)))
-              break;
-            tc_fence_after();
-            issue_s(0, st1);
-            mma_commit(bar(L::bSFull + 0));
-          }
-          // tile 1
-          if (!(ok = wait_bounded(bar(L::bPFull + 1), par, p, abort_flag))) break;
-          tc_fence_after();
-          if (kLTensor && tensor_pass) {
-            issue_rs(1);
-            mma_commit(bar(L::bRsFull + 1));
-          }
-          issue_pv(1, st, j > 0, tensor_pass ? static_cast<int>(pv_scale[1]) : 0);
-          mma_commit(bar(L::bVEmpty + st));
-          if (more) {
-            if (kLTensor && tensor_pass && !(ok = wait_bounded(bar(L::bLFree + 1), par, p, abort_flag)))
-              break;
-            tc_fence_after();
-            issue_s(1, st1);
-            mma_commit(bar(L::bSFull + 1));
-            mma_commit(bar(L::bKEmpty + st1));
-          }
-        }
-        if (ok) {
-          mma_commit(bar(L::bOFinal));
-        } else {
-          // every MMA issued so far must finish before TMEM can be released
-          mma_commit(bar(L::bDrain));
-          wait_drain(bar(L::bDrain), 0);
-        }
-      }
-      __syncwarp();
-    } else {
-      // =================== softmax warpgroups ===================
-      const int t = warp >> 2;        // tile
-      const int wq = warp & 3;        // quarter of the tile (TMEM lanes 32*wq ..)
-      const int r = wq * 32 + lane;   // row within the tile
-      const int row_g = m0 + t * kBlockM + r;
-      const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-      const uint32_t s_taddr = tmem + lane_base + t * kBlockN;
-      const uint32_t o_taddr = tmem + lane_base + 2 * kBlockN + t * D;
-      const float c = p.c;
-      const int X = p.X;
-      float* red = reinterpret_cast<float*>(smem + L::kRed);
-
-      float M = -INFINITY;      // offset of the exponent, binades (exact row max * c in vec mode)
-      float m_row = -INFINITY;  // exact running row maximum, raw logits
-      float l = 0.f;            // running row sum
-      float delta = 0.f;        // tensorized: rounding of each tile's dominant term
-      bool ok = true;
-
-      for (int j = 0; j < n_kv; ++j) {
-        const int it = it0 + j;
-        const uint32_t par = it & 1;
-        ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bSFull + t), par, p, abort_flag));
-        if (!ok) break;
-        tc_fence_after();
-        uint32_t s[4][32];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) tmem_ld32(s_taddr + 32 * k, s[k]);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) tmem_wait_ld(s[k]);
-
-        // mask: keys >= N, keys after the query (causal), padding rows
-        const int kv0 = j * kBlockN;
-        int limit = (row_g < p.N) ? (p.causal ? min(p.N, row_g + 1) : p.N) - kv0 : 0;
-        if (limit < kBlockN) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (32 * k + i >= limit) s[k][i] = __float_as_uint(-INFINITY);
-        }
-        float rowmax = -INFINITY;
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-#pragma unroll
-          for (int i = 0; i < 32; i += 2)
-            rowmax = fmax3(rowmax, __uint_as_float(s[k][i]), __uint_as_float(s[k][i + 1]));
-        m_row = fmaxf(m_row, rowmax);
-
-        float M_new;
-        if (tensor_pass) {
-          // Algorithm 1 step 1: maximum of the row maxima over the X-row tile
-          float tmax = rowmax;
-          const int xw = X < 32 ? X : 32;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1)
-            if (o < xw) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-          if (X > 32) {
-            float* slot = red + (t * 2 + par) * 4;
-            if (lane == 0) slot[wq] = tmax;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bar(L::bRed + t));
-            ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bRed + t), par, p, abort_flag));
-            if (!ok) break;
-            const int g0 = (X == 64) ? (wq & 2) : 0, gn = X / 32;
-            for (int w = 0; w < gn; ++w) tmax = fmaxf(tmax, slot[g0 + w]);
-          }
-          // the surrogate maximum is kept as a whole number of binades so the
-          // rescale factor of steps 2-3 is an exact power of two
-          const float Mc = (tmax == -INFINITY) ? -INFINITY : ceilf(tmax * c);
-          M_new = fmaxf(M, Mc);
-        } else {
-          M_new = (m_row == -INFINITY) ? -INFINITY : m_row * c;
-        }
-
-        // Algorithm 1 steps 2-3 factor: exp(m_old - m_new), one exact power
-        // of two per X-row tile (exact per-row factor in the vector variant).
-        const bool grow = j > 0 && M_new > M;
-        const float alpha = (M_new == -INFINITY) ? 1.f : ex2_approx(M - M_new);
-        if (j > 0) {
-          l *= alpha;
-          if (kLTensor) delta *= alpha;
-        }
-        // With X = 128 the whole 128-row tile shares the factor 2^-k, and the
-        // tensor pipe applies it inside the next O += P V (scale-input-d);
-        // other cases rescale O in TMEM from the vector side below.
-        bool vec_rescale = grow;
-        if (tensor_pass && X == 128) {
-          int kscale = 0;
-          if (grow && M_new - M <= 15.f) {
-            kscale = static_cast<int>(M_new - M);
-            vec_rescale = false;
-          }
-          if (wq == 0 && lane == 0) misc[4 + t] = static_cast<uint32_t>(kscale);
-        }
-        M = M_new;
-        const float neg_M = (M == -INFINITY) ? 0.f : -M;
-
-        // steps 4-6: Z = c S - m_hat, P~ = exp2(Z), stored as bf16 over S
-        const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(neg_M, neg_M);
-        uint64_t acc2 = f2_pack(0.f, 0.f);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const uint64_t z = f2_fma(f2_pack(__uint_as_float(s[k][2 * i]),
-                                              __uint_as_float(s[k][2 * i + 1])), c2, nm2);
-            float z0, z1;
-            f2_unpack(z, z0, z1);
-            const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
-            if (!(kLTensor && tensor_pass)) acc2 = f2_add(acc2, f2_pack(p0, p1));
-            pk[i] = pack_bf16x2(p0, p1);
-          }
-          tmem_st16(s_taddr + 16 * k, pk);
-        }
-        // steps 2-3 on the vector side: O <- alpha O in TMEM.  PV_{j-1} has
-        // completed (issued before S_j, whose completion we waited for) and
-        // PV_j waits for this warpgroup's P-full signal below.
-        if (__any_sync(0xffffffffu, vec_rescale)) {
-          const uint64_t a2 = f2_pack(alpha, alpha);
-#pragma unroll
-          for (int k = 0; k < D / 32; ++k) {
-            uint32_t ov[32];
-            tmem_ld32(o_taddr + 32 * k, ov);
-            tmem_wait_ld(ov);
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              float o0, o1;
-              f2_unpack(f2_mul(f2_pack(__uint_as_float(ov[i]), __uint_as_float(ov[i + 1])), a2),
-                        o0, o1);
-              ov[i] = __float_as_uint(o0);
-              ov[i + 1] = __float_as_uint(o1);
-            }
-            tmem_st32(o_taddr + 32 * k, ov);
-          }
-        }
-        tmem_wait_st();
-        tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(L::bPFull + t));
+      } else if (warp == kMmaWarp) {
+        // =================== MMA issuer ===================
+        if (lane == 0) {
+          constexpr uint32_t idesc_s = idesc_f32acc<false>(kBlockM, kBlockN, false);
+          constexpr uint32_t idesc_pv = idesc_f32acc<false>(kBlockM, D, true);
+          constexpr uint32_t idesc_rs = idesc_f32acc<false>(kBlockM, 16, false);
+          const uint64_t ones_desc = sdesc_sw128(sb + L::kOnes, 16, 1024);
+          bool ok = true;
+          auto issue_s = [&](int t, int st) {
+            const uint32_t qa = sb + L::kQ + t * L::kTile, ka = sb + L::kK + st * L::kTile;
+  #pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+              mma_ss<false>(tmem + t * kBlockN, sdesc_sw128(qa + off, 16, 1024),
+                            sdesc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
+            }
+          };
+          // O_t (+)= P_t V; with kscale > 0 the first K step also applies the
+          // uniform rescale O_t <- 2^-kscale O_t of Algorithm 1 steps 2-3.
+          auto issue_pv = [&](int t, int st, bool acc, int kscale) {
+            const uint32_t va = sb + L::kV + st * L::kTile;
+  #pragma unroll
+            for (int kk = 0; kk < kBlockN / 16; ++kk) {
+              const uint32_t d_t = tmem + 2 * kBlockN + t * D, a_t = tmem + t * kBlockN + kk * 8;
+              const uint64_t bd = sdesc_sw128(va + kk * 2048, 16384, 1024);
+              if (kk == 0 && acc && kscale > 0)
+                mma_ts_scale_rt(d_t, a_t, bd, idesc_pv, kscale);
+              else
+                mma_ts<false>(d_t, a_t, bd, idesc_pv, acc || kk > 0);
+            }
+          };
+          volatile uint32_t* pv_scale = misc + 4;
+          auto issue_rs = [&](int t) {
+  #pragma unroll
+            for (int kk = 0; kk < kBlockN / 16; ++kk)
+              mma_ts<false>(tmem + t * kBlockN + 64, tmem + t * kBlockN + kk * 8, ones_desc, idesc_rs,
+                            kk > 0);
+          };
 
-        if (kLTensor && tensor_pass) {
-          // step 7: the row sum comes from the tensor pipe (P~ times ones);
-          // the LSE also gets back the bf16 rounding of the dominant term.
-          if (rowmax != -INFINITY) {
-            const float pm = ex2_approx(fmaf(rowmax, c, neg_M));
-            delta += pm - bf16_round(pm);
-          }
-          ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bRsFull + t), par, p, abort_flag));
-          if (!ok) break;
-          tc_fence_after();
-          uint32_t lt;
-          tmem_ld1(s_taddr + 64, lt);
-          tmem_wait_ld1(lt);
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(bar(L::bLFree + t));
-          l += __uint_as_float(lt);
-        } else {
-          float r0, r1;
-          f2_unpack(acc2, r0, r1);
-          l += r0 + r1;
-        }
-      }
-
-      if (ok) ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bOFinal), pass & 1, p, abort_flag));
-      if (ok) {
-        tc_fence_after();
-        // detector for the all-underflow case: surrogate far above the exact
-        // maximum, or nothing left of the row sum
-        if (tensor_pass) {
-          const bool flagged =
-              row_g < p.N && (!(l > 0.f) || (M - m_row * c) > p.underflow_thresh);
-          const uint32_t ball = __ballot_sync(0xffffffffu, flagged);
-          if (ball != 0 && lane == 0) {
-            atomicOr(const_cast<uint32_t*>(misc + 2), 1u);
-            if (p.fallback_rows) atomicAdd(p.fallback_rows, __popc(ball));
-          }
-        }
-        // epilogue: O / l and LSE
-        const float inv_l = 1.f / l;
-        float* orow = p.o + (static_cast<size_t>(bh) * p.N + row_g) * D;
-#pragma unroll
-        for (int k = 0; k < D / 32; ++k) {
-          uint32_t ov[32];
-          tmem_ld32(o_taddr + 32 * k, ov);
-          tmem_wait_ld(ov);
-          if (row_g < p.N) {
-#pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              float4 v4 = make_float4(__uint_as_float(ov[i]) * inv_l, __uint_as_float(ov[i + 1]) * inv_l,
-                                      __uint_as_float(ov[i + 2]) * inv_l, __uint_as_float(ov[i + 3]) * inv_l);
-              *reinterpret_cast<float4*>(orow + 32 * k + i) = v4;
+          if (pass == 0) ok = wait_bounded(bar(L::bQFull), 0, p, abort_flag);
+          if (ok) {
+            const int st = it0 % S;
+            ok = wait_bounded(bar(L::bKFull + st), (it0 / S) & 1, p, abort_flag);
+            if (ok) {
+              tc_fence_after();
+              issue_s(0, st);
+              mma_commit(bar(L::bSFull + 0));
+              issue_s(1, st);
+              mma_commit(bar(L::bSFull + 1));
+              mma_commit(bar(L::bKEmpty + st));
             }
           }
+          for (int j = 0; ok && j < n_kv; ++j) {
+            const int it = it0 + j, st = it % S;
+            const uint32_t ph = (it / S) & 1, par = it & 1;
+            const bool more = j + 1 < n_kv;
+            const int st1 = (it + 1) % S;
+            const uint32_t ph1 = ((it + 1) / S) & 1;
+            if (!(ok = wait_bounded(bar(L::bVFull + st), ph, p, abort_flag))) break;
+            // tile 0
+            if (!(ok = wait_bounded(bar(L::bPFull + 0), par, p, abort_flag))) break;
+            tc_fence_after();
+            if (kLTensor && tensor_pass) {
+              issue_rs(0);
+              mma_commit(bar(L::bRsFull + 0));
+            }
+            issue_pv(0, st, j > 0, tensor_pass ? static_cast<int>(pv_scale[0]) : 0);
+            if (more) {
+              if (!(ok = wait_bounded(bar(L::bKFull + st1), ph1, p, abort_flag))) break;
+              if (kLTensor && tensor_pass && !(ok = wait_bounded(bar(L::bLFree + 0), par, p, abort_flag)))
+                break;
+              tc_fence_after();
+              issue_s(0, st1);
+              mma_commit(bar(L::bSFull + 0));
+            }
+            // tile 1
+            if (!(ok = wait_bounded(bar(L::bPFull + 1), par, p, abort_flag))) break;
+            tc_fence_after();
+            if (kLTensor && tensor_pass) {
+              issue_rs(1);
+              mma_commit(bar(L::bRsFull + 1));
+            }
+            issue_pv(1, st, j > 0, tensor_pass ? static_cast<int>(pv_scale[1]) : 0);
+            mma_commit(bar(L::bVEmpty + st));
+            if (more) {
+              if (kLTensor && tensor_pass && !(ok = wait_bounded(bar(L::bLFree + 1), par, p, abort_flag)))
+                break;
+              tc_fence_after();
+              issue_s(1, st1);
+              mma_commit(bar(L::bSFull + 1));
+              mma_commit(bar(L::bKEmpty + st1));
+            }
+          }
+          if (ok) {
+            mma_commit(bar(L::bOFinal));
+          } else {
+            // every MMA issued so far must finish before TMEM can be released
+            mma_commit(bar(L::bDrain));
+            wait_drain(bar(L::bDrain), 0);
+          }
         }
-        if (row_g < p.N) {
-          const float lsum = (kLTensor && tensor_pass) ? l + delta : l;
-          p.lse[static_cast<size_t>(bh) * p.N + row_g] = (M + __log2f(lsum)) * kLn2;
-        }
+        __syncwarp();
+      }
+      __syncthreads();
+      if (!kTensor || misc[2] == 0u || *abort_flag != 0u) break;
+    }
+    tc_fence_after();
+    if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
+  } else {
+    regs_inc<kSoftmaxRegs>();
+    for (int pass = 0; pass < 2; ++pass) {
+      const bool tensor_pass = kTensor && pass == 0;
+      const int it0 = pass * n_kv;
+      // =================== softmax warpgroups ===================
+      if constexpr (kTensor) {
+        if (tensor_pass)
+          softmax_role<D, true, kLTensor>(p, smem, sb, tmem, misc, warp, lane, m0, bh, n_kv, it0,
+                                          pass);
+        else
+          softmax_role_fallback<D>(p, smem, sb, tmem, misc, warp, lane, m0, bh, n_kv, it0, pass);
+      } else {
+        softmax_role<D, false, false>(p, smem, sb, tmem, misc, warp, lane, m0, bh, n_kv, it0, pass);
       }
       tc_fence_before();
+      __syncthreads();
+      // some row of this CTA was flagged: recompute the block with the exact
+      // per-row maximum (the optional vector fallback of the page's
+      // all-underflow discussion)
+      if (!kTensor || misc[2] == 0u || *abort_flag != 0u) break;
     }
-
-    __syncthreads();
-    if (!kTensor || misc[2] == 0u || *abort_flag != 0u) break;
-    // some row of this CTA was flagged: recompute the block with the exact
-    // per-row maximum (the optional vector fallback of the page's
-    // all-underflow discussion)
   }
-
-  tc_fence_after();
-  if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace fat
