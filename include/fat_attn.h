@@ -78,9 +78,11 @@ typedef enum { FAT_LMODE_VECTOR = 0, FAT_LMODE_TENSOR = 1 } fat_lmode;
  *   - the row sum l of step 7 is an fp32 sum on the vector units (see
  *     fat_lmode for the tensor-pipe alternative);
  *   - rows whose surrogate maximum exceeds their exact maximum by more than
- *     the underflow threshold (default 64 binades), or whose sum is zero,
- *     are recomputed with the exact per-row maximum (the optional fallback of
- *     the all-underflow discussion).
+ *     the underflow threshold (default 64 binades for bf16 P~, 14 for e4m3),
+ *     or whose sum is zero, are detected; their 256-row block is recomputed
+ *     with one-row tiles (X = 1: each row's own maximum rounded up to a whole
+ *     binade, so no row can underflow) -- the optional fallback of the
+ *     all-underflow discussion.
  * q, k, v: bf16.  Returns a fat_status.
  */
 int fat_attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse, int B, int H,
@@ -98,7 +100,10 @@ int fat_attn_fwd_vec(const void* q, const void* k, const void* v, float* o, floa
 /*
  * FP8 (e4m3) inputs with per-tensor fp32 descales (real value = code * descale),
  * fp32 accumulation, the tensorized softmax of fat_attn_fwd.  (The page
- * evaluates FP8-FP32 attention in its section A4.)
+ * evaluates FP8-FP32 attention in its section A4.)  d must be 128.  P~ is
+ * stored as e4m3 scaled by 2^8 (largest term <= 256 < 448; the factor cancels
+ * in O / l and is removed from LSE); O is rescaled on the vector side.
+ * Descales must be finite and > 0.
  */
 int fat_attn_fwd_fp8(const void* q, const void* k, const void* v, float q_descale,
                      float k_descale, float v_descale, float* o, float* lse, int B, int H, int N,

@@ -19,7 +19,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceCache {
   std::once_flag once;
   int arch_ok = 0;  // 1: sm_103
-  int smem_set[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  int smem_set[12] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
 };
 DeviceCache g_dev[kMaxDevices];
 
@@ -59,10 +59,10 @@ bool encode_qkv_map(CUtensorMap* tm, const void* ptr, int d, int N, int BH, int 
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-template <int D, bool kTensor, bool kLTensor>
+template <int D, bool kTensor, bool kLTensor, bool kE4M3>
 int launch(const fat::FwdParams& fp, int dev, int slot, int grid, cudaStream_t stream) {
-  auto kern = fat::fat_fwd_kernel<D, kTensor, kLTensor>;
-  const int smem = fat::Smem<D>::kAlloc;
+  auto kern = fat::fat_fwd_kernel<D, kTensor, kLTensor, kE4M3>;
+  const int smem = fat::Smem<D, kE4M3>::kAlloc;
   if (!g_dev[dev].smem_set[slot]) {
     // The warpgroup register split inside the kernel assumes exactly
     // kLaunchRegs registers per thread at launch; anything else could make
@@ -127,14 +127,19 @@ int fat_attn_fwd_ex(const fat_params* p) {
   if (!aligned16(p->q) || !aligned16(p->k) || !aligned16(p->v) || !aligned16(p->o) ||
       !aligned16(p->lse))
     return FAT_ERR_ALIGNMENT;
-  if (p->dtype == FAT_DTYPE_E4M3) return FAT_ERR_UNSUPPORTED;
+  const bool e4m3 = p->dtype == FAT_DTYPE_E4M3;
+  if (e4m3) {
+    for (float ds : {p->q_descale, p->k_descale, p->v_descale})
+      if (!(ds > 0.f) || !std::isfinite(ds)) return FAT_ERR_INVALID_ARG;
+    if (p->d != 128) return FAT_ERR_UNSUPPORTED;  // e4m3 rows must fill a 128-byte slab
+  }
 
   int dev = 0;
   const int arch = check_device(&dev);
   if (arch != FAT_OK) return arch;
 
   fat::FwdParams fp;
-  const int elt = 2;
+  const int elt = e4m3 ? 1 : 2;
   if (!encode_qkv_map(&fp.tm_q, p->q, p->d, p->N, static_cast<int>(BH), elt) ||
       !encode_qkv_map(&fp.tm_k, p->k, p->d, p->N, static_cast<int>(BH), elt) ||
       !encode_qkv_map(&fp.tm_v, p->v, p->d, p->N, static_cast<int>(BH), elt))
@@ -149,22 +154,33 @@ int fat_attn_fwd_ex(const fat_params* p) {
   fp.X = p->X;
   fp.n_mblocks = static_cast<int>(n_mblocks);
   fp.scale = p->scale;
-  fp.c = p->scale * fat::kLog2e;
-  fp.underflow_thresh = p->underflow_log2_threshold > 0.f ? p->underflow_log2_threshold : 64.f;
+  // logits are scale * (q_descale * q_code) . (k_descale * k_code)
+  fp.c = e4m3 ? p->scale * p->q_descale * p->k_descale * fat::kLog2e : p->scale * fat::kLog2e;
+  fp.v_scale = e4m3 ? p->v_descale : 1.f;
+  // bf16 P~ keeps fp32's exponent range (2^-64 leaves 62 binades); e4m3 P~ =
+  // 2^(Z+8) has its smallest normal at 2^-6, i.e. Z = -14
+  const float t_default = e4m3 ? 14.f : 64.f;
+  fp.underflow_thresh =
+      p->underflow_log2_threshold > 0.f ? p->underflow_log2_threshold : t_default;
   fp.poll_limit = p->wait_poll_limit;
   fp.timeout_ns = p->wait_timeout_ns ? p->wait_timeout_ns : 4000000000ull;
 
   const int grid = static_cast<int>(BH * n_mblocks);
   const bool tensor = p->variant == FAT_VARIANT_TENSOR;
   const bool l_tensor = p->l_mode == FAT_LMODE_TENSOR;
-  if (p->d == 128) {
-    if (!tensor) return launch<128, false, false>(fp, dev, 0, grid, p->stream);
-    return l_tensor ? launch<128, true, true>(fp, dev, 1, grid, p->stream)
-                    : launch<128, true, false>(fp, dev, 2, grid, p->stream);
+  if (e4m3) {
+    if (!tensor) return launch<128, false, false, true>(fp, dev, 6, grid, p->stream);
+    return l_tensor ? launch<128, true, true, true>(fp, dev, 7, grid, p->stream)
+                    : launch<128, true, false, true>(fp, dev, 8, grid, p->stream);
   }
-  if (!tensor) return launch<64, false, false>(fp, dev, 3, grid, p->stream);
-  return l_tensor ? launch<64, true, true>(fp, dev, 4, grid, p->stream)
-                  : launch<64, true, false>(fp, dev, 5, grid, p->stream);
+  if (p->d == 128) {
+    if (!tensor) return launch<128, false, false, false>(fp, dev, 0, grid, p->stream);
+    return l_tensor ? launch<128, true, true, false>(fp, dev, 1, grid, p->stream)
+                    : launch<128, true, false, false>(fp, dev, 2, grid, p->stream);
+  }
+  if (!tensor) return launch<64, false, false, false>(fp, dev, 3, grid, p->stream);
+  return l_tensor ? launch<64, true, true, false>(fp, dev, 4, grid, p->stream)
+                  : launch<64, true, false, false>(fp, dev, 5, grid, p->stream);
 }
 
 static int fwd_common(const void* q, const void* k, const void* v, float* o, float* lse, int B,

@@ -59,19 +59,25 @@ struct FwdParams {
   float scale;             // softmax scale as received
   float c;                 // log2(e) * scale (times q/k descales for e4m3)
   float underflow_thresh;  // binades between surrogate and exact row maximum
+  float v_scale;           // applied to O in the epilogue (e4m3 V descale; 1 for bf16)
   unsigned long long poll_limit;
   unsigned long long timeout_ns;
 };
 
-template <int D>
+template <int D, bool kE4M3 = false>
 struct Smem {
-  static constexpr int kStages = (D == 128) ? 2 : 4;
-  static constexpr int kTile = kBlockM * D * 2;  // bytes of one 128 x D bf16 tile
-  static constexpr int kAtoms = D / 64;          // 128-byte-wide column slabs per tile
+  static constexpr int kElt = kE4M3 ? 1 : 2;          // bytes per input element
+  static constexpr int kStages = (D * kElt == 256) ? 2 : 4;
+  static constexpr int kTile = kBlockM * D * kElt;    // bytes of one 128 x D tile
+  static constexpr int kAtoms = D * kElt / 128;       // 128-byte-wide column slabs per tile
+  static constexpr int kAtomCols = 128 / kElt;        // elements per slab row
+  static constexpr int kMmaK = 32 / kElt;             // K of one MMA (bf16 16, e4m3 32)
+  static constexpr int kPvStep = kMmaK * 128;         // bytes of V rows per PV K step
+  static_assert(kAtoms >= 1, "rows must span at least one 128-byte slab");
   static constexpr int kQ = 0;                   // Q_t at kQ + t * kTile
   static constexpr int kK = 2 * kTile;           // K ring
   static constexpr int kV = kK + kStages * kTile;  // V ring
-  static constexpr int kOnes = kV + kStages * kTile;  // 16 x 64 bf16 ones (2 KB)
+  static constexpr int kOnes = kV + kStages * kTile;  // 16 rows x 128 B of ones (2 KB)
   static constexpr int kBars = kOnes + 2048;
   // barrier slots
   static constexpr int bQFull = 0;
@@ -133,13 +139,17 @@ __device__ __forceinline__ float bf16_round(float x) {
 // (TMEM lane i).  kTensorPass selects the tensorized online softmax (surrogate
 // maximum over X-row tiles); otherwise the exact per-row maximum.
 // ---------------------------------------------------------------------------
-template <int D, bool kTensorPass, bool kLTensor>
+template <int D, bool kTensorPass, bool kLTensor, bool kE4M3>
 __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, uint32_t sb,
                                              uint32_t tmem, volatile uint32_t* misc, int warp,
                                              int lane, int m0, int bh, int n_kv, int it0,
-                                             int pass) {
-  using L = Smem<D>;
+                                             int pass, int X) {
+  using L = Smem<D, kE4M3>;
   constexpr bool tensor_pass = kTensorPass;
+  // e4m3 P~ is formed as 2^(Z + kKappa) <= 2^8 < 448 so that its largest
+  // terms use the format's range; the factor cancels in O / l and is taken
+  // off LSE.
+  constexpr float kKappa = kE4M3 ? 8.f : 0.f;
   volatile uint32_t* abort_flag = misc + 1;
   auto bar = [&](int i) -> uint32_t { return sb + L::kBars + 8 * i; };
     const int t = warp >> 2;        // tile
@@ -150,7 +160,6 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     const uint32_t s_taddr = tmem + lane_base + t * kBlockN;
     const uint32_t o_taddr = tmem + lane_base + 2 * kBlockN + t * D;
     const float c = p.c;
-    const int X = p.X;
     float* red = reinterpret_cast<float*>(smem + L::kRed);
 
     float M = -INFINITY;      // offset of the exponent, binades (exact row max * c in vec mode)
@@ -210,7 +219,9 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
         if (tensor_pass) {
           // Algorithm 1 step 1, within the warp: max of the row maxima over
           // the X-row tile (X = 16: half warps; X >= 32: the whole warp)
-          if (X == 16) {
+          if (X == 1) {
+            tmax = rowmax;  // one-row tiles: the exact maximum (the fallback pass)
+          } else if (X == 16) {
             tmax = rowmax;
 #pragma unroll
             for (int o = 1; o < 16; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
@@ -257,7 +268,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       // tensor pipe applies it inside the next O += P V (scale-input-d);
       // other cases rescale O in TMEM from the vector side below.
       bool vec_rescale = grow;
-      if (tensor_pass && X == 128) {
+      if (tensor_pass && X == 128 && !kE4M3) {
         int kscale = 0;
         if (grow && M_new - M <= 15.f) {
           kscale = static_cast<int>(M_new - M);
@@ -268,25 +279,37 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       M = M_new;
       const float neg_M = (M == -INFINITY) ? 0.f : -M;
 
-      // steps 4-6: Z = c S - m_hat, P~ = exp2(Z), stored as bf16 over S
-      const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(neg_M, neg_M);
+      // steps 4-6: Z = c S - m_hat, P~ = exp2(Z), stored as bf16 (e4m3) over S
+      const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(neg_M + kKappa, neg_M + kKappa);
       uint64_t acc2[4];
 #pragma unroll
       for (int a = 0; a < 4; ++a) acc2[a] = f2_pack(0.f, 0.f);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        uint32_t pk[16];
+        float pf[32];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const uint64_t z = f2_fma(f2_pack(__uint_as_float(s[k][2 * i]),
                                             __uint_as_float(s[k][2 * i + 1])), c2, nm2);
           float z0, z1;
           f2_unpack(z, z0, z1);
-          const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
-          if (!(kLTensor && tensor_pass)) acc2[i & 3] = f2_add(acc2[i & 3], f2_pack(p0, p1));
-          pk[i] = pack_bf16x2(p0, p1);
+          pf[2 * i] = ex2_approx(z0);
+          pf[2 * i + 1] = ex2_approx(z1);
+          if (!(kLTensor && tensor_pass))
+            acc2[i & 3] = f2_add(acc2[i & 3], f2_pack(pf[2 * i], pf[2 * i + 1]));
         }
-        tmem_st16(s_taddr + 16 * k, pk);
+        if constexpr (kE4M3) {
+          uint32_t pk[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            pk[i] = pack_e4m3x4(pf[4 * i], pf[4 * i + 1], pf[4 * i + 2], pf[4 * i + 3]);
+          tmem_st8(s_taddr + 8 * k, pk);
+        } else {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(pf[2 * i], pf[2 * i + 1]);
+          tmem_st16(s_taddr + 16 * k, pk);
+        }
       }
       // steps 2-3 on the vector side: O <- alpha O in TMEM.  PV_{j-1} has
       // completed (issued before S_j, whose completion we waited for) and
@@ -318,8 +341,8 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
         // step 7: the row sum comes from the tensor pipe (P~ times ones);
         // the LSE also gets back the bf16 rounding of the dominant term.
         if (rowmax != -INFINITY) {
-          const float pm = ex2_approx(fmaf(rowmax, c, neg_M));
-          delta += pm - bf16_round(pm);
+          const float pm = ex2_approx(fmaf(rowmax, c, neg_M + kKappa));
+          delta += pm - (kE4M3 ? e4m3_round(pm) : bf16_round(pm));
         }
         dead = !__all_sync(0xffffffffu, wait_bounded(bar(L::bRsFull + t), par, p, abort_flag));
         if (dead) continue;
@@ -344,7 +367,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       tc_fence_after();
       // detector for the all-underflow case: surrogate far above the exact
       // maximum, or nothing left of the row sum
-      if (tensor_pass) {
+      if (tensor_pass && pass == 0) {
         const bool flagged =
             row_g < p.N && (!(l > 0.f) || (M - m_row * c) > p.underflow_thresh);
         const uint32_t ball = __ballot_sync(0xffffffffu, flagged);
@@ -354,7 +377,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
         }
       }
       // epilogue: O / l and LSE
-      const float inv_l = 1.f / l;
+      const float inv_l = p.v_scale / l;
       float* orow = p.o + (static_cast<size_t>(bh) * p.N + row_g) * D;
 #pragma unroll
       for (int k = 0; k < D / 32; ++k) {
@@ -372,21 +395,10 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       }
       if (row_g < p.N) {
         const float lsum = (kLTensor && tensor_pass) ? l + delta : l;
-        p.lse[static_cast<size_t>(bh) * p.N + row_g] = (M + __log2f(lsum)) * kLn2;
+        p.lse[static_cast<size_t>(bh) * p.N + row_g] = (M - kKappa + __log2f(lsum)) * kLn2;
       }
     }
     tc_fence_before();
-}
-
-// The exact-maximum recomputation that follows a flagged tensorized pass is
-// rare; as a separate (not inlined) function its registers do not weigh on
-// the hot tensorized loop.
-template <int D>
-__device__ __noinline__ void softmax_role_fallback(const FwdParams& p, uint8_t* smem, uint32_t sb,
-                                                   uint32_t tmem, volatile uint32_t* misc,
-                                                   int warp, int lane, int m0, int bh, int n_kv,
-                                                   int it0, int pass) {
-  softmax_role<D, false, false>(p, smem, sb, tmem, misc, warp, lane, m0, bh, n_kv, it0, pass);
 }
 
 // ---------------------------------------------------------------------------
@@ -397,9 +409,10 @@ __device__ __noinline__ void softmax_role_fallback(const FwdParams& p, uint8_t* 
 // kLTensor: (kTensor only) the row sum of step 7 on the tensor pipe as
 //           P~ (bf16) times a block of ones; otherwise an fp32 sum of the
 //           unrounded P~ on the vector units.
-template <int D, bool kTensor, bool kLTensor>
+// kE4M3:    e4m3 inputs, kind::f8f6f4 MMAs, e4m3 P~ (otherwise bf16).
+template <int D, bool kTensor, bool kLTensor, bool kE4M3>
 __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_constant__ FwdParams p) {
-  using L = Smem<D>;
+  using L = Smem<D, kE4M3>;
   constexpr int S = L::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -444,7 +457,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
     fence_mbar_init();
   }
   if (threadIdx.x < 256) {  // the ones tile used as B of the row-sum MMA
-    reinterpret_cast<uint2*>(smem + L::kOnes)[threadIdx.x] = make_uint2(0x3F803F80u, 0x3F803F80u);
+    // 1.0 in bf16 (0x3F80) or e4m3 (0x38)
+    const uint32_t one = kE4M3 ? 0x38383838u : 0x3F803F80u;
+    reinterpret_cast<uint2*>(smem + L::kOnes)[threadIdx.x] = make_uint2(one, one);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   if (warp == kMmaWarp) {
@@ -475,7 +490,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
             mbar_arrive_expect_tx(bar(L::bQFull), 2 * L::kTile);
             for (int t = 0; t < 2; ++t)
               for (int a = 0; a < L::kAtoms; ++a)
-                tma_load_3d(sb + L::kQ + t * L::kTile + a * 16384, &p.tm_q, bar(L::bQFull), a * 64,
+                tma_load_3d(sb + L::kQ + t * L::kTile + a * 16384, &p.tm_q, bar(L::bQFull), a * L::kAtomCols,
                             m0 + t * kBlockM, bh);
           }
           for (int j = 0; j < n_kv; ++j) {
@@ -485,13 +500,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
             mbar_arrive_expect_tx(bar(L::bKFull + st), L::kTile);
             for (int a = 0; a < L::kAtoms; ++a)
               tma_load_3d(sb + L::kK + st * L::kTile + a * 16384, &p.tm_k, bar(L::bKFull + st),
-                          a * 64, j * kBlockN, bh);
+                          a * L::kAtomCols, j * kBlockN, bh);
             k_issued = j + 1;
             if (!wait_bounded(bar(L::bVEmpty + st), ph ^ 1, p, abort_flag)) break;
             mbar_arrive_expect_tx(bar(L::bVFull + st), L::kTile);
             for (int a = 0; a < L::kAtoms; ++a)
               tma_load_3d(sb + L::kV + st * L::kTile + a * 16384, &p.tm_v, bar(L::bVFull + st),
-                          a * 64, j * kBlockN, bh);
+                          a * L::kAtomCols, j * kBlockN, bh);
             v_issued = j + 1;
           }
           if (*abort_flag) {
@@ -507,17 +522,18 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
       } else if (warp == kMmaWarp) {
         // =================== MMA issuer ===================
         if (lane == 0) {
-          constexpr uint32_t idesc_s = idesc_f32acc<false>(kBlockM, kBlockN, false);
-          constexpr uint32_t idesc_pv = idesc_f32acc<false>(kBlockM, D, true);
-          constexpr uint32_t idesc_rs = idesc_f32acc<false>(kBlockM, 16, false);
+          constexpr uint32_t idesc_s = idesc_f32acc<kE4M3>(kBlockM, kBlockN, false);
+          constexpr uint32_t idesc_pv = idesc_f32acc<kE4M3>(kBlockM, D, true);
+          constexpr uint32_t idesc_rs = idesc_f32acc<kE4M3>(kBlockM, 16, false);
           const uint64_t ones_desc = sdesc_sw128(sb + L::kOnes, 16, 1024);
           bool ok = true;
           auto issue_s = [&](int t, int st) {
             const uint32_t qa = sb + L::kQ + t * L::kTile, ka = sb + L::kK + st * L::kTile;
   #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
+            for (int kk = 0; kk < D / L::kMmaK; ++kk) {
+              // each 128-byte slab row holds four 32-byte K steps
               const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-              mma_ss<false>(tmem + t * kBlockN, sdesc_sw128(qa + off, 16, 1024),
+              mma_ss<kE4M3>(tmem + t * kBlockN, sdesc_sw128(qa + off, 16, 1024),
                             sdesc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
             }
           };
@@ -526,20 +542,21 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
           auto issue_pv = [&](int t, int st, bool acc, int kscale) {
             const uint32_t va = sb + L::kV + st * L::kTile;
   #pragma unroll
-            for (int kk = 0; kk < kBlockN / 16; ++kk) {
+            for (int kk = 0; kk < kBlockN / L::kMmaK; ++kk) {
+              // P~ packs 2 (bf16) or 4 (e4m3) keys per TMEM column: 8 columns per K step
               const uint32_t d_t = tmem + 2 * kBlockN + t * D, a_t = tmem + t * kBlockN + kk * 8;
-              const uint64_t bd = sdesc_sw128(va + kk * 2048, 16384, 1024);
-              if (kk == 0 && acc && kscale > 0)
+              const uint64_t bd = sdesc_sw128(va + kk * L::kPvStep, 16384, 1024);
+              if (!kE4M3 && kk == 0 && acc && kscale > 0)
                 mma_ts_scale_rt(d_t, a_t, bd, idesc_pv, kscale);
               else
-                mma_ts<false>(d_t, a_t, bd, idesc_pv, acc || kk > 0);
+                mma_ts<kE4M3>(d_t, a_t, bd, idesc_pv, acc || kk > 0);
             }
           };
           volatile uint32_t* pv_scale = misc + 4;
           auto issue_rs = [&](int t) {
   #pragma unroll
-            for (int kk = 0; kk < kBlockN / 16; ++kk)
-              mma_ts<false>(tmem + t * kBlockN + 64, tmem + t * kBlockN + kk * 8, ones_desc, idesc_rs,
+            for (int kk = 0; kk < kBlockN / L::kMmaK; ++kk)
+              mma_ts<kE4M3>(tmem + t * kBlockN + 64, tmem + t * kBlockN + kk * 8, ones_desc, idesc_rs,
                             kk > 0);
           };
 
@@ -566,14 +583,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
             // tile 0
             if (!(ok = wait_bounded(bar(L::bPFull + 0), par, p, abort_flag))) break;
             tc_fence_after();
-            if (kLTensor && tensor_pass) {
+            if (kLTensor) {
               issue_rs(0);
               mma_commit(bar(L::bRsFull + 0));
             }
             issue_pv(0, st, j > 0, tensor_pass ? static_cast<int>(pv_scale[0]) : 0);
             if (more) {
               if (!(ok = wait_bounded(bar(L::bKFull + st1), ph1, p, abort_flag))) break;
-              if (kLTensor && tensor_pass && !(ok = wait_bounded(bar(L::bLFree + 0), par, p, abort_flag)))
+              if (kLTensor && !(ok = wait_bounded(bar(L::bLFree + 0), par, p, abort_flag)))
                 break;
               tc_fence_after();
               issue_s(0, st1);
@@ -582,14 +599,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
             // tile 1
             if (!(ok = wait_bounded(bar(L::bPFull + 1), par, p, abort_flag))) break;
             tc_fence_after();
-            if (kLTensor && tensor_pass) {
+            if (kLTensor) {
               issue_rs(1);
               mma_commit(bar(L::bRsFull + 1));
             }
             issue_pv(1, st, j > 0, tensor_pass ? static_cast<int>(pv_scale[1]) : 0);
             mma_commit(bar(L::bVEmpty + st));
             if (more) {
-              if (kLTensor && tensor_pass && !(ok = wait_bounded(bar(L::bLFree + 1), par, p, abort_flag)))
+              if (kLTensor && !(ok = wait_bounded(bar(L::bLFree + 1), par, p, abort_flag)))
                 break;
               tc_fence_after();
               issue_s(1, st1);
@@ -615,23 +632,15 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
   } else {
     regs_inc<kSoftmaxRegs>();
     for (int pass = 0; pass < 2; ++pass) {
-      const bool tensor_pass = kTensor && pass == 0;
       const int it0 = pass * n_kv;
       // =================== softmax warpgroups ===================
-      if constexpr (kTensor) {
-        if (tensor_pass)
-          softmax_role<D, true, kLTensor>(p, smem, sb, tmem, misc, warp, lane, m0, bh, n_kv, it0,
-                                          pass);
-        else
-          softmax_role_fallback<D>(p, smem, sb, tmem, misc, warp, lane, m0, bh, n_kv, it0, pass);
-      } else {
-        softmax_role<D, false, false>(p, smem, sb, tmem, misc, warp, lane, m0, bh, n_kv, it0, pass);
-      }
-      tc_fence_before();
+      // Pass 1 (only after a flagged pass 0) reruns the block with one-row
+      // tiles, X = 1: every row's own maximum rounded up to a whole binade,
+      // so no row can underflow (the vector fallback of the page's
+      // all-underflow discussion, on the same code path).
+      softmax_role<D, kTensor, kLTensor, kE4M3>(p, smem, sb, tmem, misc, warp, lane, m0, bh, n_kv,
+                                               it0, pass, pass == 0 ? p.X : 1);
       __syncthreads();
-      // some row of this CTA was flagged: recompute the block with the exact
-      // per-row maximum (the optional vector fallback of the page's
-      // all-underflow discussion)
       if (!kTensor || misc[2] == 0u || *abort_flag != 0u) break;
     }
   }

@@ -13,8 +13,8 @@ import oracle
 import tensorized_online_softmax_gb300 as fat
 from tensorized_online_softmax_gb300 import inputs as gen
 
-from gpu_helpers import (compare, compare_sampled, oracle_full, oracle_sampled, run_cuda,
-                         sample_rows, to_dev, tol_key)
+from gpu_helpers import (compare, compare_sampled, e4m3_row_bound, oracle_full, oracle_sampled,
+                         run_cuda, sample_rows, to_dev, tol_key)
 
 pytestmark = pytest.mark.gpu
 
@@ -59,7 +59,41 @@ def test_tiny_workload(cuda_device, variant):
 
 
 FULL = ["b4h16n2048d128", "b4h16n2048d128_causal", "b2h16n8192d128_causal",
-        "stress_b1h32n16384d64"]
+        "stress_b1h32n16384d64", "fp8_b4h16n4096d128"]
+
+SMALL_FP8 = [
+    # (B, H, N, d, causal, X); e4m3 rows must span 128 bytes, so d = 128
+    (1, 2, 256, 128, False, 128),
+    (1, 1, 300, 128, True, 64),
+    (2, 2, 513, 128, False, 32),
+    (1, 1, 77, 128, True, 16),
+]
+
+
+@pytest.mark.parametrize("variant", ["tensor", "vec"])
+@pytest.mark.parametrize("shape", SMALL_FP8, ids=lambda s: "B{}H{}N{}d{}{}X{}".format(
+    s[0], s[1], s[2], s[3], "c" if s[4] else "", s[5]))
+def test_small_shapes_fp8(cuda_device, shape, variant):
+    """Rows with at least 128 allowed keys meet the e4m3 bars; causal rows
+    with fewer keys are held to the per-row e4m3 rounding bound instead, and
+    LSE (formed from unrounded weights) meets the 1e-3 bar everywhere."""
+    B, H, N, d, causal, X = shape
+    w = gen.Workload("small_fp8", B, H, N, d, causal, X, dtype="e4m3", seed=17 + N)
+    inp = gen.make_inputs(w)
+    o, lse = run_cuda(w, to_dev(inp), variant)
+    o_ref, lse_ref = oracle_full(w, inp)
+    o_g = o.cpu().double().numpy()
+    lse_g = lse.cpu().double().numpy()
+    keys = np.arange(1, N + 1) if causal else np.full(N, N)
+    many = keys >= 128
+    if many.any():
+        compare(o_g[:, :, many], lse_g[:, :, many], o_ref[:, :, many], lse_ref[:, :, many],
+                "e4m3", what=f"{shape} {variant} rows with >= 128 keys")
+    err = np.abs(o_g - o_ref).max(axis=-1)
+    bound = e4m3_row_bound(gen.widened(inp, "v").numpy(), causal)
+    assert np.all(err <= bound), f"{shape} {variant}: {(err / bound).max():.3f} of the bound"
+    assert np.abs(o_g - o_ref).mean() <= 6e-3
+    assert np.abs(lse_g - lse_ref).max() <= 1e-3
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
