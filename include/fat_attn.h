@@ -129,7 +129,22 @@ typedef struct fat_params {
   unsigned long long wait_poll_limit; /* 0: no cap on polls of one device wait */
   unsigned long long wait_timeout_ns; /* 0: default of 4 s per device wait */
   cudaStream_t stream;
+  /* nullable device buffer of FAT_TRACE_WORDS u64 (8-byte aligned): SM-clock
+   * stamps of the first thread block's pipeline phases, for measuring how
+   * long the tensor pipe waits for the softmax (see fat_trace_layout below) */
+  unsigned long long* trace;
 } fat_params;
+
+/*
+ * Trace layout: word (e * 2 + t) * FAT_TRACE_ITERS + j holds the clock of
+ * event e for query tile t (0/1) at K/V tile j (< FAT_TRACE_ITERS), first
+ * pass only: e = 0 softmax received S_j; 1 softmax computed m_hat; 2 softmax
+ * published P_j; 3 MMA issuer saw P_j; 4 MMA issuer queued O += P_j V and
+ * S_{j+1}.  Word FAT_TRACE_WORDS-2: kernel start; FAT_TRACE_WORDS-1: end of
+ * the softmax loop.  Words of events that did not happen are left untouched.
+ */
+#define FAT_TRACE_ITERS 128
+#define FAT_TRACE_WORDS (5 * 2 * FAT_TRACE_ITERS + 2)
 
 int fat_attn_fwd_ex(const fat_params* p);
 

@@ -37,6 +37,8 @@ FAT_ERR_ARCH = -6
 VARIANTS = {"tensor": 0, "vec": 1}
 DTYPES = {"bf16": 0, "e4m3": 1}
 LMODES = {"vector": 0, "tensor": 1}
+TRACE_ITERS = 128
+TRACE_WORDS = 5 * 2 * TRACE_ITERS + 2
 
 # every extern "C" entry point declared in include/fat_attn.h
 ABI_SYMBOLS = (
@@ -67,6 +69,7 @@ class FatParams(ctypes.Structure):
         ("wait_poll_limit", ctypes.c_ulonglong),
         ("wait_timeout_ns", ctypes.c_ulonglong),
         ("stream", ctypes.c_void_p),
+        ("trace", ctypes.c_void_p),
     ]
 
 
@@ -143,7 +146,7 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, X: int =
              variant: str = "tensor", *, out=None, stream=None, fallback_rows=None,
              underflow_log2_threshold: float = 0.0, wait_poll_limit: int = 0,
              wait_timeout_ns: int = 0, dtype: str = "bf16", descales=(1.0, 1.0, 1.0),
-             l_mode: str = "vector"):
+             l_mode: str = "vector", trace=None):
     """Fused attention forward.  Returns ``(o, lse)`` (fp32 [B,H,N,d], fp32 [B,H,N]).
 
     ``q, k, v``: contiguous CUDA tensors [B, H, N, d] (bf16, or float8_e4m3fn
@@ -183,6 +186,7 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, X: int =
     p.wait_poll_limit = int(wait_poll_limit)
     p.wait_timeout_ns = int(wait_timeout_ns)
     p.stream = _stream_handle(stream).value
+    p.trace = trace.data_ptr() if trace is not None else None
     with torch.cuda.device(q.device):
         st = lib.fat_attn_fwd_ex(ctypes.byref(p))
     if st != FAT_OK:

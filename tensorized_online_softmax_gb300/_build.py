@@ -12,13 +12,16 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libfat_attn.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
-MAIN_SOURCE = os.path.join(CSRC, "fat_attn_api.cu")
-
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-std=c++17", "-lineinfo",
-    "-Xcompiler", "-fPIC", "-shared",
+    "-Xcompiler", "-fPIC",
 ]
+
+
+def translation_units():
+    """Every .cu in csrc: the C ABI plus one file per group of kernel instances."""
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
 def _sources():
@@ -44,21 +47,45 @@ def is_stale(path: str = LIB_PATH) -> bool:
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Build ``_build/libfat_attn.so`` with nvcc (sm_103a only)."""
+    """Build ``_build/libfat_attn.so`` with nvcc (sm_103a only).
+
+    The translation units compile in parallel (one nvcc per unit), then link.
+    """
     if not force and not is_stale():
         return LIB_PATH
     nvcc = nvcc_path()
     if nvcc is None:
         raise RuntimeError("nvcc not found: cannot build the CUDA library")
     os.makedirs(BUILD_DIR, exist_ok=True)
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [nvcc, *NVCC_FLAGS, *extra_flags, "-o", tmp, MAIN_SOURCE]
+    tag = f".tmp{os.getpid()}"
+    units = translation_units()
+    objs = [os.path.join(BUILD_DIR, os.path.basename(u)[:-3] + tag + ".o") for u in units]
+    procs = []
+    for u, o in zip(units, objs):
+        cmd = [nvcc, *NVCC_FLAGS, *extra_flags, "-c", "-o", o, u]
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+        procs.append((u, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT,
+                                          text=True)))
+    failed, logs = [], []
+    for u, pr in procs:
+        out, _ = pr.communicate()
+        logs.append(out)
+        if pr.returncode != 0:
+            failed.append((u, out))
+    if failed:
+        for o in objs:
+            if os.path.exists(o):
+                os.remove(o)
+        raise RuntimeError("nvcc failed:\n" + "\n".join(f"{u}:\n{out}" for u, out in failed))
     if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    res = subprocess.run(cmd, capture_output=True, text=True)
+        print("".join(logs))
+    tmp = LIB_PATH + tag
+    res = subprocess.run([nvcc, "-shared", "-gencode", "arch=compute_103a,code=sm_103a", "-o", tmp,
+                          *objs], capture_output=True, text=True)
+    for o in objs:
+        os.remove(o)
     if res.returncode != 0:
-        raise RuntimeError("nvcc failed:\n" + res.stdout + res.stderr)
-    if verbose:
-        print(res.stdout + res.stderr)
+        raise RuntimeError("nvcc link failed:\n" + res.stdout + res.stderr)
     os.replace(tmp, LIB_PATH)
     return LIB_PATH

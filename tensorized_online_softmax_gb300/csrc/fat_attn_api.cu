@@ -10,16 +10,20 @@
 #include <mutex>
 
 #include "../../include/fat_attn.h"
-#include "fat_fwd_kernel.cuh"
+#include "fat_launch.cuh"
 
 namespace {
 
-constexpr int kMaxDevices = 64;
+constexpr int kMaxDevices = fat::kMaxDevices;
+
+// Device error word shared by every kernel of the library (their address is
+// passed in the kernel parameters): bit 0 = a bounded wait ran out.
+__device__ unsigned int g_fat_error_word = 0;
 
 struct DeviceCache {
   std::once_flag once;
-  int arch_ok = 0;  // 1: sm_103
-  int smem_set[12] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+  int arch_ok = 0;                       // 1: sm_103
+  unsigned int* error_word = nullptr;    // device address of g_fat_error_word
 };
 DeviceCache g_dev[kMaxDevices];
 
@@ -59,26 +63,6 @@ bool encode_qkv_map(CUtensorMap* tm, const void* ptr, int d, int N, int BH, int 
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-template <int D, bool kTensor, bool kLTensor, bool kE4M3>
-int launch(const fat::FwdParams& fp, int dev, int slot, int grid, cudaStream_t stream) {
-  auto kern = fat::fat_fwd_kernel<D, kTensor, kLTensor, kE4M3>;
-  const int smem = fat::Smem<D, kE4M3>::kAlloc;
-  if (!g_dev[dev].smem_set[slot]) {
-    // The warpgroup register split inside the kernel assumes exactly
-    // kLaunchRegs registers per thread at launch; anything else could make
-    // the register increase wait forever, so refuse to launch.
-    cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs != fat::kLaunchRegs)
-      return FAT_ERR_LAUNCH;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-      return FAT_ERR_LAUNCH;
-    g_dev[dev].smem_set[slot] = 1;
-  }
-  kern<<<grid, fat::kNumThreads, smem, stream>>>(fp);
-  return cudaGetLastError() == cudaSuccess ? FAT_OK : FAT_ERR_LAUNCH;
-}
-
 int check_device(int* dev_out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FAT_ERR_LAUNCH;
@@ -88,9 +72,13 @@ int check_device(int* dev_out) {
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
     c.arch_ok = (major == 10 && minor == 3) ? 1 : 0;
+    void* addr = nullptr;
+    if (c.arch_ok && cudaGetSymbolAddress(&addr, g_fat_error_word) == cudaSuccess)
+      c.error_word = static_cast<unsigned int*>(addr);
   });
   *dev_out = dev;
-  return c.arch_ok ? FAT_OK : FAT_ERR_ARCH;
+  if (!c.arch_ok) return FAT_ERR_ARCH;
+  return c.error_word ? FAT_OK : FAT_ERR_LAUNCH;
 }
 
 }  // namespace
@@ -164,23 +152,25 @@ int fat_attn_fwd_ex(const fat_params* p) {
       p->underflow_log2_threshold > 0.f ? p->underflow_log2_threshold : t_default;
   fp.poll_limit = p->wait_poll_limit;
   fp.timeout_ns = p->wait_timeout_ns ? p->wait_timeout_ns : 4000000000ull;
+  fp.trace = p->trace;
+  fp.error_word = g_dev[dev].error_word;
+  if (p->trace && (reinterpret_cast<uintptr_t>(p->trace) & 7u)) return FAT_ERR_ALIGNMENT;
 
   const int grid = static_cast<int>(BH * n_mblocks);
   const bool tensor = p->variant == FAT_VARIANT_TENSOR;
-  const bool l_tensor = p->l_mode == FAT_LMODE_TENSOR;
-  if (e4m3) {
-    if (!tensor) return launch<128, false, false, true>(fp, dev, 6, grid, p->stream);
-    return l_tensor ? launch<128, true, true, true>(fp, dev, 7, grid, p->stream)
-                    : launch<128, true, false, true>(fp, dev, 8, grid, p->stream);
-  }
-  if (p->d == 128) {
-    if (!tensor) return launch<128, false, false, false>(fp, dev, 0, grid, p->stream);
-    return l_tensor ? launch<128, true, true, false>(fp, dev, 1, grid, p->stream)
-                    : launch<128, true, false, false>(fp, dev, 2, grid, p->stream);
-  }
-  if (!tensor) return launch<64, false, false, false>(fp, dev, 3, grid, p->stream);
-  return l_tensor ? launch<64, true, true, false>(fp, dev, 4, grid, p->stream)
-                  : launch<64, true, false, false>(fp, dev, 5, grid, p->stream);
+  const bool l_tensor = tensor && p->l_mode == FAT_LMODE_TENSOR;
+  const int X = tensor ? p->X : 0;  // X = 0: the vector-softmax kernel
+  int st;
+  if (e4m3)
+    st = l_tensor ? fat::dispatch_e4m3_d128_ltensor(fp, X, dev, grid, p->stream)
+                  : fat::dispatch_e4m3_d128_lvec(fp, X, dev, grid, p->stream);
+  else if (p->d == 128)
+    st = l_tensor ? fat::dispatch_bf16_d128_ltensor(fp, X, dev, grid, p->stream)
+                  : fat::dispatch_bf16_d128_lvec(fp, X, dev, grid, p->stream);
+  else
+    st = l_tensor ? fat::dispatch_bf16_d64_ltensor(fp, X, dev, grid, p->stream)
+                  : fat::dispatch_bf16_d64_lvec(fp, X, dev, grid, p->stream);
+  return st == 0 ? FAT_OK : (st == -1 ? FAT_ERR_UNSUPPORTED : FAT_ERR_LAUNCH);
 }
 
 static int fwd_common(const void* q, const void* k, const void* v, float* o, float* lse, int B,
@@ -243,11 +233,11 @@ int fat_attn_fwd_fp8(const void* q, const void* k, const void* v, float q_descal
 int fat_check_device_error(cudaStream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return FAT_ERR_LAUNCH;
   unsigned int word = 0;
-  if (cudaMemcpyFromSymbol(&word, fat::g_fat_error_word, sizeof(word)) != cudaSuccess)
+  if (cudaMemcpyFromSymbol(&word, g_fat_error_word, sizeof(word)) != cudaSuccess)
     return FAT_ERR_LAUNCH;
   if (word != 0) {
     const unsigned int zero = 0;
-    if (cudaMemcpyToSymbol(fat::g_fat_error_word, &zero, sizeof(zero)) != cudaSuccess)
+    if (cudaMemcpyToSymbol(g_fat_error_word, &zero, sizeof(zero)) != cudaSuccess)
       return FAT_ERR_LAUNCH;
     return FAT_ERR_DEVICE_TIMEOUT;
   }

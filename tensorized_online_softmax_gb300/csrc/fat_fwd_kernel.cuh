@@ -34,16 +34,14 @@ constexpr int kNumThreads = 384;
 // warpgroup drops to kCtrlRegs and the two softmax warpgroups rise to
 // kSoftmaxRegs.  256 * kSoftmaxRegs + 128 * kCtrlRegs <= 384 * kLaunchRegs.
 constexpr int kLaunchRegs = 168;
-constexpr int kCtrlRegs = 64;
-constexpr int kSoftmaxRegs = 216;
+constexpr int kCtrlRegs = 56;
+constexpr int kSoftmaxRegs = 224;
 static_assert(256 * kSoftmaxRegs + 128 * kCtrlRegs <= kNumThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-// Device error word: bit 0 = a bounded wait ran out.
-__device__ unsigned int g_fat_error_word = 0;
 
 struct FwdParams {
   CUtensorMap tm_q;
@@ -62,7 +60,22 @@ struct FwdParams {
   float v_scale;           // applied to O in the epilogue (e4m3 V descale; 1 for bf16)
   unsigned long long poll_limit;
   unsigned long long timeout_ns;
+  unsigned long long* trace;  // nullable: phase stamps of CTA 0 (kTraceWords)
+  unsigned int* error_word;   // device error word: bit 0 = a bounded wait ran out
 };
+
+// Phase trace of CTA 0, SM clock (clock64) stamps, pass 0 only:
+//   word (e * 2 + t) * kTraceIters + j for event e, tile t, K/V tile j:
+//   e = 0 softmax got S_j, 1 softmax has m_hat, 2 softmax publishes P_j,
+//       3 MMA issuer sees P_j, 4 MMA issuer has queued O += P_j V, S_{j+1};
+//   word kTraceWords - 2 / - 1: kernel start / softmax epilogue done.
+constexpr int kTraceIters = 128;
+constexpr int kTraceWords = 5 * 2 * kTraceIters + 2;
+
+__device__ __forceinline__ void trace_mark(const FwdParams& p, int e, int t, int j, int pass) {
+  if (p.trace != nullptr && blockIdx.x == 0 && pass == 0 && j < kTraceIters)
+    p.trace[(e * 2 + t) * kTraceIters + j] = static_cast<unsigned long long>(clock64());
+}
 
 template <int D, bool kE4M3 = false>
 struct Smem {
@@ -116,7 +129,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
     if (p.poll_limit != 0 && polls >= p.poll_limit) break;
     if ((polls & 63) == 0 && globaltimer_ns() - t0 > p.timeout_ns) break;
   }
-  atomicOr(&g_fat_error_word, 1u);
+  atomicOr(p.error_word, 1u);
   *abort_flag = 1u;
   return false;
 }
@@ -136,284 +149,292 @@ __device__ __forceinline__ float bf16_round(float x) {
 
 // ---------------------------------------------------------------------------
 // softmax warpgroups: warpgroup t owns query tile t; thread i owns row i
-// (TMEM lane i).  kTensorPass selects the tensorized online softmax (surrogate
-// maximum over X-row tiles); otherwise the exact per-row maximum.
+// (TMEM lane i).
+//   kX > 0   tensorized online softmax with the surrogate maximum over kX-row
+//            tiles (X is a compile-time constant so no runtime branching sits
+//            in the hot loop); `exact` (the fallback pass) uses each row's own
+//            maximum instead, rounded up to a whole binade.
+//   kX == 0  the vector-softmax ablation: exact per-row maximum.
 // ---------------------------------------------------------------------------
-template <int D, bool kTensorPass, bool kLTensor, bool kE4M3>
+template <int D, int kX, bool kLTensor, bool kE4M3>
 __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, uint32_t sb,
                                              uint32_t tmem, volatile uint32_t* misc, int warp,
                                              int lane, int m0, int bh, int n_kv, int it0,
-                                             int pass, int X) {
+                                             int pass, bool exact) {
   using L = Smem<D, kE4M3>;
-  constexpr bool tensor_pass = kTensorPass;
+  constexpr bool kTensor = kX > 0;
+  constexpr bool kGroup = kX > 32;  // tile maximum spans several warps
+  constexpr bool kMmaScale = kX == 128 && !kE4M3;
   // e4m3 P~ is formed as 2^(Z + kKappa) <= 2^8 < 448 so that its largest
   // terms use the format's range; the factor cancels in O / l and is taken
   // off LSE.
   constexpr float kKappa = kE4M3 ? 8.f : 0.f;
   volatile uint32_t* abort_flag = misc + 1;
   auto bar = [&](int i) -> uint32_t { return sb + L::kBars + 8 * i; };
-    const int t = warp >> 2;        // tile
-    const int wq = warp & 3;        // quarter of the tile (TMEM lanes 32*wq ..)
-    const int r = wq * 32 + lane;   // row within the tile
-    const int row_g = m0 + t * kBlockM + r;
-    const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t s_taddr = tmem + lane_base + t * kBlockN;
-    const uint32_t o_taddr = tmem + lane_base + 2 * kBlockN + t * D;
-    const float c = p.c;
-    float* red = reinterpret_cast<float*>(smem + L::kRed);
+  const int t = warp >> 2;       // tile
+  const int wq = warp & 3;       // quarter of the tile (TMEM lanes 32 wq ..)
+  const int r = wq * 32 + lane;  // row within the tile
+  const int row_g = m0 + t * kBlockM + r;
+  const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
+  const uint32_t s_taddr = tmem + lane_base + t * kBlockN;
+  const uint32_t o_taddr = tmem + lane_base + 2 * kBlockN + t * D;
+  const float c = p.c;
+  float* red = reinterpret_cast<float*>(smem + L::kRed);
+  const uint32_t gbar_id = 1 + 4 * t + (kX == 64 ? (wq >> 1) : 0);
+  constexpr uint32_t kGbarN = kX == 64 ? 64 : 128;
+  const bool mma_scale = kMmaScale && !exact;
 
-    float M = -INFINITY;      // offset of the exponent, binades (exact row max * c in vec mode)
-    float m_row = -INFINITY;  // exact running row maximum, raw logits
-    float l = 0.f;            // running row sum
-    float delta = 0.f;        // tensorized: rounding of each tile's dominant term
-    // A warp whose bounded wait ran out turns "dead": it stops touching TMEM
-    // and barriers of the pipeline, but keeps joining the named barrier of
-    // its X-row group every iteration, so no other warp can be left waiting
-    // there; the OR on that barrier spreads the abort to the whole group.
-    bool dead = false;
-    const bool group_exchange = tensor_pass && X > 32;
-    const uint32_t gbar_id = 1 + 4 * t + (X == 64 ? (wq >> 1) : 0);
-    const uint32_t gbar_n = X == 64 ? 64 : 128;
-
-    for (int j = 0; j < n_kv; ++j) {
-      const int it = it0 + j;
-      const uint32_t par = it & 1;
-      if (!dead)
-        dead = !__all_sync(0xffffffffu, wait_bounded(bar(L::bSFull + t), par, p, abort_flag));
-      uint32_t s[4][32];
-      float rowmax = -INFINITY, tmax = -INFINITY;
+  float M = -INFINITY;      // offset of the exponent, binades (exact row max * c in vec mode)
+  float m_row = -INFINITY;  // exact running row maximum, raw logits
+  float l = 0.f;            // running row sum
+  float delta = 0.f;        // tensorized row sum: rounding of each tile's dominant term
+  bool dead = false;        // a bounded wait of this warp (or of its X-row group) ran out
+  int j = 0;
+  for (; j < n_kv; ++j) {
+    const int it = it0 + j;
+    const uint32_t par = it & 1;
+    dead = !__all_sync(0xffffffffu, wait_bounded(bar(L::bSFull + t), par, p, abort_flag));
+    if (wq == 0 && lane == 0) trace_mark(p, 0, t, j, pass);
+    uint32_t s[4][32];
+    float rowmax = -INFINITY;
+    if (!dead) {
+      tc_fence_after();
+#pragma unroll
+      for (int k = 0; k < 4; ++k) tmem_ld32(s_taddr + 32 * k, s[k]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) tmem_wait_ld(s[k]);
+      // mask: keys >= N, keys after the query (causal), padding rows
+      const int kv0 = j * kBlockN;
+      const int limit = (row_g < p.N) ? (p.causal ? min(p.N, row_g + 1) : p.N) - kv0 : 0;
+      if (limit < kBlockN) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (32 * k + i >= limit) s[k][i] = __float_as_uint(-INFINITY);
+      }
+      // row maximum as a tree of independent 3-input maxima
+      float mx[8];
+#pragma unroll
+      for (int a = 0; a < 8; ++a) {
+        const int k = a >> 1, b = (a & 1) * 16;
+        mx[a] = fmax3(__uint_as_float(s[k][b]), __uint_as_float(s[k][b + 1]),
+                      __uint_as_float(s[k][b + 2]));
+#pragma unroll
+        for (int i = 3; i < 15; i += 2)
+          mx[a] = fmax3(mx[a], __uint_as_float(s[k][b + i]), __uint_as_float(s[k][b + i + 1]));
+        mx[a] = fmaxf(mx[a], __uint_as_float(s[k][b + 15]));
+      }
+      rowmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7])));
+      m_row = fmaxf(m_row, rowmax);
+    }
+    // Algorithm 1 step 1: maximum of the row maxima over the X-row tile
+    float tmax = rowmax;
+    if constexpr (kX == 16) {
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
+    } else if constexpr (kX >= 32) {
+      tmax = warp_max(rowmax);
+    }
+    if constexpr (kGroup) {
+      // X = 64 / 128: combine the warps of the X-row group.  Every warp of the
+      // group joins this barrier once per K/V tile, aborted or not (see the
+      // drain loop below), and the OR spreads an abort to the whole group.
+      float* slot = red + (t * 2 + par) * 4;
+      if (lane == 0) slot[wq] = tmax;
+      dead = named_bar_or(gbar_id, kGbarN, dead);
       if (!dead) {
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < 4; ++k) tmem_ld32(s_taddr + 32 * k, s[k]);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) tmem_wait_ld(s[k]);
-
-        // mask: keys >= N, keys after the query (causal), padding rows
-        const int kv0 = j * kBlockN;
-        const int limit = (row_g < p.N) ? (p.causal ? min(p.N, row_g + 1) : p.N) - kv0 : 0;
-        if (limit < kBlockN) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-#pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (32 * k + i >= limit) s[k][i] = __float_as_uint(-INFINITY);
-        }
-        // row maximum as a tree of independent 3-input maxima
-        float mx[8];
-#pragma unroll
-        for (int a = 0; a < 8; ++a)
-          mx[a] = fmax3(__uint_as_float(s[a >> 1][(a & 1) * 16]),
-                        __uint_as_float(s[a >> 1][(a & 1) * 16 + 1]),
-                        __uint_as_float(s[a >> 1][(a & 1) * 16 + 2]));
-#pragma unroll
-        for (int a = 0; a < 8; ++a) {
-          const int k = a >> 1, b = (a & 1) * 16;
-#pragma unroll
-          for (int i = 3; i < 15; i += 2)
-            mx[a] = fmax3(mx[a], __uint_as_float(s[k][b + i]), __uint_as_float(s[k][b + i + 1]));
-          mx[a] = fmaxf(mx[a], __uint_as_float(s[k][b + 15]));
-        }
-        rowmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7])));
-        m_row = fmaxf(m_row, rowmax);
-        if (tensor_pass) {
-          // Algorithm 1 step 1, within the warp: max of the row maxima over
-          // the X-row tile (X = 16: half warps; X >= 32: the whole warp)
-          if (X == 1) {
-            tmax = rowmax;  // one-row tiles: the exact maximum (the fallback pass)
-          } else if (X == 16) {
-            tmax = rowmax;
-#pragma unroll
-            for (int o = 1; o < 16; o <<= 1) tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-          } else {
-            tmax = warp_max(rowmax);
-          }
-        }
-      }
-      if (group_exchange) {
-        // X = 64 / 128: combine the warps of the X-row group
-        float* slot = red + (t * 2 + par) * 4;
-        if (lane == 0) slot[wq] = tmax;
-        dead = named_bar_or(gbar_id, gbar_n, dead);
-        if (!dead) {
-          const int g0 = (X == 64) ? (wq & 2) : 0;
-          tmax = fmaxf(tmax, fmaxf(slot[g0], slot[g0 + 1]));
-          if (X == 128) tmax = fmaxf(tmax, fmaxf(slot[2], slot[3]));
-        }
-      }
-      if (dead) {
-        if (group_exchange) continue;
-        break;
-      }
-
-      float M_new;
-      if (tensor_pass) {
-        // the surrogate maximum is kept as a whole number of binades so the
-        // rescale factor of steps 2-3 is an exact power of two
-        const float Mc = (tmax == -INFINITY) ? -INFINITY : ceilf(tmax * c);
-        M_new = fmaxf(M, Mc);
-      } else {
-        M_new = (m_row == -INFINITY) ? -INFINITY : m_row * c;
-      }
-
-      // Algorithm 1 steps 2-3 factor: exp(m_old - m_new), one exact power
-      // of two per X-row tile (exact per-row factor in the vector variant).
-      const bool grow = j > 0 && M_new > M;
-      const float alpha = (M_new == -INFINITY) ? 1.f : ex2_approx(M - M_new);
-      if (j > 0) {
-        l *= alpha;
-        if (kLTensor) delta *= alpha;
-      }
-      // With X = 128 the whole 128-row tile shares the factor 2^-k, and the
-      // tensor pipe applies it inside the next O += P V (scale-input-d);
-      // other cases rescale O in TMEM from the vector side below.
-      bool vec_rescale = grow;
-      if (tensor_pass && X == 128 && !kE4M3) {
-        int kscale = 0;
-        if (grow && M_new - M <= 15.f) {
-          kscale = static_cast<int>(M_new - M);
-          vec_rescale = false;
-        }
-        if (wq == 0 && lane == 0) misc[4 + t] = static_cast<uint32_t>(kscale);
-      }
-      M = M_new;
-      const float neg_M = (M == -INFINITY) ? 0.f : -M;
-
-      // steps 4-6: Z = c S - m_hat, P~ = exp2(Z), stored as bf16 (e4m3) over S
-      const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(neg_M + kKappa, neg_M + kKappa);
-      uint64_t acc2[4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a) acc2[a] = f2_pack(0.f, 0.f);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        float pf[32];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint64_t z = f2_fma(f2_pack(__uint_as_float(s[k][2 * i]),
-                                            __uint_as_float(s[k][2 * i + 1])), c2, nm2);
-          float z0, z1;
-          f2_unpack(z, z0, z1);
-          pf[2 * i] = ex2_approx(z0);
-          pf[2 * i + 1] = ex2_approx(z1);
-          if (!(kLTensor && tensor_pass))
-            acc2[i & 3] = f2_add(acc2[i & 3], f2_pack(pf[2 * i], pf[2 * i + 1]));
-        }
-        if constexpr (kE4M3) {
-          uint32_t pk[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            pk[i] = pack_e4m3x4(pf[4 * i], pf[4 * i + 1], pf[4 * i + 2], pf[4 * i + 3]);
-          tmem_st8(s_taddr + 8 * k, pk);
+        if constexpr (kX == 64) {
+          tmax = fmaxf(slot[wq & 2], slot[(wq & 2) + 1]);
         } else {
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(pf[2 * i], pf[2 * i + 1]);
-          tmem_st16(s_taddr + 16 * k, pk);
+          tmax = fmaxf(fmaxf(slot[0], slot[1]), fmaxf(slot[2], slot[3]));
         }
-      }
-      // steps 2-3 on the vector side: O <- alpha O in TMEM.  PV_{j-1} has
-      // completed (issued before S_j, whose completion we waited for) and
-      // PV_j waits for this warpgroup's P-full signal below.
-      if (__any_sync(0xffffffffu, vec_rescale)) {
-        const uint64_t a2 = f2_pack(alpha, alpha);
-#pragma unroll
-        for (int k = 0; k < D / 32; ++k) {
-          uint32_t ov[32];
-          tmem_ld32(o_taddr + 32 * k, ov);
-          tmem_wait_ld(ov);
-#pragma unroll
-          for (int i = 0; i < 32; i += 2) {
-            float o0, o1;
-            f2_unpack(f2_mul(f2_pack(__uint_as_float(ov[i]), __uint_as_float(ov[i + 1])), a2),
-                      o0, o1);
-            ov[i] = __float_as_uint(o0);
-            ov[i + 1] = __float_as_uint(o1);
-          }
-          tmem_st32(o_taddr + 32 * k, ov);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::bPFull + t));
-
-      if (kLTensor && tensor_pass) {
-        // step 7: the row sum comes from the tensor pipe (P~ times ones);
-        // the LSE also gets back the bf16 rounding of the dominant term.
-        if (rowmax != -INFINITY) {
-          const float pm = ex2_approx(fmaf(rowmax, c, neg_M + kKappa));
-          delta += pm - (kE4M3 ? e4m3_round(pm) : bf16_round(pm));
-        }
-        dead = !__all_sync(0xffffffffu, wait_bounded(bar(L::bRsFull + t), par, p, abort_flag));
-        if (dead) continue;
-        tc_fence_after();
-        uint32_t lt;
-        tmem_ld1(s_taddr + 64, lt);
-        tmem_wait_ld1(lt);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(L::bLFree + t));
-        l += __uint_as_float(lt);
-      } else {
-        float r0, r1;
-        f2_unpack(f2_add(f2_add(acc2[0], acc2[1]), f2_add(acc2[2], acc2[3])), r0, r1);
-        l += r0 + r1;
       }
     }
-    bool ok = !dead;
+    if (dead) break;
 
-    if (ok) ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bOFinal), pass & 1, p, abort_flag));
-    if (ok) {
-      tc_fence_after();
-      // detector for the all-underflow case: surrogate far above the exact
-      // maximum, or nothing left of the row sum
-      if (tensor_pass && pass == 0) {
-        const bool flagged =
-            row_g < p.N && (!(l > 0.f) || (M - m_row * c) > p.underflow_thresh);
-        const uint32_t ball = __ballot_sync(0xffffffffu, flagged);
-        if (ball != 0 && lane == 0) {
-          atomicOr(const_cast<uint32_t*>(misc + 2), 1u);
-          if (p.fallback_rows) atomicAdd(p.fallback_rows, __popc(ball));
-        }
+    float M_new;
+    if constexpr (kTensor) {
+      // the surrogate maximum is kept as a whole number of binades so the
+      // rescale factor of steps 2-3 is an exact power of two; the fallback
+      // pass uses one-row tiles (each row's own maximum)
+      const float tm = exact ? rowmax : tmax;
+      const float Mc = (tm == -INFINITY) ? -INFINITY : ceilf(tm * c);
+      M_new = fmaxf(M, Mc);
+    } else {
+      M_new = (m_row == -INFINITY) ? -INFINITY : m_row * c;
+    }
+
+    // Algorithm 1 steps 2-3 factor: exp(m_old - m_new), one exact power of
+    // two per X-row tile (exact per-row factor in the vector variant).
+    const bool grow = j > 0 && M_new > M;
+    const float alpha = (M_new == -INFINITY) ? 1.f : ex2_approx(M - M_new);
+    if (j > 0) {
+      l *= alpha;
+      if (kLTensor) delta *= alpha;
+    }
+    // With X = 128 the whole 128-row tile shares the factor 2^-k and the
+    // tensor pipe applies it inside the next O += P V (scale-input-d); other
+    // cases rescale O in TMEM from the vector side below.
+    bool vec_rescale = grow;
+    if constexpr (kMmaScale) {
+      int kscale = 0;
+      if (mma_scale && grow && M_new - M <= 15.f) {
+        kscale = static_cast<int>(M_new - M);
+        vec_rescale = false;
       }
-      // epilogue: O / l and LSE
-      const float inv_l = p.v_scale / l;
-      float* orow = p.o + (static_cast<size_t>(bh) * p.N + row_g) * D;
+      if (wq == 0 && lane == 0) misc[4 + t] = static_cast<uint32_t>(kscale);
+    }
+    M = M_new;
+    const float neg_M = (M == -INFINITY) ? 0.f : -M;
+    if (wq == 0 && lane == 0) trace_mark(p, 1, t, j, pass);
+
+    // steps 4-6: Z = c S - m_hat, P~ = exp2(Z), stored as bf16 (e4m3) over S
+    const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(neg_M + kKappa, neg_M + kKappa);
+    uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float pf[32];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint64_t z = f2_fma(f2_pack(__uint_as_float(s[k][2 * i]),
+                                          __uint_as_float(s[k][2 * i + 1])), c2, nm2);
+        float z0, z1;
+        f2_unpack(z, z0, z1);
+        pf[2 * i] = ex2_approx(z0);
+        pf[2 * i + 1] = ex2_approx(z1);
+        if (!kLTensor) acc2[i & 1] = f2_add(acc2[i & 1], f2_pack(pf[2 * i], pf[2 * i + 1]));
+      }
+      if constexpr (kE4M3) {
+        uint32_t pk[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          pk[i] = pack_e4m3x4(pf[4 * i], pf[4 * i + 1], pf[4 * i + 2], pf[4 * i + 3]);
+        tmem_st8(s_taddr + 8 * k, pk);
+      } else {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(pf[2 * i], pf[2 * i + 1]);
+        tmem_st16(s_taddr + 16 * k, pk);
+      }
+    }
+    // steps 2-3 on the vector side: O <- alpha O in TMEM.  PV_{j-1} has
+    // completed (issued before S_j, whose completion was awaited) and PV_j
+    // waits for this warpgroup's P-full signal below.
+    if (__any_sync(0xffffffffu, vec_rescale)) {
+      const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
       for (int k = 0; k < D / 32; ++k) {
         uint32_t ov[32];
         tmem_ld32(o_taddr + 32 * k, ov);
         tmem_wait_ld(ov);
-        if (row_g < p.N) {
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            float4 v4 = make_float4(__uint_as_float(ov[i]) * inv_l, __uint_as_float(ov[i + 1]) * inv_l,
-                                    __uint_as_float(ov[i + 2]) * inv_l, __uint_as_float(ov[i + 3]) * inv_l);
-            *reinterpret_cast<float4*>(orow + 32 * k + i) = v4;
-          }
+        for (int i = 0; i < 32; i += 2) {
+          float o0, o1;
+          f2_unpack(f2_mul(f2_pack(__uint_as_float(ov[i]), __uint_as_float(ov[i + 1])), a2), o0,
+                    o1);
+          ov[i] = __float_as_uint(o0);
+          ov[i + 1] = __float_as_uint(o1);
         }
-      }
-      if (row_g < p.N) {
-        const float lsum = (kLTensor && tensor_pass) ? l + delta : l;
-        p.lse[static_cast<size_t>(bh) * p.N + row_g] = (M - kKappa + __log2f(lsum)) * kLn2;
+        tmem_st32(o_taddr + 32 * k, ov);
       }
     }
+    tmem_wait_st();
     tc_fence_before();
+    __syncwarp();
+    if (wq == 0 && lane == 0) trace_mark(p, 2, t, j, pass);
+    if (lane == 0) mbar_arrive(bar(L::bPFull + t));
+
+    if constexpr (kLTensor) {
+      // step 7 on the tensor pipe (P~ times ones, S column 64); the LSE also
+      // gets back the rounding of the tile's dominant term
+      if (rowmax != -INFINITY) {
+        const float pm = ex2_approx(fmaf(rowmax, c, neg_M + kKappa));
+        delta += pm - (kE4M3 ? e4m3_round(pm) : bf16_round(pm));
+      }
+      dead = !__all_sync(0xffffffffu, wait_bounded(bar(L::bRsFull + t), par, p, abort_flag));
+      if (dead) break;
+      tc_fence_after();
+      uint32_t lt;
+      tmem_ld1(s_taddr + 64, lt);
+      tmem_wait_ld1(lt);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::bLFree + t));
+      l += __uint_as_float(lt);
+    } else {
+      float r0, r1;
+      f2_unpack(f2_add(acc2[0], acc2[1]), r0, r1);
+      l += r0 + r1;
+    }
+  }
+  if constexpr (kGroup) {
+    // an aborted warp left the loop at K/V tile j after joining the group
+    // barriers of tiles 0..j; it joins the remaining ones so the other warps
+    // of the group are never left waiting there
+    if (dead) {
+      for (++j; j < n_kv; ++j) named_bar_or(gbar_id, kGbarN, true);
+    }
+  }
+
+  bool ok = !dead;
+  if (ok) ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bOFinal), pass & 1, p, abort_flag));
+  if (ok) {
+    tc_fence_after();
+    // detector for the all-underflow case: surrogate far above the exact
+    // maximum, or nothing left of the row sum
+    if (kTensor && pass == 0) {
+      const bool flagged = row_g < p.N && (!(l > 0.f) || (M - m_row * c) > p.underflow_thresh);
+      const uint32_t ball = __ballot_sync(0xffffffffu, flagged);
+      if (ball != 0 && lane == 0) {
+        atomicOr(const_cast<uint32_t*>(misc + 2), 1u);
+        if (p.fallback_rows) atomicAdd(p.fallback_rows, __popc(ball));
+      }
+    }
+    // epilogue: O / l and LSE
+    const float inv_l = p.v_scale / l;
+    float* orow = p.o + (static_cast<size_t>(bh) * p.N + row_g) * D;
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) {
+      uint32_t ov[32];
+      tmem_ld32(o_taddr + 32 * k, ov);
+      tmem_wait_ld(ov);
+      if (row_g < p.N) {
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const float4 v4 =
+              make_float4(__uint_as_float(ov[i]) * inv_l, __uint_as_float(ov[i + 1]) * inv_l,
+                          __uint_as_float(ov[i + 2]) * inv_l, __uint_as_float(ov[i + 3]) * inv_l);
+          *reinterpret_cast<float4*>(orow + 32 * k + i) = v4;
+        }
+      }
+    }
+    if (r == 0 && t == 0 && pass == 0 && p.trace != nullptr && blockIdx.x == 0)
+      p.trace[kTraceWords - 1] = static_cast<unsigned long long>(clock64());
+    if (row_g < p.N) {
+      const float lsum = kLTensor ? l + delta : l;
+      p.lse[static_cast<size_t>(bh) * p.N + row_g] = (M - kKappa + __log2f(lsum)) * kLn2;
+    }
+  }
+  tc_fence_before();
 }
 
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
-// kTensor:  surrogate maximum over X-row tiles (Algorithm 1); otherwise the
-//           exact per-row maximum (vector-softmax ablation).
+// kX:       > 0: surrogate maximum over kX-row tiles (Algorithm 1);
+//           0: the exact per-row maximum (vector-softmax ablation).
 // kLTensor: (kTensor only) the row sum of step 7 on the tensor pipe as
 //           P~ (bf16) times a block of ones; otherwise an fp32 sum of the
 //           unrounded P~ on the vector units.
 // kE4M3:    e4m3 inputs, kind::f8f6f4 MMAs, e4m3 P~ (otherwise bf16).
-template <int D, bool kTensor, bool kLTensor, bool kE4M3>
+template <int D, int kX, bool kLTensor, bool kE4M3>
 __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = Smem<D, kE4M3>;
   constexpr int S = L::kStages;
+  constexpr bool kTensor = kX > 0;
+  // X = 128 (bf16): the uniform rescale of O rides in the PV MMA
+  constexpr bool kMmaScale = kX == 128 && !kE4M3;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -470,6 +491,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
+  if (threadIdx.x == 0 && p.trace != nullptr && blockIdx.x == 0)
+    p.trace[kTraceWords - 2] = static_cast<unsigned long long>(clock64());
 
   // Registers: the control warpgroup (TMA, MMA) gives registers back and the
   // softmax warpgroups take them.  Each role runs its own loop over the
@@ -546,7 +569,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
               // P~ packs 2 (bf16) or 4 (e4m3) keys per TMEM column: 8 columns per K step
               const uint32_t d_t = tmem + 2 * kBlockN + t * D, a_t = tmem + t * kBlockN + kk * 8;
               const uint64_t bd = sdesc_sw128(va + kk * L::kPvStep, 16384, 1024);
-              if (!kE4M3 && kk == 0 && acc && kscale > 0)
+              if (kMmaScale && kk == 0 && acc && kscale > 0)
                 mma_ts_scale_rt(d_t, a_t, bd, idesc_pv, kscale);
               else
                 mma_ts<kE4M3>(d_t, a_t, bd, idesc_pv, acc || kk > 0);
@@ -582,12 +605,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
             if (!(ok = wait_bounded(bar(L::bVFull + st), ph, p, abort_flag))) break;
             // tile 0
             if (!(ok = wait_bounded(bar(L::bPFull + 0), par, p, abort_flag))) break;
+            trace_mark(p, 3, 0, j, pass);
             tc_fence_after();
             if (kLTensor) {
               issue_rs(0);
               mma_commit(bar(L::bRsFull + 0));
             }
-            issue_pv(0, st, j > 0, tensor_pass ? static_cast<int>(pv_scale[0]) : 0);
+            issue_pv(0, st, j > 0, (kMmaScale && pass == 0) ? static_cast<int>(pv_scale[0]) : 0);
             if (more) {
               if (!(ok = wait_bounded(bar(L::bKFull + st1), ph1, p, abort_flag))) break;
               if (kLTensor && !(ok = wait_bounded(bar(L::bLFree + 0), par, p, abort_flag)))
@@ -596,14 +620,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
               issue_s(0, st1);
               mma_commit(bar(L::bSFull + 0));
             }
+            trace_mark(p, 4, 0, j, pass);
             // tile 1
             if (!(ok = wait_bounded(bar(L::bPFull + 1), par, p, abort_flag))) break;
+            trace_mark(p, 3, 1, j, pass);
             tc_fence_after();
             if (kLTensor) {
               issue_rs(1);
               mma_commit(bar(L::bRsFull + 1));
             }
-            issue_pv(1, st, j > 0, tensor_pass ? static_cast<int>(pv_scale[1]) : 0);
+            issue_pv(1, st, j > 0, (kMmaScale && pass == 0) ? static_cast<int>(pv_scale[1]) : 0);
             mma_commit(bar(L::bVEmpty + st));
             if (more) {
               if (kLTensor && !(ok = wait_bounded(bar(L::bLFree + 1), par, p, abort_flag)))
@@ -613,6 +639,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
               mma_commit(bar(L::bSFull + 1));
               mma_commit(bar(L::bKEmpty + st1));
             }
+            trace_mark(p, 4, 1, j, pass);
           }
           if (ok) {
             mma_commit(bar(L::bOFinal));
@@ -638,8 +665,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
       // tiles, X = 1: every row's own maximum rounded up to a whole binade,
       // so no row can underflow (the vector fallback of the page's
       // all-underflow discussion, on the same code path).
-      softmax_role<D, kTensor, kLTensor, kE4M3>(p, smem, sb, tmem, misc, warp, lane, m0, bh, n_kv,
-                                               it0, pass, pass == 0 ? p.X : 1);
+      softmax_role<D, kX, kLTensor, kE4M3>(p, smem, sb, tmem, misc, warp, lane, m0, bh, n_kv, it0,
+                                           pass, /*exact=*/pass == 1);
       __syncthreads();
       if (!kTensor || misc[2] == 0u || *abort_flag != 0u) break;
     }
