@@ -183,6 +183,42 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def phase_trace(fat, torch, w, dev, variant, l_mode, stream, sm_mhz, peak_tflops):
+    """One traced launch: per-iteration clock stamps of the first thread block.
+
+    Returns the median steady-state iteration period (both query tiles), the
+    median softmax time per tile (S received -> P published), and the
+    vector-interval ratio: the share of an iteration in which the tensor pipe
+    has no work because it waits for the softmax, estimated as
+    1 - (ideal tensor cycles of the iteration) / (measured period), with the
+    ideal cycles from the measured dense peak at the sampled SM clock.
+    """
+    import numpy as np
+
+    I = fat.TRACE_ITERS
+    tr = torch.zeros(fat.TRACE_WORDS, dtype=torch.int64, device=dev["q"].device)
+    with torch.cuda.stream(stream):
+        fat.attn_fwd(dev["q"], dev["k"], dev["v"], w.causal, w.scale, w.X, variant=variant,
+                     l_mode=l_mode, stream=stream, trace=tr)
+    stream.synchronize()
+    t = tr.cpu().numpy().astype(np.int64)
+    ev = t[:10 * I].reshape(5, 2, I)
+    n = int((ev[0, 0] > 0).sum())
+    if n < 12:
+        return None
+    mid = slice(4, n - 3)
+    period = float(np.median(np.diff(ev[3, 0])[mid]))
+    softmax = float(np.median((ev[2] - ev[0])[:, mid]))
+    out = {"period_cycles": period, "softmax_cycles": softmax, "iterations": n}
+    if sm_mhz:
+        n_sm = torch.cuda.get_device_properties(dev["q"].device).multi_processor_count
+        flop_per_clk = peak_tflops * 1e12 / (n_sm * sm_mhz * 1e6)
+        ideal = 2 * 4.0 * 128 * 128 * w.d / flop_per_clk  # PV + S for both tiles
+        out["ideal_tensor_cycles"] = ideal
+        out["vector_interval_ratio"] = max(0.0, 1.0 - ideal / period)
+    return out
+
+
 def config_dict(w, variant):
     return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
             "X": w.X, "dtype": w.dtype, "variant": variant,
@@ -327,6 +363,14 @@ def main():
         e2e = {"value": w.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
+    traces = None
+    if w.dtype == "bf16" and w.N >= 2048:
+        mhz = (clocks or {}).get("sm_mhz")
+        traces = {"tensor": phase_trace(fat, torch, w, dev, "tensor", "vector", stream, mhz,
+                                        peaks["bf16_tflops"]),
+                  "vec": phase_trace(fat, torch, w, dev, "vec", "vector", stream, mhz,
+                                     peaks["bf16_tflops"])}
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = cpu_oracle_sample(w, inp)
@@ -342,7 +386,7 @@ def main():
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
                          "peak_source": f"{peaks['source']} bf16 dense (burst)"},
-            "ablation": ablation, "e2e": e2e, "cpu_baseline": cpu,
+            "ablation": ablation, "phase_trace": traces, "e2e": e2e, "cpu_baseline": cpu,
             "gpu_launches": args.steps, "clocks": clocks,
             "wall_s_timed_region": wall,
         }

@@ -364,7 +364,7 @@ __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, boo
 // Maximum over the 32 lanes of the warp (NaN inputs ignored).
 __device__ __forceinline__ float warp_max(float x) {
   float r;
-  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+  asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
   return r;
 }
 
