@@ -109,6 +109,23 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """Largest value over all ranks (the slowest rank's time); identity at N = 1."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world: int, flops_per_step: float, steps: int, max_total_ms: float) -> float:
+    """Every rank runs its own replica of the workload (weak scaling): the
+    whole job processes world * steps workloads in the slowest rank's time."""
+    return world * flops_per_step * steps / (max_total_ms * 1e-3) / 1e12
+
+
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -174,7 +191,7 @@ def run_reference(args, w):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / len(per_step), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_dict(w, "oracle"),
+        "config": config_dict(w, "oracle", l2="n/a (host cores)"),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"each step: 1/8 of the rows of one head of {w.name}"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -219,10 +236,9 @@ def phase_trace(fat, torch, w, dev, variant, l_mode, stream, sm_mhz, peak_tflops
     return out
 
 
-def config_dict(w, variant):
+def config_dict(w, variant, l2="flushed before every timed step (256 MiB write)"):
     return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
-            "X": w.X, "dtype": w.dtype, "variant": variant,
-            "l2": "flushed before every timed step (256 MiB write)"}
+            "X": w.X, "dtype": w.dtype, "variant": variant, "l2": l2}
 
 
 def time_variant(fat, torch, w, dev, args, variant, flush, stream, l_mode="vector"):
@@ -317,12 +333,8 @@ def main():
     times, wall, clocks = timed("tensor", True)
     if fat.check_device_error(stream) != fat.FAT_OK:
         raise SystemExit("device error word set during the timed run")
-    total_ms = sum(times)
-    if pg:
-        t = torch.tensor([total_ms], device=device)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * w.flops * args.steps / (total_ms * 1e-3) / 1e12
+    total_ms = max_over_ranks(sum(times), pg, device)
+    value = whole_job_tflops(world, w.flops, args.steps, total_ms)
     avg_ms = total_ms / args.steps
     achieved = w.flops / (avg_ms * 1e-3) / 1e12
 
