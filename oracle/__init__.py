@@ -7,6 +7,7 @@ reference leg may import this package.  The product path (the CUDA library and
 It wraps ``oracle.c`` (plain C, double precision, pthreads) through ctypes:
 
 * :func:`attn_fwd`       -- the plain definition of softmax attention (the oracle);
+* :func:`attn_fwd_qk`    -- the same for Nq query rows against Nk keys;
 * :func:`attn_naive`     -- brute force in long double, full S materialised;
 * :func:`attn_surrogate` -- Algorithm 1 of "FlashAttention-T: Towards Fully
   Tensorized Attention by Exploiting Tensor-Vector Parallelism" (section A2,
@@ -58,6 +59,9 @@ def load(path: str = _SO):
     lib.oracle_attn_fwd.restype = ctypes.c_int
     lib.oracle_attn_fwd.argtypes = [_D, _D, _D, _D, _D, _L, _L, _L, _L, ctypes.c_int,
                                     ctypes.c_double, _L, _L, _L, ctypes.c_int]
+    lib.oracle_attn_fwd_qk.restype = ctypes.c_int
+    lib.oracle_attn_fwd_qk.argtypes = [_D, _D, _D, _D, _D, _L, _L, _L, _L, _L, ctypes.c_int,
+                                       ctypes.c_double, _L, _L, _L, ctypes.c_int]
     lib.oracle_attn_naive.restype = ctypes.c_int
     lib.oracle_attn_naive.argtypes = [_D, _D, _D, _D, _D, _L, _L, _L, _L, ctypes.c_int,
                                       ctypes.c_double]
@@ -115,6 +119,29 @@ def attn_fwd(q, k, v, causal: bool, scale: float, rows: slice | None = None,
                              int(bool(causal)), float(scale), rb, re_, rs, int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle_attn_fwd failed ({rc})")
+    return o, lse
+
+
+def attn_fwd_qk(q, k, v, causal: bool, scale: float, rows: slice | None = None,
+                nthreads: int = 0, lib=None):
+    """Plain softmax attention of Nq query rows against Nk keys, in double.
+
+    q: [B, H, Nq, d]; k, v: [B, H, Nk, d].  Causal keeps key j for query i iff
+    j <= i + Nk - Nq (the queries are the last Nq positions).
+    """
+    lib = lib or _get()
+    q, k, v = _as_f64(q), _as_f64(k), _as_f64(v)
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if k.shape != (B, H, Nk, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, H, Nk, d] with q's B, H, d")
+    o = np.full((B, H, Nq, d), np.nan)
+    lse = np.full((B, H, Nq), np.nan)
+    rb, re_, rs = (0, Nq, 1) if rows is None else rows.indices(Nq)
+    rc = lib.oracle_attn_fwd_qk(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, Nq, Nk, d,
+                                int(bool(causal)), float(scale), rb, re_, rs, int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_attn_fwd_qk failed ({rc})")
     return o, lse
 
 

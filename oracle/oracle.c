@@ -17,8 +17,10 @@
  *     any-overflow / all-underflow discussion, and Algorithm 1 steps 1-7.
  *   - section A4 results, Fig. 11: accuracy is judged against an FP64 attention.
  *
- * Three functions live here:
- *   oracle_attn_fwd       the plain definition in double precision (the oracle);
+ * Functions:
+ *   oracle_attn_fwd_qk    the plain definition in double precision (the oracle),
+ *                         Nq query rows against Nk keys;
+ *   oracle_attn_fwd       the same with Nq = Nk;
  *   oracle_attn_naive     brute force in long double with the full S matrix
  *                         materialised and sorted summation (pins the oracle);
  *   oracle_attn_surrogate the blocked online algorithm with the surrogate
@@ -67,14 +69,17 @@ int oracle_available_cores(void) {
  *   l_i   = sum_j exp(s_j - m_i)
  *   O_i   = (sum_j exp(s_j - m_i) v_j) / l_i
  *   LSE_i = m_i + ln(l_i)
- * with J_i = {0..N-1}, or {0..i} when causal.  Rows listed by
+ * with Nq query rows and Nk keys per (b, h); J_i = {0..Nk-1}, or, causal,
+ * {0..i + Nk - Nq}: the queries are the last Nq positions of the key
+ * sequence (for Nq = Nk this is the ordinary j <= i).  Rows listed by
  * [row_begin, row_end) with stride row_step are computed, in every (b, h);
- * other rows of o / lse are left untouched.
+ * other rows of o / lse are left untouched.  q, o: [B, H, Nq, d]; k, v:
+ * [B, H, Nk, d]; lse: [B, H, Nq].
  */
 typedef struct {
     const double *q, *k, *v;
     double *o, *lse;
-    long B, H, N, d;
+    long B, H, Nq, Nk, d;
     int causal;
     double scale;
     long row_begin, row_end, row_step;
@@ -83,11 +88,12 @@ typedef struct {
 } exact_job;
 
 static void exact_row(const exact_job *jb, long bh, long i, double *s) {
-    const long N = jb->N, d = jb->d;
-    const double *qi = jb->q + (bh * N + i) * d;
+    const long N = jb->Nk, d = jb->d;
+    const double *qi = jb->q + (bh * jb->Nq + i) * d;
     const double *kb = jb->k + bh * N * d;
     const double *vb = jb->v + bh * N * d;
-    const long nkeys = jb->causal ? i + 1 : N;
+    long nkeys = jb->causal ? i + 1 + (jb->Nk - jb->Nq) : N;
+    if (nkeys > N) nkeys = N;
     double m = -INFINITY;
     for (long j = 0; j < nkeys; ++j) {
         const double *kj = kb + j * d;
@@ -101,7 +107,7 @@ static void exact_row(const exact_job *jb, long bh, long i, double *s) {
         s[j] = exp(s[j] - m); /* s now holds the unnormalised weights */
         l += s[j];
     }
-    double *oi = jb->o + (bh * N + i) * d;
+    double *oi = jb->o + (bh * jb->Nq + i) * d;
     for (long c = 0; c < d; ++c) oi[c] = 0.0;
     for (long j = 0; j < nkeys; ++j) {
         const double *vj = vb + j * d;
@@ -109,12 +115,12 @@ static void exact_row(const exact_job *jb, long bh, long i, double *s) {
         for (long c = 0; c < d; ++c) oi[c] += w * vj[c];
     }
     for (long c = 0; c < d; ++c) oi[c] /= l;
-    jb->lse[bh * N + i] = m + log(l);
+    jb->lse[bh * jb->Nq + i] = m + log(l);
 }
 
 static void *exact_worker(void *arg) {
     const exact_job *jb = (const exact_job *)arg;
-    double *s = (double *)malloc(sizeof(double) * (size_t)(jb->N > 0 ? jb->N : 1));
+    double *s = (double *)malloc(sizeof(double) * (size_t)(jb->Nk > 0 ? jb->Nk : 1));
     if (!s) return (void *)1;
     for (long t = jb->task_begin; t < jb->task_end; t += jb->task_stride) {
         const long bh = t / jb->n_rows_per_bh;
@@ -126,21 +132,22 @@ static void *exact_worker(void *arg) {
     return NULL;
 }
 
-int oracle_attn_fwd(const double *q, const double *k, const double *v, double *o, double *lse,
-                    long B, long H, long N, long d, int causal, double scale,
-                    long row_begin, long row_end, long row_step, int nthreads) {
+int oracle_attn_fwd_qk(const double *q, const double *k, const double *v, double *o, double *lse,
+                       long B, long H, long Nq, long Nk, long d, int causal, double scale,
+                       long row_begin, long row_end, long row_step, int nthreads) {
     if (!q || !k || !v || !o || !lse) return -1;
-    if (B < 0 || H < 0 || N < 0 || d < 1) return -1;
+    if (B < 0 || H < 0 || Nq < 0 || Nk < 0 || d < 1) return -1;
+    if (causal && Nk < Nq) return -1; /* the first queries would see no key */
     if (row_step < 1) row_step = 1;
     if (row_begin < 0) row_begin = 0;
-    if (row_end > N || row_end < 0) row_end = N;
+    if (row_end > Nq || row_end < 0) row_end = Nq;
     if (row_end <= row_begin || B * H == 0) return 0;
     const long n_rows = (row_end - row_begin + row_step - 1) / row_step;
     const long n_tasks = B * H * n_rows;
     if (nthreads <= 0) nthreads = oracle_available_cores();
     if (nthreads > n_tasks) nthreads = (int)n_tasks;
 
-    exact_job base = {q, k, v, o, lse, B, H, N, d, causal, scale,
+    exact_job base = {q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale,
                       row_begin, row_end, row_step, n_rows, 0, 0, 1};
     exact_job *jobs = (exact_job *)calloc((size_t)nthreads, sizeof(exact_job));
     pthread_t *th = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
@@ -169,6 +176,14 @@ int oracle_attn_fwd(const double *q, const double *k, const double *v, double *o
     free(jobs);
     free(th);
     return rc;
+}
+
+/* Equal query and key lengths (the self-attention case). */
+int oracle_attn_fwd(const double *q, const double *k, const double *v, double *o, double *lse,
+                    long B, long H, long N, long d, int causal, double scale,
+                    long row_begin, long row_end, long row_step, int nthreads) {
+    return oracle_attn_fwd_qk(q, k, v, o, lse, B, H, N, N, d, causal, scale, row_begin, row_end,
+                              row_step, nthreads);
 }
 
 /* ------------------------------------------------------------------------ */

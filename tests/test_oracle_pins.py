@@ -248,14 +248,15 @@ def test_surrogate_reports_all_underflow():
 
 MUTANTS = {
     "scale_dropped": ("s[j] = jb->scale * dot;", "s[j] = dot;"),
-    "causal_off_by_one": ("const long nkeys = jb->causal ? i + 1 : N;",
-                          "const long nkeys = jb->causal ? i : N;"),
-    "lse_log2": ("jb->lse[bh * N + i] = m + log(l);", "jb->lse[bh * N + i] = m + log2(l);"),
-    "lse_max_dropped": ("jb->lse[bh * N + i] = m + log(l);", "jb->lse[bh * N + i] = log(l);"),
+    "causal_off_by_one": ("long nkeys = jb->causal ? i + 1 + (jb->Nk - jb->Nq) : N;",
+                          "long nkeys = jb->causal ? i + (jb->Nk - jb->Nq) : N;"),
+    "lse_log2": ("jb->lse[bh * jb->Nq + i] = m + log(l);",
+                 "jb->lse[bh * jb->Nq + i] = m + log2(l);"),
+    "lse_max_dropped": ("jb->lse[bh * jb->Nq + i] = m + log(l);", "jb->lse[bh * jb->Nq + i] = log(l);"),
     "no_normalisation": ("for (long c = 0; c < d; ++c) oi[c] /= l;", ""),
     "exp_sign": ("s[j] = exp(s[j] - m);", "s[j] = exp(m - s[j]);"),
     "q_k_swapped": ("dot += qi[c] * kj[c];",
-                    "dot += jb->k[(bh * N + i) * d + c] * jb->q[(bh * N + j) * d + c];"),
+                    "dot += jb->k[(bh * N + i) * d + c] * jb->q[(bh * jb->Nq + j) * d + c];"),
     "v_index": ("const double *vj = vb + j * d;", "const double *vj = vb + (N - 1 - j) * d;"),
     "v_transposed": ("for (long c = 0; c < d; ++c) oi[c] += w * vj[c];",
                      "for (long c = 0; c < d; ++c) oi[c] += w * vb[(c % N) * d + (j % d)];"),
@@ -282,3 +283,29 @@ def test_pins_catch_planted_mistake(name, tmp_path):
         except (AssertionError, RuntimeError, ValueError):
             failures += 1
     assert failures >= 1, f"no pin caught the planted mistake {name}"
+
+
+def test_rectangular_rows_equal_the_tail_of_a_square_problem():
+    """Nq queries against Nk keys (causal: the queries are the last Nq key
+    positions) give exactly the last Nq rows of the square problem, which is
+    itself pinned by brute force above."""
+    B, H, N, d = 2, 2, 70, 8
+    q, k, v = (_rand((B, H, N, d), 80 + i) for i in range(3))
+    for causal in (False, True):
+        o_sq, lse_sq = oracle.attn_naive(q, k, v, causal, 0.4)
+        for nq in (1, 5, 70):
+            o, lse = oracle.attn_fwd_qk(q[:, :, N - nq:], k, v, causal, 0.4)
+            np.testing.assert_allclose(o, o_sq[:, :, N - nq:], atol=1e-12)
+            np.testing.assert_allclose(lse, lse_sq[:, :, N - nq:], atol=1e-12)
+
+
+def test_rectangular_non_causal_ignores_key_order_and_rejects_short_causal():
+    q = _rand((1, 1, 3, 4), 90)
+    k, v = _rand((1, 1, 11, 4), 91), _rand((1, 1, 11, 4), 92)
+    perm = np.random.default_rng(4).permutation(11)
+    o, lse = oracle.attn_fwd_qk(q, k, v, False, 0.7)
+    op, lsep = oracle.attn_fwd_qk(q, k[:, :, perm], v[:, :, perm], False, 0.7)
+    np.testing.assert_allclose(op, o, atol=1e-12)
+    np.testing.assert_allclose(lsep, lse, atol=1e-12)
+    with pytest.raises(RuntimeError):
+        oracle.attn_fwd_qk(_rand((1, 1, 12, 4), 93), k, v, True, 0.7)
