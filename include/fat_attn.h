@@ -36,6 +36,8 @@
 #ifndef FAT_ATTN_H_
 #define FAT_ATTN_H_
 
+#include <stddef.h>
+
 #include <cuda_runtime_api.h>
 
 #ifdef __cplusplus
@@ -108,6 +110,33 @@ int fat_attn_fwd_vec(const void* q, const void* k, const void* v, float* o, floa
 int fat_attn_fwd_fp8(const void* q, const void* k, const void* v, float q_descale,
                      float k_descale, float v_descale, float* o, float* lse, int B, int H, int N,
                      int d, int causal, float scale, int X, cudaStream_t stream);
+
+/*
+ * Split-KV forward (decode and long-key shapes): Nq query rows against Nk
+ * keys per (b, h); q [B, H, Nq, d], k and v [B, H, Nk, d] (bf16), o fp32
+ * [B, H, Nq, d], lse fp32 [B, H, Nq].  Causal keeps key j for query i iff
+ * j <= i + Nk - Nq (the queries are the last Nq positions; requires
+ * Nk >= Nq).  The key range is cut into up to num_splits ranges of whole
+ * 128-key tiles (1 <= num_splits <= 64), each computed by its own thread
+ * blocks with the tensorized online softmax of fat_attn_fwd; their partial
+ * O and LSE go to `workspace` (device memory owned by the caller, at least
+ * fat_attn_splitkv_workspace_bytes(B, H, Nq, d, num_splits) bytes; may be
+ * NULL when a single range results) and are merged by LSE weights:
+ * LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s.  The merge is
+ * the exact identity behind the page's online softmax (per-block maxima
+ * and sums combined afterwards, section A3 / Fig. 2).  Calls sharing a
+ * workspace must not overlap on the device.
+ */
+int fat_attn_fwd_splitkv(const void* q, const void* k, const void* v, float* o, float* lse, int B,
+                         int H, int Nq, int Nk, int d, int causal, float scale, int X,
+                         int num_splits, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
+/* Workspace size for fat_attn_fwd_splitkv (0 for invalid arguments). */
+size_t fat_attn_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits);
+
+/* A split count giving about one thread block per SM of the current device. */
+int fat_attn_splitkv_default_splits(int B, int H, int Nq, int Nk);
 
 /* Every knob of the entry points above in one struct (tests and ablations). */
 typedef struct fat_params {

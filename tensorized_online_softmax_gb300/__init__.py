@@ -20,7 +20,7 @@ import threading
 from . import _build
 
 __all__ = [
-    "FatError", "load_library", "attn_fwd", "attn_fwd_vec", "attn_fwd_fp8",
+    "FatError", "load_library", "attn_fwd", "attn_fwd_vec", "attn_fwd_fp8", "attn_fwd_splitkv",
     "check_device_error", "status_string", "ABI_SYMBOLS", "FAT_OK",
     "FAT_ERR_INVALID_ARG", "FAT_ERR_UNSUPPORTED", "FAT_ERR_ALIGNMENT", "FAT_ERR_LAUNCH",
     "FAT_ERR_DEVICE_TIMEOUT", "FAT_ERR_ARCH",
@@ -42,7 +42,8 @@ TRACE_WORDS = 5 * 2 * TRACE_ITERS + 2
 
 # every extern "C" entry point declared in include/fat_attn.h
 ABI_SYMBOLS = (
-    "fat_attn_fwd", "fat_attn_fwd_vec", "fat_attn_fwd_fp8", "fat_attn_fwd_ex",
+    "fat_attn_fwd", "fat_attn_fwd_vec", "fat_attn_fwd_fp8", "fat_attn_fwd_splitkv",
+    "fat_attn_splitkv_workspace_bytes", "fat_attn_splitkv_default_splits", "fat_attn_fwd_ex",
     "fat_status_string", "fat_check_device_error",
 )
 
@@ -101,6 +102,13 @@ def load_library(build_if_missing: bool = True):
             getattr(lib, name).restype = I
         lib.fat_attn_fwd_fp8.argtypes = [P, P, P, F, F, F, P, P, I, I, I, I, I, F, I, P]
         lib.fat_attn_fwd_fp8.restype = I
+        lib.fat_attn_fwd_splitkv.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, I, P,
+                                             ctypes.c_size_t, P]
+        lib.fat_attn_fwd_splitkv.restype = I
+        lib.fat_attn_splitkv_workspace_bytes.argtypes = [I, I, I, I, I]
+        lib.fat_attn_splitkv_workspace_bytes.restype = ctypes.c_size_t
+        lib.fat_attn_splitkv_default_splits.argtypes = [I, I, I, I]
+        lib.fat_attn_splitkv_default_splits.restype = I
         lib.fat_attn_fwd_ex.argtypes = [ctypes.POINTER(FatParams)]
         lib.fat_attn_fwd_ex.restype = I
         lib.fat_status_string.argtypes = [I]
@@ -204,6 +212,50 @@ def attn_fwd_fp8(q, k, v, q_descale: float, k_descale: float, v_descale: float,
     """e4m3 inputs with per-tensor descales; fp32 accumulation and outputs."""
     return attn_fwd(q, k, v, causal, scale, X, dtype="e4m3",
                     descales=(q_descale, k_descale, v_descale), **kw)
+
+
+def attn_fwd_splitkv(q, k, v, causal: bool = False, scale: float | None = None, X: int = 128,
+                     num_splits: int | None = None, *, workspace=None, out=None, stream=None):
+    """Split-KV forward: q [B, H, Nq, d] against k, v [B, H, Nk, d] (bf16).
+
+    The key range is split across thread blocks and the partial results are
+    merged by LSE weights.  ``num_splits=None`` picks about one block per SM.
+    ``workspace`` (a CUDA uint8 tensor) is allocated here if not given.
+    Returns ``(o, lse)``.
+    """
+    import torch
+
+    lib = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be a bf16 CUDA tensor")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous 4-D tensor")
+    B, H, Nq, d = q.shape
+    Nk = k.shape[2]
+    if k.shape != (B, H, Nk, d) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, H, Nk, d] with q's B, H, d")
+    if scale is None:
+        scale = d ** -0.5
+    with torch.cuda.device(q.device):
+        if num_splits is None:
+            num_splits = lib.fat_attn_splitkv_default_splits(B, H, Nq, Nk)
+        nbytes = lib.fat_attn_splitkv_workspace_bytes(B, H, Nq, d, int(num_splits))
+        if workspace is None:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+        if out is None:
+            o = torch.empty((B, H, Nq, d), dtype=torch.float32, device=q.device)
+            lse = torch.empty((B, H, Nq), dtype=torch.float32, device=q.device)
+        else:
+            o, lse = out
+        st = lib.fat_attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                      lse.data_ptr(), B, H, Nq, Nk, d, int(bool(causal)),
+                                      float(scale), int(X), int(num_splits),
+                                      workspace.data_ptr(), workspace.numel(),
+                                      _stream_handle(stream))
+    if st != FAT_OK:
+        raise FatError(st, "fat_attn_fwd_splitkv")
+    return o, lse
 
 
 def check_device_error(stream=None) -> int:

@@ -98,28 +98,60 @@ const char* fat_status_string(int status) {
   }
 }
 
-int fat_attn_fwd_ex(const fat_params* p) {
+}  // extern "C"
+
+namespace {
+
+constexpr int kMaxSplits = 64;
+
+long long splitkv_bytes(long long BH, long long Nq, int d, int splits) {
+  return static_cast<long long>(splits) * BH * Nq * (d + 1) * 4 + 256;
+}
+
+// Shared body of every entry point: Nq query rows against Nk keys, the key
+// range cut into `splits` ranges (one thread-block row of the grid each) whose
+// partial results go to `workspace` and are merged afterwards.
+int run_fwd(const fat_params* p, int Nq, int Nk, int splits, void* workspace,
+            size_t workspace_bytes) {
   if (!p) return FAT_ERR_INVALID_ARG;
   // ---- synchronous validation: nothing is launched on failure ----
   if (!p->q || !p->k || !p->v || !p->o || !p->lse) return FAT_ERR_INVALID_ARG;
-  if (p->B < 1 || p->H < 1 || p->N < 1) return FAT_ERR_INVALID_ARG;
+  if (p->B < 1 || p->H < 1 || Nq < 1 || Nk < 1) return FAT_ERR_INVALID_ARG;
+  if (p->causal && Nk < Nq) return FAT_ERR_INVALID_ARG;  // early queries would see no key
   if (p->d != 64 && p->d != 128) return FAT_ERR_INVALID_ARG;
   if (p->X != 16 && p->X != 32 && p->X != 64 && p->X != 128) return FAT_ERR_INVALID_ARG;
   if (!(p->scale > 0.f) || !std::isfinite(p->scale)) return FAT_ERR_INVALID_ARG;
   if (p->variant != FAT_VARIANT_TENSOR && p->variant != FAT_VARIANT_VEC) return FAT_ERR_INVALID_ARG;
   if (p->dtype != FAT_DTYPE_BF16 && p->dtype != FAT_DTYPE_E4M3) return FAT_ERR_INVALID_ARG;
   if (p->l_mode != FAT_LMODE_VECTOR && p->l_mode != FAT_LMODE_TENSOR) return FAT_ERR_INVALID_ARG;
+  if (splits < 1 || splits > kMaxSplits) return FAT_ERR_INVALID_ARG;
   const long long BH = static_cast<long long>(p->B) * p->H;
-  const long long n_mblocks = (p->N + fat::kRowsPerCta - 1) / fat::kRowsPerCta;
+  const long long n_mblocks = (Nq + fat::kRowsPerCta - 1) / fat::kRowsPerCta;
   if (BH > (1ll << 30) || BH * n_mblocks > 0x7fffffffll) return FAT_ERR_INVALID_ARG;
   if (!aligned16(p->q) || !aligned16(p->k) || !aligned16(p->v) || !aligned16(p->o) ||
       !aligned16(p->lse))
     return FAT_ERR_ALIGNMENT;
+  if (p->trace && (reinterpret_cast<uintptr_t>(p->trace) & 7u)) return FAT_ERR_ALIGNMENT;
   const bool e4m3 = p->dtype == FAT_DTYPE_E4M3;
   if (e4m3) {
     for (float ds : {p->q_descale, p->k_descale, p->v_descale})
       if (!(ds > 0.f) || !std::isfinite(ds)) return FAT_ERR_INVALID_ARG;
     if (p->d != 128) return FAT_ERR_UNSUPPORTED;  // e4m3 rows must fill a 128-byte slab
+  }
+  // keys per split: a multiple of the 128-key tile; fewer splits may result
+  const int n_kv_tiles = (Nk + fat::kBlockN - 1) / fat::kBlockN;
+  const int tiles_per_split = (n_kv_tiles + splits - 1) / splits;
+  const int kv_split_len = tiles_per_split * fat::kBlockN;
+  const int n_splits = (Nk + kv_split_len - 1) / kv_split_len;
+  float* o_part = nullptr;
+  float* lse_part = nullptr;
+  if (n_splits > 1) {
+    if (!workspace) return FAT_ERR_INVALID_ARG;
+    if (static_cast<long long>(workspace_bytes) < splitkv_bytes(BH, Nq, p->d, n_splits))
+      return FAT_ERR_INVALID_ARG;
+    const uintptr_t base = (reinterpret_cast<uintptr_t>(workspace) + 255) & ~uintptr_t(255);
+    o_part = reinterpret_cast<float*>(base);
+    lse_part = o_part + static_cast<size_t>(n_splits) * BH * Nq * p->d;
   }
 
   int dev = 0;
@@ -128,19 +160,23 @@ int fat_attn_fwd_ex(const fat_params* p) {
 
   fat::FwdParams fp;
   const int elt = e4m3 ? 1 : 2;
-  if (!encode_qkv_map(&fp.tm_q, p->q, p->d, p->N, static_cast<int>(BH), elt) ||
-      !encode_qkv_map(&fp.tm_k, p->k, p->d, p->N, static_cast<int>(BH), elt) ||
-      !encode_qkv_map(&fp.tm_v, p->v, p->d, p->N, static_cast<int>(BH), elt))
+  if (!encode_qkv_map(&fp.tm_q, p->q, p->d, Nq, static_cast<int>(BH), elt) ||
+      !encode_qkv_map(&fp.tm_k, p->k, p->d, Nk, static_cast<int>(BH), elt) ||
+      !encode_qkv_map(&fp.tm_v, p->v, p->d, Nk, static_cast<int>(BH), elt))
     return FAT_ERR_LAUNCH;
   fp.o = p->o;
   fp.lse = p->lse;
   fp.fallback_rows = p->fallback_rows;
   fp.B = p->B;
   fp.H = p->H;
-  fp.N = p->N;
+  fp.Nq = Nq;
+  fp.Nk = Nk;
   fp.causal = p->causal ? 1 : 0;
   fp.X = p->X;
   fp.n_mblocks = static_cast<int>(n_mblocks);
+  fp.kv_split_len = kv_split_len;
+  fp.o_part = o_part;
+  fp.lse_part = lse_part;
   fp.scale = p->scale;
   // logits are scale * (q_descale * q_code) . (k_descale * k_code)
   fp.c = e4m3 ? p->scale * p->q_descale * p->k_descale * fat::kLog2e : p->scale * fat::kLog2e;
@@ -154,7 +190,6 @@ int fat_attn_fwd_ex(const fat_params* p) {
   fp.timeout_ns = p->wait_timeout_ns ? p->wait_timeout_ns : 4000000000ull;
   fp.trace = p->trace;
   fp.error_word = g_dev[dev].error_word;
-  if (p->trace && (reinterpret_cast<uintptr_t>(p->trace) & 7u)) return FAT_ERR_ALIGNMENT;
 
   const int grid = static_cast<int>(BH * n_mblocks);
   const bool tensor = p->variant == FAT_VARIANT_TENSOR;
@@ -162,15 +197,71 @@ int fat_attn_fwd_ex(const fat_params* p) {
   const int X = tensor ? p->X : 0;  // X = 0: the vector-softmax kernel
   int st;
   if (e4m3)
-    st = l_tensor ? fat::dispatch_e4m3_d128_ltensor(fp, X, dev, grid, p->stream)
-                  : fat::dispatch_e4m3_d128_lvec(fp, X, dev, grid, p->stream);
+    st = l_tensor ? fat::dispatch_e4m3_d128_ltensor(fp, X, dev, grid, n_splits, p->stream)
+                  : fat::dispatch_e4m3_d128_lvec(fp, X, dev, grid, n_splits, p->stream);
   else if (p->d == 128)
-    st = l_tensor ? fat::dispatch_bf16_d128_ltensor(fp, X, dev, grid, p->stream)
-                  : fat::dispatch_bf16_d128_lvec(fp, X, dev, grid, p->stream);
+    st = l_tensor ? fat::dispatch_bf16_d128_ltensor(fp, X, dev, grid, n_splits, p->stream)
+                  : fat::dispatch_bf16_d128_lvec(fp, X, dev, grid, n_splits, p->stream);
   else
-    st = l_tensor ? fat::dispatch_bf16_d64_ltensor(fp, X, dev, grid, p->stream)
-                  : fat::dispatch_bf16_d64_lvec(fp, X, dev, grid, p->stream);
-  return st == 0 ? FAT_OK : (st == -1 ? FAT_ERR_UNSUPPORTED : FAT_ERR_LAUNCH);
+    st = l_tensor ? fat::dispatch_bf16_d64_ltensor(fp, X, dev, grid, n_splits, p->stream)
+                  : fat::dispatch_bf16_d64_lvec(fp, X, dev, grid, n_splits, p->stream);
+  if (st != 0) return st == -1 ? FAT_ERR_UNSUPPORTED : FAT_ERR_LAUNCH;
+  if (n_splits > 1 &&
+      fat::launch_splitkv_combine(o_part, lse_part, p->o, p->lse, BH * Nq, n_splits, p->d,
+                                  p->stream) != 0)
+    return FAT_ERR_LAUNCH;
+  return FAT_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int fat_attn_fwd_ex(const fat_params* p) {
+  if (!p) return FAT_ERR_INVALID_ARG;
+  return run_fwd(p, p->N, p->N, 1, nullptr, 0);
+}
+
+size_t fat_attn_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits) {
+  if (B < 1 || H < 1 || Nq < 1 || (d != 64 && d != 128) || num_splits < 1 ||
+      num_splits > kMaxSplits)
+    return 0;
+  return static_cast<size_t>(splitkv_bytes(static_cast<long long>(B) * H, Nq, d, num_splits));
+}
+
+int fat_attn_splitkv_default_splits(int B, int H, int Nq, int Nk) {
+  if (B < 1 || H < 1 || Nq < 1 || Nk < 1) return 1;
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long items = static_cast<long long>(B) * H * ((Nq + fat::kRowsPerCta - 1) / fat::kRowsPerCta);
+  long long s = (sms + items - 1) / items;  // about one thread block per SM
+  const long long tiles = (Nk + fat::kBlockN - 1) / fat::kBlockN;
+  if (s > tiles) s = tiles;
+  if (s > kMaxSplits) s = kMaxSplits;
+  return static_cast<int>(s < 1 ? 1 : s);
+}
+
+int fat_attn_fwd_splitkv(const void* q, const void* k, const void* v, float* o, float* lse, int B,
+                         int H, int Nq, int Nk, int d, int causal, float scale, int X,
+                         int num_splits, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream) {
+  fat_params p = {};
+  p.q = q;
+  p.k = k;
+  p.v = v;
+  p.o = o;
+  p.lse = lse;
+  p.B = B;
+  p.H = H;
+  p.N = Nq;
+  p.d = d;
+  p.causal = causal;
+  p.scale = scale;
+  p.X = X;
+  p.variant = FAT_VARIANT_TENSOR;
+  p.dtype = FAT_DTYPE_BF16;
+  p.stream = stream;
+  return run_fwd(&p, Nq, Nk, num_splits, workspace, workspace_bytes);
 }
 
 static int fwd_common(const void* q, const void* k, const void* v, float* o, float* lse, int B,

@@ -50,10 +50,14 @@ struct FwdParams {
   float* o;
   float* lse;
   int* fallback_rows;
-  int B, H, N;
-  int causal;
+  int B, H;
+  int Nq, Nk;              // query rows, keys per (b, h)
+  int causal;              // key j allowed for query i iff j <= i + Nk - Nq
   int X;
-  int n_mblocks;           // ceil(N / 256)
+  int n_mblocks;           // ceil(Nq / 256)
+  int kv_split_len;        // keys per split (a multiple of 128): blockIdx.y = split
+  float* o_part;           // nullable: per-split partial O [splits][B*H][Nq][d] ...
+  float* lse_part;         // ... and LSE [splits][B*H][Nq] instead of o / lse
   float scale;             // softmax scale as received
   float c;                 // log2(e) * scale (times q/k descales for e4m3)
   float underflow_thresh;  // binades between surrogate and exact row maximum
@@ -160,7 +164,8 @@ template <int D, int kX, bool kLTensor, bool kE4M3>
 __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, uint32_t sb,
                                              uint32_t tmem, volatile uint32_t* misc, int warp,
                                              int lane, int m0, int bh, int n_kv, int it0,
-                                             int pass, bool exact) {
+                                             int pass, bool exact, int split, int kv_begin,
+                                             int kv_end, int kv_off) {
   using L = Smem<D, kE4M3>;
   constexpr bool kTensor = kX > 0;
   constexpr bool kGroup = kX > 32;  // tile maximum spans several warps
@@ -204,8 +209,8 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
 #pragma unroll
       for (int k = 0; k < 4; ++k) tmem_wait_ld(s[k]);
       // mask: keys >= N, keys after the query (causal), padding rows
-      const int kv0 = j * kBlockN;
-      const int limit = (row_g < p.N) ? (p.causal ? min(p.N, row_g + 1) : p.N) - kv0 : 0;
+      const int kv0 = kv_begin + j * kBlockN;
+      const int limit = (row_g < p.Nq) ? (p.causal ? min(kv_end, row_g + kv_off + 1) : kv_end) - kv0 : 0;
       if (limit < kBlockN) {
 #pragma unroll
         for (int k = 0; k < 4; ++k)
@@ -384,7 +389,9 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     // detector for the all-underflow case: surrogate far above the exact
     // maximum, or nothing left of the row sum
     if (kTensor && pass == 0) {
-      const bool flagged = row_g < p.N && (!(l > 0.f) || (M - m_row * c) > p.underflow_thresh);
+      // (a row with no key in this split's range is empty, not flagged)
+      const bool flagged = row_g < p.Nq && m_row != -INFINITY &&
+                           (!(l > 0.f) || (M - m_row * c) > p.underflow_thresh);
       const uint32_t ball = __ballot_sync(0xffffffffu, flagged);
       if (ball != 0 && lane == 0) {
         atomicOr(const_cast<uint32_t*>(misc + 2), 1u);
@@ -392,14 +399,15 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       }
     }
     // epilogue: O / l and LSE
-    const float inv_l = p.v_scale / l;
-    float* orow = p.o + (static_cast<size_t>(bh) * p.N + row_g) * D;
+    const float inv_l = l > 0.f ? p.v_scale / l : 0.f;  // an empty row gets O = 0
+    const size_t out_row = (static_cast<size_t>(split) * (p.B * p.H) + bh) * p.Nq + row_g;
+    float* orow = (p.o_part ? p.o_part : p.o) + out_row * D;
 #pragma unroll
     for (int k = 0; k < D / 32; ++k) {
       uint32_t ov[32];
       tmem_ld32(o_taddr + 32 * k, ov);
       tmem_wait_ld(ov);
-      if (row_g < p.N) {
+      if (row_g < p.Nq) {
 #pragma unroll
         for (int i = 0; i < 32; i += 4) {
           const float4 v4 =
@@ -411,9 +419,10 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     }
     if (r == 0 && t == 0 && pass == 0 && p.trace != nullptr && blockIdx.x == 0)
       p.trace[kTraceWords - 1] = static_cast<unsigned long long>(clock64());
-    if (row_g < p.N) {
+    if (row_g < p.Nq) {
       const float lsum = kLTensor ? l + delta : l;
-      p.lse[static_cast<size_t>(bh) * p.N + row_g] = (M - kKappa + __log2f(lsum)) * kLn2;
+      (p.lse_part ? p.lse_part : p.lse)[out_row] =
+          l > 0.f ? (M - kKappa + __log2f(lsum)) * kLn2 : -INFINITY;
     }
   }
   tc_fence_before();
@@ -450,8 +459,27 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
   const int mblock = p.n_mblocks - 1 - static_cast<int>(blockIdx.x) / BH;
   const int bh = static_cast<int>(blockIdx.x) % BH;
   const int m0 = mblock * kRowsPerCta;
-  const int n_kv_all = (p.N + kBlockN - 1) / kBlockN;
-  const int n_kv = p.causal ? min(n_kv_all, (m0 + kRowsPerCta) / kBlockN) : n_kv_all;
+  // this block's key range: the split's range, cut at the causal limit of
+  // its last row
+  const int split = static_cast<int>(blockIdx.y);
+  const int kv_begin = split * p.kv_split_len;
+  const int kv_end = min(p.Nk, kv_begin + p.kv_split_len);
+  const int kv_off = p.Nk - p.Nq;
+  const int kv_hi = p.causal ? min(kv_end, m0 + kRowsPerCta + kv_off) : kv_end;
+  const int n_kv = kv_hi > kv_begin ? (kv_hi - kv_begin + kBlockN - 1) / kBlockN : 0;
+  if (n_kv == 0) {
+    // no key of this split reaches these rows (split-KV, causal): an empty
+    // partial result that the combine step weighs by zero
+    for (int i = threadIdx.x; i < kRowsPerCta; i += kNumThreads) {
+      const int row = m0 + i;
+      if (row >= p.Nq) continue;
+      const size_t out_row = (static_cast<size_t>(split) * BH + bh) * p.Nq + row;
+      float4* orow = reinterpret_cast<float4*>(p.o_part + out_row * D);
+      for (int c4 = 0; c4 < D / 4; ++c4) orow[c4] = make_float4(0.f, 0.f, 0.f, 0.f);
+      p.lse_part[out_row] = -INFINITY;
+    }
+    return;
+  }
 
   // ---- set-up --------------------------------------------------------------
   if (threadIdx.x == 0) {
@@ -523,13 +551,13 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
             mbar_arrive_expect_tx(bar(L::bKFull + st), L::kTile);
             for (int a = 0; a < L::kAtoms; ++a)
               tma_load_3d(sb + L::kK + st * L::kTile + a * 16384, &p.tm_k, bar(L::bKFull + st),
-                          a * L::kAtomCols, j * kBlockN, bh);
+                          a * L::kAtomCols, kv_begin + j * kBlockN, bh);
             k_issued = j + 1;
             if (!wait_bounded(bar(L::bVEmpty + st), ph ^ 1, p, abort_flag)) break;
             mbar_arrive_expect_tx(bar(L::bVFull + st), L::kTile);
             for (int a = 0; a < L::kAtoms; ++a)
               tma_load_3d(sb + L::kV + st * L::kTile + a * 16384, &p.tm_v, bar(L::bVFull + st),
-                          a * L::kAtomCols, j * kBlockN, bh);
+                          a * L::kAtomCols, kv_begin + j * kBlockN, bh);
             v_issued = j + 1;
           }
           if (*abort_flag) {
@@ -666,7 +694,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
       // so no row can underflow (the vector fallback of the page's
       // all-underflow discussion, on the same code path).
       softmax_role<D, kX, kLTensor, kE4M3>(p, smem, sb, tmem, misc, warp, lane, m0, bh, n_kv, it0,
-                                           pass, /*exact=*/pass == 1);
+                                           pass, /*exact=*/pass == 1, split, kv_begin, kv_end,
+                                           kv_off);
       __syncthreads();
       if (!kTensor || misc[2] == 0u || *abort_flag != 0u) break;
     }

@@ -13,7 +13,7 @@ constexpr int kMaxDevices = 64;
 
 // Returns 0 or the fat_status code FAT_ERR_LAUNCH (-4).
 template <int D, int kX, bool kLTensor, bool kE4M3>
-int launch_fwd(const FwdParams& fp, int dev, int grid, cudaStream_t stream) {
+int launch_fwd(const FwdParams& fp, int dev, int grid, int splits, cudaStream_t stream) {
   static int ready[kMaxDevices];  // per device: attributes checked and set
   auto kern = fat_fwd_kernel<D, kX, kLTensor, kE4M3>;
   const int smem = Smem<D, kE4M3>::kAlloc;
@@ -28,14 +28,18 @@ int launch_fwd(const FwdParams& fp, int dev, int grid, cudaStream_t stream) {
       return -4;
     ready[dev] = 1;
   }
-  kern<<<grid, kNumThreads, smem, stream>>>(fp);
+  kern<<<dim3(grid, splits), kNumThreads, smem, stream>>>(fp);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
+
+// LSE-weighted merge of split-KV partial results (fat_splitkv_combine.cu).
+int launch_splitkv_combine(const float* o_part, const float* lse_part, float* o, float* lse,
+                           long long rows, int splits, int d, cudaStream_t stream);
 
 // X = 0 selects the vector-softmax kernel (row-sum mode ignored); otherwise
 // X in {16, 32, 64, 128}.  Returns -1 for an X without an instance.
 #define FAT_DECLARE_DISPATCH(name) \
-  int name(const FwdParams& fp, int X, int dev, int grid, cudaStream_t stream);
+  int name(const FwdParams& fp, int X, int dev, int grid, int splits, cudaStream_t stream);
 FAT_DECLARE_DISPATCH(dispatch_bf16_d128_lvec)
 FAT_DECLARE_DISPATCH(dispatch_bf16_d128_ltensor)
 FAT_DECLARE_DISPATCH(dispatch_bf16_d64_lvec)
@@ -45,15 +49,15 @@ FAT_DECLARE_DISPATCH(dispatch_e4m3_d128_ltensor)
 #undef FAT_DECLARE_DISPATCH
 
 #define FAT_DEFINE_DISPATCH(name, D, LT, E4M3)                                  \
-  int name(const FwdParams& fp, int X, int dev, int grid, cudaStream_t stream) { \
+  int name(const FwdParams& fp, int X, int dev, int grid, int splits, cudaStream_t stream) { \
     switch (X) {                                                                 \
       case 0:                                                                    \
-        if constexpr (!(LT)) return launch_fwd<D, 0, false, E4M3>(fp, dev, grid, stream); \
+        if constexpr (!(LT)) return launch_fwd<D, 0, false, E4M3>(fp, dev, grid, splits, stream); \
         return -1;                                                               \
-      case 16: return launch_fwd<D, 16, LT, E4M3>(fp, dev, grid, stream);        \
-      case 32: return launch_fwd<D, 32, LT, E4M3>(fp, dev, grid, stream);        \
-      case 64: return launch_fwd<D, 64, LT, E4M3>(fp, dev, grid, stream);        \
-      case 128: return launch_fwd<D, 128, LT, E4M3>(fp, dev, grid, stream);      \
+      case 16: return launch_fwd<D, 16, LT, E4M3>(fp, dev, grid, splits, stream);        \
+      case 32: return launch_fwd<D, 32, LT, E4M3>(fp, dev, grid, splits, stream);        \
+      case 64: return launch_fwd<D, 64, LT, E4M3>(fp, dev, grid, splits, stream);        \
+      case 128: return launch_fwd<D, 128, LT, E4M3>(fp, dev, grid, splits, stream);      \
       default: return -1;                                                        \
     }                                                                            \
   }

@@ -99,3 +99,25 @@ def test_params_struct_layout_matches_header(tmp_path):
     assert vals[0] == ctypes.sizeof(fat.FatParams)
     for f, off in zip(fields, vals[1:]):
         assert getattr(fat.FatParams, f).offset == off, f
+
+
+def test_splitkv_workspace_and_validation(lib):
+    ws = lib.fat_attn_splitkv_workspace_bytes
+    # splits x B*H x Nq x (d + 1) fp32, plus alignment slack
+    assert ws(2, 3, 5, 128, 4) == 4 * 6 * 5 * 129 * 4 + 256
+    assert ws(1, 1, 1, 96, 2) == 0 and ws(1, 1, 1, 64, 0) == 0 and ws(1, 1, 1, 64, 65) == 0
+    f = lib.fat_attn_fwd_splitkv
+    args = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000, B=1, H=1, Nq=4, Nk=1024,
+                d=128, causal=0, scale=0.1, X=128, splits=4, ws=None, wsb=0)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return f(a["q"], a["k"], a["v"], a["o"], a["lse"], a["B"], a["H"], a["Nq"], a["Nk"],
+                 a["d"], a["causal"], a["scale"], a["X"], a["splits"], a["ws"], a["wsb"], None)
+
+    assert call() == fat.FAT_ERR_INVALID_ARG               # several ranges, no workspace
+    assert call(ws=0x8000, wsb=16) == fat.FAT_ERR_INVALID_ARG  # workspace too small
+    assert call(splits=0) == fat.FAT_ERR_INVALID_ARG
+    assert call(splits=65) == fat.FAT_ERR_INVALID_ARG
+    assert call(causal=1, Nq=2048, Nk=1024) == fat.FAT_ERR_INVALID_ARG  # Nk < Nq, causal
+    assert call(Nk=0) == fat.FAT_ERR_INVALID_ARG
