@@ -138,6 +138,30 @@ size_t fat_attn_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_spl
 /* A split count giving about one thread block per SM of the current device. */
 int fat_attn_splitkv_default_splits(int B, int H, int Nq, int Nk);
 
+/*
+ * fat_attn_fwd_splitkv without any device allocation, for callers that
+ * cannot allocate device memory at the time of the call (their process gives
+ * all device memory to its own pool at start-up, or they must not call
+ * cudaMalloc / cudaFree, which can block or synchronise the device).  The
+ * pages have no counterpart: this is a convenience of this library.
+ *
+ * Same arguments and results as fat_attn_fwd_splitkv, minus the workspace:
+ * the partial results use a fixed array of FAT_NOALLOC_SCRATCH_BYTES that
+ * belongs to the library's device image, so every GPU that loads the library
+ * holds that memory until the process exits.  Requests whose workspace
+ * (fat_attn_splitkv_workspace_bytes) exceeds it return FAT_ERR_INVALID_ARG
+ * and launch nothing.  The first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress); make that first call before any
+ * stream capture.  Nothing in the array needs to start at zero (each call
+ * writes every entry it reads), but all calls share it and it keeps the last
+ * call's contents: calls whose work overlaps on the device race with each
+ * other, so serialise them (for example on one stream).
+ */
+#define FAT_NOALLOC_SCRATCH_BYTES (16u << 20)
+int fat_attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, float* o,
+                                 float* lse, int B, int H, int Nq, int Nk, int d, int causal,
+                                 float scale, int X, int num_splits, cudaStream_t stream);
+
 /* Every knob of the entry points above in one struct (tests and ablations). */
 typedef struct fat_params {
   const void* q;

@@ -43,7 +43,8 @@ TRACE_WORDS = 5 * 2 * TRACE_ITERS + 2
 # every extern "C" entry point declared in include/fat_attn.h
 ABI_SYMBOLS = (
     "fat_attn_fwd", "fat_attn_fwd_vec", "fat_attn_fwd_fp8", "fat_attn_fwd_splitkv",
-    "fat_attn_splitkv_workspace_bytes", "fat_attn_splitkv_default_splits", "fat_attn_fwd_ex",
+    "fat_attn_splitkv_workspace_bytes", "fat_attn_splitkv_default_splits",
+    "fat_attn_fwd_splitkv_noalloc", "fat_attn_fwd_ex",
     "fat_status_string", "fat_check_device_error",
 )
 
@@ -109,6 +110,8 @@ def load_library(build_if_missing: bool = True):
         lib.fat_attn_splitkv_workspace_bytes.restype = ctypes.c_size_t
         lib.fat_attn_splitkv_default_splits.argtypes = [I, I, I, I]
         lib.fat_attn_splitkv_default_splits.restype = I
+        lib.fat_attn_fwd_splitkv_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, I, F, I, I, P]
+        lib.fat_attn_fwd_splitkv_noalloc.restype = I
         lib.fat_attn_fwd_ex.argtypes = [ctypes.POINTER(FatParams)]
         lib.fat_attn_fwd_ex.restype = I
         lib.fat_status_string.argtypes = [I]

@@ -321,6 +321,46 @@ int fat_attn_fwd_fp8(const void* q, const void* k, const void* v, float q_descal
   return fat_attn_fwd_ex(&p);
 }
 
+// ---------------------------------------------------------------------------
+// Split-KV without allocation.  Some callers cannot obtain device memory when
+// they call us: their process hands all device memory to its own pool at
+// start-up, or they may not call cudaMalloc / cudaFree on this path because
+// those can block or synchronise the device.  For them the split-KV partial
+// results live in a fixed array that is part of this library's device image
+// (every GPU that loads the library holds it until the process exits).
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = FAT_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocScratch {
+  std::once_flag once;
+  void* ptr = nullptr;  // device address of g_noalloc_scratch on this device
+};
+NoAllocScratch g_noalloc[kMaxDevices];
+
+}  // namespace
+
+int fat_attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, float* o,
+                                 float* lse, int B, int H, int Nq, int Nk, int d, int causal,
+                                 float scale, int X, int num_splits, cudaStream_t stream) {
+  const size_t need = fat_attn_splitkv_workspace_bytes(B, H, Nq, d, num_splits);
+  if (need == 0 || need > kNoAllocScratchBytes) return FAT_ERR_INVALID_ARG;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FAT_ERR_LAUNCH;
+  NoAllocScratch& c = g_noalloc[dev];
+  // once per device, with that device current: the array's device address
+  // (in host code its name is only a host-side stand-in)
+  std::call_once(c.once, [&] {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) == cudaSuccess) c.ptr = addr;
+  });
+  if (!c.ptr) return FAT_ERR_LAUNCH;
+  return fat_attn_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, X, num_splits,
+                              c.ptr, kNoAllocScratchBytes, stream);
+}
+
 int fat_check_device_error(cudaStream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return FAT_ERR_LAUNCH;
   unsigned int word = 0;
