@@ -271,6 +271,75 @@ def time_variant(fat, torch, w, dev, args, variant, flush, stream, l_mode="vecto
     yield [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
+def run_all(args):
+    """One JSON line per workload (results tables): both softmax variants for
+    bf16, the tensorized one for e4m3, and split-KV decode shapes with their
+    HBM roofline (K and V read once: 2 * B * H * Nk * d * 2 bytes)."""
+    import torch
+
+    import tensorized_online_softmax_gb300 as fat
+    from tensorized_online_softmax_gb300 import inputs as gen
+
+    device = torch.device("cuda", 0)
+    peaks = load_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    def timeit(fn, steps):
+        for _ in range(3):
+            flush.zero_()
+            fn()
+        tot = 0.0
+        for _ in range(steps):
+            flush.zero_()
+            s0, s1 = torch.cuda.Event(True), torch.cuda.Event(True)
+            s0.record()
+            fn()
+            s1.record()
+            s1.synchronize()
+            tot += s0.elapsed_time(s1)
+        return tot / steps
+
+    steps = max(10, min(args.steps, 100))
+    for name, w in gen.WORKLOADS.items():
+        if name == "tiny":
+            continue
+        inp = gen.make_inputs(w)
+        q, k, v = (inp[n].to(device) for n in ("q", "k", "v"))
+        arms = {}
+        if w.dtype == "bf16":
+            for variant in ("tensor", "vec"):
+                ms = timeit(lambda: fat.attn_fwd(q, k, v, w.causal, w.scale, w.X, variant=variant),
+                            steps)
+                arms[variant] = {"ms": ms, "tflops": w.flops / ms / 1e9}
+        else:
+            ds = (inp["q_descale"], inp["k_descale"], inp["v_descale"])
+            for variant in ("tensor", "vec"):
+                ms = timeit(lambda: fat.attn_fwd(q, k, v, w.causal, w.scale, w.X, variant=variant,
+                                                 dtype="e4m3", descales=ds), steps)
+                arms[variant] = {"ms": ms, "tflops": w.flops / ms / 1e9}
+        peak = peaks["bf16_tflops"] * (2.0 if w.dtype == "e4m3" else 1.0)
+        print(json.dumps({"workload": name, "dtype": w.dtype, "causal": w.causal, "X": w.X,
+                          "arms": arms, "peak_tflops": peak,
+                          "peak_source": peaks["source"] + (" bf16 x 2 (fp8 nominal ratio)"
+                                                            if w.dtype == "e4m3" else " bf16"),
+                          "frac_tensor": arms["tensor"]["tflops"] / peak}), flush=True)
+    for B, H, Nq, Nk, d in ((8, 32, 1, 16384, 128), (4, 32, 16, 32768, 128)):
+        g = torch.Generator().manual_seed(2000 + Nq)
+        q = torch.randn((B, H, Nq, d), generator=g).to(torch.bfloat16).to(device)
+        k = torch.randn((B, H, Nk, d), generator=g).to(torch.bfloat16).to(device)
+        v = torch.randn((B, H, Nk, d), generator=g).to(torch.bfloat16).to(device)
+        splits = fat.load_library().fat_attn_splitkv_default_splits(B, H, Nq, Nk)
+        ws = torch.empty(fat.load_library().fat_attn_splitkv_workspace_bytes(B, H, Nq, d, splits),
+                         dtype=torch.uint8, device=device)
+        ms = timeit(lambda: fat.attn_fwd_splitkv(q, k, v, False, None, 128, splits, workspace=ws),
+                    steps)
+        kv_bytes = 2.0 * B * H * Nk * d * 2
+        print(json.dumps({"workload": f"decode_b{B}h{H}q{Nq}k{Nk}d{d}", "splits": splits,
+                          "ms": ms, "tflops": 4.0 * B * H * Nq * Nk * d / ms / 1e9,
+                          "hbm_gbs": kv_bytes / ms / 1e6, "hbm_peak_gbs": peaks["hbm_gbs"],
+                          "frac_hbm": kv_bytes / ms / 1e6 / peaks["hbm_gbs"]}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -281,8 +350,13 @@ def main():
     ap.add_argument("--no-ablation", action="store_true", help="skip timing the vec variant")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--all", action="store_true",
+                    help="one line per workload (results tables) instead of the benchmark line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.all:
+        run_all(args)
+        return
 
     from tensorized_online_softmax_gb300 import inputs as gen
 
