@@ -37,6 +37,38 @@ DEFAULT_WORKLOAD = "b2h16n8192d128_causal"
 METRIC = "attn fwd TFLOPS on 1 GB300 (bf16/fp8, causal+full) and % of dense tensor peak"
 L2_FLUSH_BYTES = 256 << 20
 
+# DRAM bytes (read + write) of one launch of the headline kernel from an ncu
+# capture, valid only for the kernel sources it was taken on (their hash);
+# the capture and its command are summarised in
+# profiles/fat_fwd_kernel_b2h16n8192d128_causal.md.
+MEASURED_TRAFFIC = {
+    "workload": "b2h16n8192d128_causal",
+    "variant": "tensor",
+    "bytes": 552.8e6 + 96.3e6,
+    "csrc_sha256": "0ed2b4d77596ad4612cb46ce733d016ca809ff88f5a04d4c32b9151aa8f28be2",
+}
+
+
+def csrc_sha256() -> str:
+    """Hash of the kernel sources (file names and contents, sorted)."""
+    import hashlib
+    d = os.path.join(ROOT, "tensorized_online_softmax_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            with open(os.path.join(d, name), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_traffic(workload: str, variant: str):
+    """Per-launch DRAM traffic if it was captured on these exact kernel sources."""
+    t = MEASURED_TRAFFIC
+    if t["workload"] == workload and t["variant"] == variant and t["csrc_sha256"] == csrc_sha256():
+        return t["bytes"]
+    return None
+
 
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -470,7 +502,8 @@ def main():
             "dtype": w.dtype, "data": "synthetic", "config": config_dict(w, "tensor"),
             "pct_of_peak": 100.0 * achieved / peak,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "unit": "TFLOP/s", "frac": achieved / peak,
+                         "traffic": measured_traffic(w.name, "tensor"),
                          "peak_source": f"{peaks['source']} bf16 dense (burst)"},
             "ablation": ablation, "phase_trace": traces, "e2e": e2e, "cpu_baseline": cpu,
             "gpu_launches": args.steps, "clocks": clocks,
