@@ -39,6 +39,11 @@ constexpr int kSoftmaxRegs = 224;
 static_assert(256 * kSoftmaxRegs + 128 * kCtrlRegs <= kNumThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr uint32_t kTmemCols = 512;
+// Of the 16 element pairs in each 32-column chunk of a row, this many take
+// 2^z from the FMA-pipe polynomial (f2_exp2_poly) and the rest from MUFU ex2:
+// one MUFU ex2 costs a warp 8 issue cycles of its pipe (16 results per SM
+// per cycle), the polynomial about 5 single-cycle instructions per element.
+constexpr int kPolyPairs = 0;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -193,6 +198,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
   float m_row = -INFINITY;  // exact running row maximum, raw logits
   float l = 0.f;            // running row sum
   float delta = 0.f;        // tensorized row sum: rounding of each tile's dominant term
+  int kscale_prev = 0;      // last value written to this tile's PV scale word
   bool dead = false;        // a bounded wait of this warp (or of its X-row group) ran out
   int j = 0;
   for (; j < n_kv; ++j) {
@@ -200,8 +206,18 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     const uint32_t par = it & 1;
     dead = !__all_sync(0xffffffffu, wait_bounded(bar(L::bSFull + t), par, p, abort_flag));
     if (wq == 0 && lane == 0) trace_mark(p, 0, t, j, pass);
+    // X = 128 (bf16), from the second K/V tile on: steps 4-6 start from the
+    // previous tile's surrogate maximum, and step 1 (the maximum over the four
+    // warps of the tile) is settled afterwards.  Usually no warp raises the
+    // maximum, which one OR over the group barrier establishes; a tile that
+    // does raise it has its P~ scaled by the exact power of two
+    // 2^(m_old - m_new).  The P~ that reaches the MMA is the same as when the
+    // maximum is known first.  M is uniform over the 128-row tile, and so is
+    // this choice.
+    const bool spec = kMmaScale && !exact && M != -INFINITY;
     uint32_t s[4][32];
     float rowmax = -INFINITY;
+    int limit = kBlockN;  // keys of this K/V tile the row may see
     if (!dead) {
       tc_fence_after();
 #pragma unroll
@@ -210,7 +226,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       for (int k = 0; k < 4; ++k) tmem_wait_ld(s[k]);
       // mask: keys >= N, keys after the query (causal), padding rows
       const int kv0 = kv_begin + j * kBlockN;
-      const int limit = (row_g < p.Nq) ? (p.causal ? min(kv_end, row_g + kv_off + 1) : kv_end) - kv0 : 0;
+      limit = (row_g < p.Nq) ? (p.causal ? min(kv_end, row_g + kv_off + 1) : kv_end) - kv0 : 0;
       if (limit < kBlockN) {
 #pragma unroll
         for (int k = 0; k < 4; ++k)
@@ -241,58 +257,76 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     } else if constexpr (kX >= 32) {
       tmax = warp_max(rowmax);
     }
-    if constexpr (kGroup) {
-      // X = 64 / 128: combine the warps of the X-row group.  Every warp of the
-      // group joins this barrier once per K/V tile, aborted or not (see the
-      // drain loop below), and the OR spreads an abort to the whole group.
-      float* slot = red + (t * 2 + par) * 4;
-      if (lane == 0) slot[wq] = tmax;
-      dead = named_bar_or(gbar_id, kGbarN, dead);
-      if (!dead) {
-        if constexpr (kX == 64) {
-          tmax = fmaxf(slot[wq & 2], slot[(wq & 2) + 1]);
-        } else {
-          tmax = fmaxf(fmaxf(slot[0], slot[1]), fmaxf(slot[2], slot[3]));
+    // X = 64 / 128: the warps of the X-row group combine their maxima through
+    // shared memory.  Every warp of the group joins the same sequence of group
+    // barriers, aborted or not (one per K/V tile; two on a speculative tile
+    // that raises the maximum or aborts; see the drain loop below), and the OR
+    // spreads an abort to the whole group.
+    float* slot = red + (t * 2 + par) * 4;
+    auto group_max = [&]() {
+      if constexpr (kGroup) {
+        dead = named_bar_or(gbar_id, kGbarN, dead);
+        if (!dead) {
+          if constexpr (kX == 64) {
+            tmax = fmaxf(slot[wq & 2], slot[(wq & 2) + 1]);
+          } else {
+            tmax = fmaxf(fmaxf(slot[0], slot[1]), fmaxf(slot[2], slot[3]));
+          }
         }
       }
-    }
-    if (dead) break;
-
-    float M_new;
-    if constexpr (kTensor) {
-      // the surrogate maximum is kept as a whole number of binades so the
-      // rescale factor of steps 2-3 is an exact power of two; the fallback
-      // pass uses one-row tiles (each row's own maximum)
-      const float tm = exact ? rowmax : tmax;
-      const float Mc = (tm == -INFINITY) ? -INFINITY : ceilf(tm * c);
-      M_new = fmaxf(M, Mc);
-    } else {
-      M_new = (m_row == -INFINITY) ? -INFINITY : m_row * c;
-    }
-
-    // Algorithm 1 steps 2-3 factor: exp(m_old - m_new), one exact power of
-    // two per X-row tile (exact per-row factor in the vector variant).
-    const bool grow = j > 0 && M_new > M;
-    const float alpha = (M_new == -INFINITY) ? 1.f : ex2_approx(M - M_new);
-    if (j > 0) {
-      l *= alpha;
-      if (kLTensor) delta *= alpha;
-    }
-    // With X = 128 the whole 128-row tile shares the factor 2^-k and the
-    // tensor pipe applies it inside the next O += P V (scale-input-d); other
-    // cases rescale O in TMEM from the vector side below.
-    bool vec_rescale = grow;
-    if constexpr (kMmaScale) {
-      int kscale = 0;
-      if (mma_scale && grow && M_new - M <= 15.f) {
-        kscale = static_cast<int>(M_new - M);
-        vec_rescale = false;
+    };
+    if (!spec) {
+      if constexpr (kGroup) {
+        if (lane == 0) slot[wq] = tmax;
       }
-      if (wq == 0 && lane == 0) misc[4 + t] = static_cast<uint32_t>(kscale);
+      group_max();
+      if (dead) break;
     }
-    M = M_new;
+
+    // The new offset of step 2; the factor of steps 2-3 is exp(m_old - m_new),
+    // one exact power of two per X-row tile (exact per-row factor in the
+    // vector variant).  With X = 128 the whole 128-row tile shares the factor
+    // 2^-k and the tensor pipe applies it inside the next O += P V
+    // (scale-input-d); other cases rescale O in TMEM from the vector side.
+    auto new_offset = [&]() -> float {
+      if constexpr (kTensor) {
+        // the surrogate maximum is kept as a whole number of binades so the
+        // rescale factor is an exact power of two; the fallback pass uses
+        // one-row tiles (each row's own maximum)
+        const float tm = exact ? rowmax : tmax;
+        const float Mc = (tm == -INFINITY) ? -INFINITY : ceilf(tm * c);
+        return fmaxf(M, Mc);
+      } else {
+        return (m_row == -INFINITY) ? -INFINITY : m_row * c;
+      }
+    };
+    float M_new = M, alpha = 1.f;
+    bool vec_rescale = false;
+    auto bookkeeping = [&]() {
+      const bool grow = j > 0 && M_new > M;
+      alpha = (M_new == -INFINITY) ? 1.f : ex2_approx(M - M_new);
+      vec_rescale = grow;
+      if constexpr (kMmaScale) {
+        int kscale = 0;
+        if (mma_scale && grow && M_new - M <= 15.f) {
+          kscale = static_cast<int>(M_new - M);
+          vec_rescale = false;
+        }
+        if (wq == 0 && lane == 0) misc[4 + t] = static_cast<uint32_t>(kscale);
+        kscale_prev = kscale;
+      }
+    };
+    if (!spec) {
+      M_new = new_offset();
+      bookkeeping();
+      if (j > 0) {
+        l *= alpha;
+        if (kLTensor) delta *= alpha;
+      }
+      M = M_new;
+      if (wq == 0 && lane == 0) trace_mark(p, 1, t, j, pass);
+    }
     const float neg_M = (M == -INFINITY) ? 0.f : -M;
-    if (wq == 0 && lane == 0) trace_mark(p, 1, t, j, pass);
 
     // steps 4-6: Z = c S - m_hat, P~ = exp2(Z), stored as bf16 (e4m3) over S
     const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(neg_M + kKappa, neg_M + kKappa);
@@ -306,8 +340,18 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
                                           __uint_as_float(s[k][2 * i + 1])), c2, nm2);
         float z0, z1;
         f2_unpack(z, z0, z1);
-        pf[2 * i] = ex2_approx(z0);
-        pf[2 * i + 1] = ex2_approx(z1);
+        if ((i * kPolyPairs) % 16 < kPolyPairs) {
+          // the polynomial leaves a tiny positive value for a masked (-inf)
+          // key: zero it in the tiles that have masked keys
+          f2_unpack(f2_exp2_poly(z0, z1), pf[2 * i], pf[2 * i + 1]);
+          if (limit < kBlockN) {
+            if (32 * k + 2 * i >= limit) pf[2 * i] = 0.f;
+            if (32 * k + 2 * i + 1 >= limit) pf[2 * i + 1] = 0.f;
+          }
+        } else {
+          pf[2 * i] = ex2_approx(z0);
+          pf[2 * i + 1] = ex2_approx(z1);
+        }
         if (!kLTensor) acc2[i & 1] = f2_add(acc2[i & 1], f2_pack(pf[2 * i], pf[2 * i + 1]));
       }
       if constexpr (kE4M3) {
@@ -323,6 +367,60 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
         tmem_st16(s_taddr + 16 * k, pk);
       }
     }
+    float lt_vec;  // this tile's row sum (vector row sum only)
+    {
+      float r0, r1;
+      f2_unpack(f2_add(acc2[0], acc2[1]), r0, r1);
+      lt_vec = r0 + r1;
+    }
+    if (spec) {
+      // step 1 completes: does any warp of the tile raise the maximum?
+      const float Mc_w = (tmax == -INFINITY) ? -INFINITY : ceilf(tmax * c);
+      const bool any = named_bar_or(gbar_id, kGbarN, dead || Mc_w > M);
+      if (any) {
+        // rare: exchange the raised maxima (or learn of an abort)
+        if (lane == 0) slot[wq] = Mc_w;
+        dead = named_bar_or(gbar_id, kGbarN, dead);
+        if (dead) break;
+        M_new = fmaxf(M, fmaxf(fmaxf(slot[0], slot[1]), fmaxf(slot[2], slot[3])));
+        // M_new > M here: P~ was formed with the old offset.  Multiply it
+        // (and its row sum) by 2^(m_old - m_new), exact in bf16; O takes the
+        // same factor in the PV MMA (at most 15 binades) or from the vector
+        // side.  A jump above 100 binades can only come from logits that far
+        // apart; the block is then redone with per-row maxima (the fallback
+        // pass).
+        const int kb = min(static_cast<int>(M_new - M), 126);  // M, M_new whole binades
+        alpha = __uint_as_float(static_cast<uint32_t>(127 - kb) << 23);  // 2^-kb
+        vec_rescale = kb > 15;
+        const int kscale = vec_rescale ? 0 : kb;
+        if (wq == 0 && lane == 0) {
+          misc[4 + t] = static_cast<uint32_t>(kscale);
+          if (kb > 100) atomicOr(const_cast<uint32_t*>(misc + 2), 1u);
+        }
+        kscale_prev = kscale;
+        const uint32_t a2 = pack_bf16x2(alpha, alpha);
+        tmem_wait_st();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pv[32];
+          tmem_ld32(s_taddr + 32 * h, pv);
+          tmem_wait_ld(pv);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pv[i] = bf16x2_mul(pv[i], a2);
+          tmem_st32(s_taddr + 32 * h, pv);
+        }
+        lt_vec *= alpha;
+        l *= alpha;
+        if (kLTensor) delta *= alpha;
+        M = M_new;
+      } else if (kscale_prev != 0) {
+        // the previous tile's PV scale is spent
+        if (wq == 0 && lane == 0) misc[4 + t] = 0u;
+        kscale_prev = 0;
+      }
+      if (wq == 0 && lane == 0) trace_mark(p, 1, t, j, pass);
+    }
+    const float neg_Mn = (M == -INFINITY) ? 0.f : -M;
     // steps 2-3 on the vector side: O <- alpha O in TMEM.  PV_{j-1} has
     // completed (issued before S_j, whose completion was awaited) and PV_j
     // waits for this warpgroup's P-full signal below.
@@ -354,7 +452,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       // step 7 on the tensor pipe (P~ times ones, S column 64); the LSE also
       // gets back the rounding of the tile's dominant term
       if (rowmax != -INFINITY) {
-        const float pm = ex2_approx(fmaf(rowmax, c, neg_M + kKappa));
+        const float pm = ex2_approx(fmaf(rowmax, c, neg_Mn + kKappa));
         delta += pm - (kE4M3 ? e4m3_round(pm) : bf16_round(pm));
       }
       dead = !__all_sync(0xffffffffu, wait_bounded(bar(L::bRsFull + t), par, p, abort_flag));
@@ -368,9 +466,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       if (lane == 0) mbar_arrive(bar(L::bLFree + t));
       l += __uint_as_float(lt);
     } else {
-      float r0, r1;
-      f2_unpack(f2_add(acc2[0], acc2[1]), r0, r1);
-      l += r0 + r1;
+      l += lt_vec;
     }
   }
   if constexpr (kGroup) {
@@ -378,7 +474,11 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     // barriers of tiles 0..j; it joins the remaining ones so the other warps
     // of the group are never left waiting there
     if (dead) {
-      for (++j; j < n_kv; ++j) named_bar_or(gbar_id, kGbarN, true);
+      const bool spec = kMmaScale && !exact && M != -INFINITY;
+      for (++j; j < n_kv; ++j) {
+        named_bar_or(gbar_id, kGbarN, true);
+        if (spec) named_bar_or(gbar_id, kGbarN, true);
+      }
     }
   }
 

@@ -46,10 +46,11 @@ class Workload:
     causal: bool
     X: int
     dtype: str = "bf16"  # "bf16" or "e4m3"
-    kind: str = "normal"  # "normal" or "stress"
+    kind: str = "normal"  # "normal", "stress" or "growth"
     seed: int = 0
     shift_coord: float = 15.5  # stress only
     qk_std: float = 1.0
+    growth_nats: float = 0.0  # growth only: logit added per 128-key tile
 
     @property
     def scale(self) -> float:
@@ -118,6 +119,13 @@ def make_inputs(w: Workload):
                 k[b, h, j0:min(j0 + 128, w.N), w.d - 1] = w.shift_coord
         out["shift_rows"] = rows
         out["shift_block"] = blocks
+    if w.kind == "growth":
+        # every query gets coordinate d-1 = 1 and key j gets
+        # growth_nats * (j // 128) / scale there, so each 128-key tile raises
+        # the logits of all rows by growth_nats over the previous one
+        q[..., w.d - 1] = 1.0
+        tile = torch.arange(w.N, dtype=torch.float32) // 128
+        k[..., w.d - 1] = (w.growth_nats / w.scale) * tile
     if w.dtype == "bf16":
         out.update(q=q.to(torch.bfloat16), k=k.to(torch.bfloat16), v=v.to(torch.bfloat16))
     elif w.dtype == "e4m3":
