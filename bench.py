@@ -235,8 +235,9 @@ def run_reference(args, w):
 def phase_trace(fat, torch, w, dev, variant, l_mode, stream, sm_mhz, peak_tflops):
     """One traced launch: per-iteration clock stamps of the first thread block.
 
-    Returns the median steady-state iteration period (both query tiles), the
-    median softmax time per tile (S received -> P published), and the
+    Returns the median steady-state iteration period (one K/V tile against
+    the block's 128 query rows), the median softmax time per half of the keys
+    (S received -> P published), and the
     vector-interval ratio: the share of an iteration in which the tensor pipe
     has no work because it waits for the softmax, estimated as
     1 - (ideal tensor cycles of the iteration) / (measured period), with the
@@ -262,7 +263,7 @@ def phase_trace(fat, torch, w, dev, variant, l_mode, stream, sm_mhz, peak_tflops
     if sm_mhz:
         n_sm = torch.cuda.get_device_properties(dev["q"].device).multi_processor_count
         flop_per_clk = peak_tflops * 1e12 / (n_sm * sm_mhz * 1e6)
-        ideal = 2 * 4.0 * 128 * 128 * w.d / flop_per_clk  # PV + S for both tiles
+        ideal = 4.0 * 128 * 128 * w.d / flop_per_clk  # PV + S of one 128-row tile
         out["ideal_tensor_cycles"] = ideal
         out["vector_interval_ratio"] = max(0.0, 1.0 - ideal / period)
     return out

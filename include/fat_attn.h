@@ -81,7 +81,7 @@ typedef enum { FAT_LMODE_VECTOR = 0, FAT_LMODE_TENSOR = 1 } fat_lmode;
  *     fat_lmode for the tensor-pipe alternative);
  *   - rows whose surrogate maximum exceeds their exact maximum by more than
  *     the underflow threshold (default 64 binades for bf16 P~, 14 for e4m3),
- *     or whose sum is zero, are detected; their 256-row block is recomputed
+ *     or whose sum is zero, are detected; their 128-row block is recomputed
  *     with one-row tiles (X = 1: each row's own maximum rounded up to a whole
  *     binade, so no row can underflow) -- the optional fallback of the
  *     all-underflow discussion.

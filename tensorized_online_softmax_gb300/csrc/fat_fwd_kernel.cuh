@@ -3,19 +3,28 @@
 // Tensor-Vector Parallelism" (papercache.org summary, section A2, Algorithm 1)
 // and its vector-softmax ablation (the FA2 arm of the page's Fig. 10).
 //
-// One CTA computes 256 query rows of one (batch, head) as two 128-row tiles
-// (t = 0, 1) that ping-pong on the tensor pipe, the fused flow of the page's
-// section A3 / Fig. 2 (one output row block per worker, S and P on chip):
+// One CTA computes one 128-row query tile of one (batch, head), the fused
+// flow of the page's section A3 / Fig. 2 (one output row block per worker, S
+// and P on chip).  Tensor-vector parallelism comes from a three-deep ring of
+// score buffers in TMEM: while the softmax warps turn S_j into P_j, the tensor
+// pipe already holds S_{j+1} and S_{j+2} and runs O += P_{j-1} V_{j-1}, so
+// neither side waits for the other in the steady state.
 //
-//   warp 9      TMA producer: Q0, Q1 once; K_j, V_j through an mbarrier ring.
-//   warp 8      MMA issuer (one thread): S_t = Q_t K_j^T into TMEM,
-//               O_t += P_t V_j from TMEM, and (tensorized) l_t = P_t 1.
-//   warps 0-7   softmax, warpgroup t owns tile t, thread i owns row i
-//               (TMEM lane i): row max, X-row tile max, O rescale, P = exp2(Z).
+//   warp 9      TMA producer of Q (once) and K_j, through an mbarrier ring;
+//   warp 10     TMA producer of V_j, through its own ring, so neither stream
+//               waits for a slot of the other (K runs three tiles ahead).
+//   warp 8      MMA issuer (one thread): S_j = Q K_j^T into buffer j % 3,
+//               O += P_j V_j, and (row sum on the tensor pipe) l_j = P_j 1.
+//   warps 0-7   softmax: warp w owns TMEM lanes 32 (w % 4) .. +31 (one row
+//               per thread) and keys 64 (w / 4) .. +63 of each K/V tile (one
+//               half of every row): row maximum, X-row tile maximum, O
+//               rescale, P = exp2(Z).
 //
-// TMEM (512 columns x 128 lanes, fp32): S_0 [0,128), S_1 [128,256),
-// O_0 [256, 256+D), O_1 [256+D, 256+2D).  P_t is written as packed bf16 over
-// S_t columns [0,64); the tensorized row sum lands in S_t column 64.
+// TMEM (512 columns x 128 lanes, fp32): score buffers [0,128), [128,256),
+// [256,384); O at [384, 384 + D).  P_j overwrites the scores it came from,
+// each half in place (bf16: columns 64h .. 64h+31 of the buffer, two keys per
+// column; e4m3: 64h .. 64h+15, four keys per column); the tensor row sum lands
+// in column 32 of the buffer.
 #pragma once
 
 #include <cuda.h>
@@ -24,11 +33,15 @@
 
 namespace fat {
 
-constexpr int kBlockM = 128;  // query rows per tile (= TMEM lanes)
+constexpr int kBlockM = 128;  // query rows per CTA (= TMEM lanes)
 constexpr int kBlockN = 128;  // keys per K/V tile
-constexpr int kRowsPerCta = 2 * kBlockM;
+constexpr int kRowsPerCta = kBlockM;
+constexpr int kSBufs = 3;     // score / P buffers in TMEM
+constexpr int kOCol = kSBufs * kBlockN;  // first TMEM column of O
+constexpr int kSoftmaxWarps = 8;
 constexpr int kMmaWarp = 8;
-constexpr int kLoadWarp = 9;   // warps 10, 11 complete the third warpgroup
+constexpr int kLoadWarp = 9;    // Q and K
+constexpr int kLoadVWarp = 10;  // V; warp 11 completes the third warpgroup
 constexpr int kNumThreads = 384;
 // Register budget: 384 threads launch with kLaunchRegs each; the MMA/TMA
 // warpgroup drops to kCtrlRegs and the two softmax warpgroups rise to
@@ -39,14 +52,18 @@ constexpr int kSoftmaxRegs = 224;
 static_assert(256 * kSoftmaxRegs + 128 * kCtrlRegs <= kNumThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr uint32_t kTmemCols = 512;
-// Of the 16 element pairs in each 32-column chunk of a row, this many take
-// 2^z from the FMA-pipe polynomial (f2_exp2_poly) and the rest from MUFU ex2:
-// one MUFU ex2 costs a warp 8 issue cycles of its pipe (16 results per SM
-// per cycle), the polynomial about 5 single-cycle instructions per element.
-constexpr int kPolyPairs = 0;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+// Of the 16 element pairs in each 32-column chunk of a half row, this many
+// take 2^z from the FMA-pipe polynomial (f2_exp2_poly) and the rest from MUFU
+// ex2: one MUFU ex2 costs a warp 8 issue cycles of its pipe (16 results per SM
+// per cycle), the polynomial about 5 single-cycle instructions per element.
+constexpr int kPolyPairs = 0;
 
+// named barriers (0 is __syncthreads)
+constexpr uint32_t kBarPair = 1;  // + quarter: the two warps sharing 32 rows (64 threads)
+constexpr uint32_t kBarHalf = 5;  // + 64-row half: four warps (128 threads), X = 64
+constexpr uint32_t kBarTile = 7;  // all eight softmax warps (256 threads), X = 128
 
 struct FwdParams {
   CUtensorMap tm_q;
@@ -59,7 +76,7 @@ struct FwdParams {
   int Nq, Nk;              // query rows, keys per (b, h)
   int causal;              // key j allowed for query i iff j <= i + Nk - Nq
   int X;
-  int n_mblocks;           // ceil(Nq / 256)
+  int n_mblocks;           // ceil(Nq / 128)
   int kv_split_len;        // keys per split (a multiple of 128): blockIdx.y = split
   float* o_part;           // nullable: per-split partial O [splits][B*H][Nq][d] ...
   float* lse_part;         // ... and LSE [splits][B*H][Nq] instead of o / lse
@@ -74,9 +91,10 @@ struct FwdParams {
 };
 
 // Phase trace of CTA 0, SM clock (clock64) stamps, pass 0 only:
-//   word (e * 2 + t) * kTraceIters + j for event e, tile t, K/V tile j:
+//   word (e * 2 + t) * kTraceIters + j for event e, K/V tile j, and t = the
+//   half of the keys (softmax events, written by warps 0 and 4) or 0 (MMA):
 //   e = 0 softmax got S_j, 1 softmax has m_hat, 2 softmax publishes P_j,
-//       3 MMA issuer sees P_j, 4 MMA issuer has queued O += P_j V, S_{j+1};
+//       3 MMA issuer sees P_j, 4 MMA issuer has queued O += P_j V, S_{j+3};
 //   word kTraceWords - 2 / - 1: kernel start / softmax epilogue done.
 constexpr int kTraceIters = 128;
 constexpr int kTraceWords = 5 * 2 * kTraceIters + 2;
@@ -89,34 +107,43 @@ __device__ __forceinline__ void trace_mark(const FwdParams& p, int e, int t, int
 template <int D, bool kE4M3 = false>
 struct Smem {
   static constexpr int kElt = kE4M3 ? 1 : 2;          // bytes per input element
-  static constexpr int kStages = (D * kElt == 256) ? 2 : 4;
   static constexpr int kTile = kBlockM * D * kElt;    // bytes of one 128 x D tile
+  // K_{j+3} is loaded once S_j is done, V_j once O += P_{j-3} V is; 256-byte
+  // rows fit two K and three V stages
+  static constexpr int kKStages = (D * kElt == 256) ? 2 : 4;
+  static constexpr int kVStages = (D * kElt == 256) ? 3 : 4;
   static constexpr int kAtoms = D * kElt / 128;       // 128-byte-wide column slabs per tile
   static constexpr int kAtomCols = 128 / kElt;        // elements per slab row
   static constexpr int kMmaK = 32 / kElt;             // K of one MMA (bf16 16, e4m3 32)
   static constexpr int kPvStep = kMmaK * 128;         // bytes of V rows per PV K step
+  static constexpr int kStepsPerHalf = 64 / kMmaK;    // PV K steps per 64-key half
   static_assert(kAtoms >= 1, "rows must span at least one 128-byte slab");
-  static constexpr int kQ = 0;                   // Q_t at kQ + t * kTile
-  static constexpr int kK = 2 * kTile;           // K ring
-  static constexpr int kV = kK + kStages * kTile;  // V ring
-  static constexpr int kOnes = kV + kStages * kTile;  // 16 rows x 128 B of ones (2 KB)
+  static constexpr int kQ = 0;
+  static constexpr int kK = kTile;                     // K ring
+  static constexpr int kV = kK + kKStages * kTile;     // V ring
+  static constexpr int kOnes = kV + kVStages * kTile;  // 16 rows x 128 B of ones (2 KB)
   static constexpr int kBars = kOnes + 2048;
   // barrier slots
   static constexpr int bQFull = 0;
   static constexpr int bKFull = 1;
-  static constexpr int bKEmpty = bKFull + kStages;
-  static constexpr int bVFull = bKEmpty + kStages;
-  static constexpr int bVEmpty = bVFull + kStages;
-  static constexpr int bSFull = bVEmpty + kStages;  // [2]
-  static constexpr int bPFull = bSFull + 2;         // [2]
-  static constexpr int bRsFull = bPFull + 2;        // [2]
-  static constexpr int bLFree = bRsFull + 2;        // [2]
-  static constexpr int bRed = bLFree + 2;           // [2] tile-max exchange
-  static constexpr int bOFinal = bRed + 2;
+  static constexpr int bKEmpty = bKFull + kKStages;
+  static constexpr int bVFull = bKEmpty + kKStages;
+  static constexpr int bVEmpty = bVFull + kVStages;
+  static constexpr int bSFull = bVEmpty + kVStages;  // [kSBufs]
+  static constexpr int bPFull = bSFull + kSBufs;     // [kSBufs], 8 arrivals
+  static constexpr int bRsFull = bPFull + kSBufs;    // [kSBufs]
+  static constexpr int bLFree = bRsFull + kSBufs;    // [kSBufs], 8 arrivals
+  // [kSBufs]: O += P_it V landed, it % 3 (per buffer, so that a waiter is
+  // never two phases behind: PV_{it-3} has completed once S_it has)
+  static constexpr int bOReady = bLFree + kSBufs;
+  static constexpr int bOFinal = bOReady + kSBufs;
   static constexpr int bDrain = bOFinal + 1;
   static constexpr int kNumBars = bDrain + 1;
-  static constexpr int kRed = kBars + 8 * kNumBars;  // float [2 tiles][2 parity][4 warps]
-  static constexpr int kMisc = kRed + 64;  // u32: tmem base, abort, redo, -, pv scale[2]
+  static constexpr int kRed = kBars + 8 * kNumBars;  // float [2 parity][8 warps]
+  static constexpr int kRowRed = kRed + 64;          // float [2 parity][2 halves][128 rows]
+  static constexpr int kFin = kRowRed + 2048;        // float [3][2 halves][128 rows]
+  // u32: tmem base, abort, redo, -, PV scale of each score buffer [3]
+  static constexpr int kMisc = kFin + 3072;
   static constexpr int kBytes = kMisc + 64;
   static constexpr int kAlloc = kBytes + 1024;       // slack for 1024-byte alignment
   static_assert(kK % 1024 == 0 && kV % 1024 == 0 && kOnes % 1024 == 0, "tiles 1 KB aligned");
@@ -157,8 +184,8 @@ __device__ __forceinline__ float bf16_round(float x) {
 }
 
 // ---------------------------------------------------------------------------
-// softmax warpgroups: warpgroup t owns query tile t; thread i owns row i
-// (TMEM lane i).
+// softmax warps: warp w owns TMEM lanes 32 (w % 4) .. +31 (row i of the tile
+// = lane i) and keys 64 h .. 64 h + 63 of every K/V tile, h = w / 4.
 //   kX > 0   tensorized online softmax with the surrogate maximum over kX-row
 //            tiles (X is a compile-time constant so no runtime branching sits
 //            in the hot loop); `exact` (the fallback pass) uses each row's own
@@ -173,71 +200,95 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
                                              int kv_end, int kv_off) {
   using L = Smem<D, kE4M3>;
   constexpr bool kTensor = kX > 0;
-  constexpr bool kGroup = kX > 32;  // tile maximum spans several warps
   constexpr bool kMmaScale = kX == 128 && !kE4M3;
   // e4m3 P~ is formed as 2^(Z + kKappa) <= 2^8 < 448 so that its largest
   // terms use the format's range; the factor cancels in O / l and is taken
   // off LSE.
   constexpr float kKappa = kE4M3 ? 8.f : 0.f;
+  constexpr int kHalfD = D / 2;  // O columns this warp rescales and writes
   volatile uint32_t* abort_flag = misc + 1;
   auto bar = [&](int i) -> uint32_t { return sb + L::kBars + 8 * i; };
-  const int t = warp >> 2;       // tile
-  const int wq = warp & 3;       // quarter of the tile (TMEM lanes 32 wq ..)
-  const int r = wq * 32 + lane;  // row within the tile
-  const int row_g = m0 + t * kBlockM + r;
-  const uint32_t lane_base = static_cast<uint32_t>(wq * 32) << 16;
-  const uint32_t s_taddr = tmem + lane_base + t * kBlockN;
-  const uint32_t o_taddr = tmem + lane_base + 2 * kBlockN + t * D;
+  const int q = warp & 3;        // quarter of the tile (TMEM lanes 32 q ..)
+  const int h = warp >> 2;       // half of the keys
+  const int r = q * 32 + lane;   // row within the tile
+  const int row_g = m0 + r;
+  const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+  const uint32_t o_taddr = tmem + lane_base + kOCol + h * kHalfD;
   const float c = p.c;
   float* red = reinterpret_cast<float*>(smem + L::kRed);
-  const uint32_t gbar_id = 1 + 4 * t + (kX == 64 ? (wq >> 1) : 0);
-  constexpr uint32_t kGbarN = kX == 64 ? 64 : 128;
+  float* rowred = reinterpret_cast<float*>(smem + L::kRowRed);
+  float* fin = reinterpret_cast<float*>(smem + L::kFin);
+  // Barrier of the group that shares a surrogate maximum: the pair of warps
+  // holding the same 32 rows (X <= 32, the fallback pass and the vector
+  // variant), four warps (X = 64) or all eight (X = 128).
+  const bool pair_mode = kX <= 32 || exact;
+  const uint32_t gbar_id = pair_mode ? kBarPair + q : (kX == 64 ? kBarHalf + (q >> 1) : kBarTile);
+  const uint32_t gbar_n = pair_mode ? 64 : (kX == 64 ? 128 : 256);
   const bool mma_scale = kMmaScale && !exact;
 
   float M = -INFINITY;      // offset of the exponent, binades (exact row max * c in vec mode)
-  float m_row = -INFINITY;  // exact running row maximum, raw logits
-  float l = 0.f;            // running row sum
+  float m_row = -INFINITY;  // running maximum of this half row (whole row in pair mode), logits
+  float l = 0.f;            // running sum of this half row (tensor row sum: whole row)
   float delta = 0.f;        // tensorized row sum: rounding of each tile's dominant term
-  int kscale_prev = 0;      // last value written to this tile's PV scale word
-  bool dead = false;        // a bounded wait of this warp (or of its X-row group) ran out
+  bool dead = false;        // a bounded wait of this warp (or of its group) ran out
   int j = 0;
+  // Tensor row sum of an earlier K/V tile (read one tile late so the read
+  // never waits), added with the given rescale factor.
+  auto take_row_sum = [&](int itp, float factor) -> bool {
+    if (!__all_sync(0xffffffffu, wait_bounded(bar(L::bRsFull + itp % kSBufs),
+                                              (itp / kSBufs) & 1, p, abort_flag)))
+      return false;
+    tc_fence_after();
+    uint32_t lt;
+    tmem_ld1(tmem + lane_base + (itp % kSBufs) * kBlockN + 32, lt);
+    tmem_wait_ld1(lt);
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(L::bLFree + itp % kSBufs));
+    l += __uint_as_float(lt) * factor;
+    return true;
+  };
+
   for (; j < n_kv; ++j) {
     const int it = it0 + j;
+    const int buf = it % kSBufs;
     const uint32_t par = it & 1;
-    dead = !__all_sync(0xffffffffu, wait_bounded(bar(L::bSFull + t), par, p, abort_flag));
-    if (wq == 0 && lane == 0) trace_mark(p, 0, t, j, pass);
+    const uint32_t s_taddr = tmem + lane_base + buf * kBlockN + h * 64;
+    dead = !__all_sync(0xffffffffu,
+                       wait_bounded(bar(L::bSFull + buf), (it / kSBufs) & 1, p, abort_flag));
+    if (q == 0 && lane == 0) trace_mark(p, 0, h, j, pass);
     // X = 128 (bf16), from the second K/V tile on: steps 4-6 start from the
-    // previous tile's surrogate maximum, and step 1 (the maximum over the four
-    // warps of the tile) is settled afterwards.  Usually no warp raises the
-    // maximum, which one OR over the group barrier establishes; a tile that
+    // previous tile's surrogate maximum, and step 1 (the maximum over the
+    // eight warps of the tile) is settled afterwards.  Usually no warp raises
+    // the maximum, which one OR over the tile barrier establishes; a tile that
     // does raise it has its P~ scaled by the exact power of two
     // 2^(m_old - m_new).  The P~ that reaches the MMA is the same as when the
-    // maximum is known first.  M is uniform over the 128-row tile, and so is
-    // this choice.
-    const bool spec = kMmaScale && !exact && M != -INFINITY;
-    uint32_t s[4][32];
+    // maximum is known first.  M is uniform over the tile, and so is this
+    // choice.
+    const bool spec = mma_scale && M != -INFINITY;
+    uint32_t s[2][32];
     float rowmax = -INFINITY;
     int limit = kBlockN;  // keys of this K/V tile the row may see
     if (!dead) {
       tc_fence_after();
-#pragma unroll
-      for (int k = 0; k < 4; ++k) tmem_ld32(s_taddr + 32 * k, s[k]);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) tmem_wait_ld(s[k]);
+      tmem_ld32(s_taddr, s[0]);
+      tmem_ld32(s_taddr + 32, s[1]);
+      tmem_wait_ld(s[0]);
+      tmem_wait_ld(s[1]);
       // mask: keys >= N, keys after the query (causal), padding rows
       const int kv0 = kv_begin + j * kBlockN;
       limit = (row_g < p.Nq) ? (p.causal ? min(kv_end, row_g + kv_off + 1) : kv_end) - kv0 : 0;
-      if (limit < kBlockN) {
+      if (limit < h * 64 + 64) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
+        for (int k = 0; k < 2; ++k)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (32 * k + i >= limit) s[k][i] = __float_as_uint(-INFINITY);
+            if (h * 64 + 32 * k + i >= limit) s[k][i] = __float_as_uint(-INFINITY);
       }
-      // row maximum as a tree of independent 3-input maxima
-      float mx[8];
+      // half-row maximum as a tree of independent 3-input maxima
+      float mx[4];
 #pragma unroll
-      for (int a = 0; a < 8; ++a) {
+      for (int a = 0; a < 4; ++a) {
         const int k = a >> 1, b = (a & 1) * 16;
         mx[a] = fmax3(__uint_as_float(s[k][b]), __uint_as_float(s[k][b + 1]),
                       __uint_as_float(s[k][b + 2]));
@@ -246,10 +297,10 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
           mx[a] = fmax3(mx[a], __uint_as_float(s[k][b + i]), __uint_as_float(s[k][b + i + 1]));
         mx[a] = fmaxf(mx[a], __uint_as_float(s[k][b + 15]));
       }
-      rowmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7])));
-      m_row = fmaxf(m_row, rowmax);
+      rowmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
     }
-    // Algorithm 1 step 1: maximum of the row maxima over the X-row tile
+    // Algorithm 1 step 1: maximum of the row maxima over the X-row tile.  This
+    // warp's part first (its 32 half rows, or 16-row groups for X = 16) ...
     float tmax = rowmax;
     if constexpr (kX == 16) {
 #pragma unroll
@@ -257,74 +308,65 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     } else if constexpr (kX >= 32) {
       tmax = warp_max(rowmax);
     }
-    // X = 64 / 128: the warps of the X-row group combine their maxima through
-    // shared memory.  Every warp of the group joins the same sequence of group
-    // barriers, aborted or not (one per K/V tile; two on a speculative tile
-    // that raises the maximum or aborts; see the drain loop below), and the OR
-    // spreads an abort to the whole group.
-    float* slot = red + (t * 2 + par) * 4;
-    auto group_max = [&]() {
-      if constexpr (kGroup) {
-        dead = named_bar_or(gbar_id, kGbarN, dead);
-        if (!dead) {
-          if constexpr (kX == 64) {
-            tmax = fmaxf(slot[wq & 2], slot[(wq & 2) + 1]);
-          } else {
-            tmax = fmaxf(fmaxf(slot[0], slot[1]), fmaxf(slot[2], slot[3]));
-          }
-        }
+    // ... then across the warps of the group, through shared memory.  Every
+    // warp of a group joins the same sequence of group barriers, aborted or
+    // not (one per K/V tile; two on a speculative tile that raises the
+    // maximum or aborts; see the drain loop below), and the OR spreads an
+    // abort to the whole group.
+    float* slot = red + par * 8;
+    auto group_max = [&](float v) -> float {
+      if (pair_mode) {
+        rowred[(par * 2 + h) * kBlockM + r] = v;
+        dead = named_bar_or(gbar_id, gbar_n, dead);
+        return dead ? v : fmaxf(v, rowred[(par * 2 + (h ^ 1)) * kBlockM + r]);
       }
+      if (lane == 0) slot[warp] = v;
+      dead = named_bar_or(gbar_id, gbar_n, dead);
+      if (dead) return v;
+      if (kX == 64) {
+        const int w0 = q & 2;
+        return fmaxf(fmaxf(slot[w0], slot[w0 + 1]), fmaxf(slot[w0 + 4], slot[w0 + 5]));
+      }
+      return fmaxf(fmaxf(fmaxf(slot[0], slot[1]), fmaxf(slot[2], slot[3])),
+                   fmaxf(fmaxf(slot[4], slot[5]), fmaxf(slot[6], slot[7])));
     };
-    if (!spec) {
-      if constexpr (kGroup) {
-        if (lane == 0) slot[wq] = tmax;
-      }
-      group_max();
-      if (dead) break;
-    }
 
-    // The new offset of step 2; the factor of steps 2-3 is exp(m_old - m_new),
-    // one exact power of two per X-row tile (exact per-row factor in the
-    // vector variant).  With X = 128 the whole 128-row tile shares the factor
-    // 2^-k and the tensor pipe applies it inside the next O += P V
-    // (scale-input-d); other cases rescale O in TMEM from the vector side.
-    auto new_offset = [&]() -> float {
+    float alpha = 1.f;  // steps 2-3: exp(m_old - m_new)
+    bool vec_rescale = false;
+    int kscale = 0;     // uniform rescale 2^-kscale applied by the PV MMA
+    if (!spec) {
+      // the fallback pass and the vector variant combine the two halves of
+      // each row; the surrogate modes combine the group's maxima
+      const float gm = group_max((pair_mode && (exact || !kTensor)) ? rowmax : tmax);
+      if (dead) break;
+      float M_new;
       if constexpr (kTensor) {
         // the surrogate maximum is kept as a whole number of binades so the
         // rescale factor is an exact power of two; the fallback pass uses
         // one-row tiles (each row's own maximum)
-        const float tm = exact ? rowmax : tmax;
-        const float Mc = (tm == -INFINITY) ? -INFINITY : ceilf(tm * c);
-        return fmaxf(M, Mc);
+        m_row = fmaxf(m_row, exact ? gm : rowmax);
+        M_new = fmaxf(M, (gm == -INFINITY) ? -INFINITY : ceilf(gm * c));
       } else {
-        return (m_row == -INFINITY) ? -INFINITY : m_row * c;
+        m_row = fmaxf(m_row, gm);
+        M_new = (m_row == -INFINITY) ? -INFINITY : m_row * c;
       }
-    };
-    float M_new = M, alpha = 1.f;
-    bool vec_rescale = false;
-    auto bookkeeping = [&]() {
       const bool grow = j > 0 && M_new > M;
       alpha = (M_new == -INFINITY) ? 1.f : ex2_approx(M - M_new);
       vec_rescale = grow;
-      if constexpr (kMmaScale) {
-        int kscale = 0;
-        if (mma_scale && grow && M_new - M <= 15.f) {
-          kscale = static_cast<int>(M_new - M);
-          vec_rescale = false;
-        }
-        if (wq == 0 && lane == 0) misc[4 + t] = static_cast<uint32_t>(kscale);
-        kscale_prev = kscale;
+      // With X = 128 the whole tile shares the factor 2^-k and the tensor
+      // pipe applies it inside the next O += P V (scale-input-d).
+      if (mma_scale && grow && M_new - M <= 15.f) {
+        kscale = static_cast<int>(M_new - M);
+        vec_rescale = false;
       }
-    };
-    if (!spec) {
-      M_new = new_offset();
-      bookkeeping();
       if (j > 0) {
         l *= alpha;
         if (kLTensor) delta *= alpha;
       }
       M = M_new;
-      if (wq == 0 && lane == 0) trace_mark(p, 1, t, j, pass);
+      if (q == 0 && lane == 0) trace_mark(p, 1, h, j, pass);
+    } else {
+      m_row = fmaxf(m_row, rowmax);
     }
     const float neg_M = (M == -INFINITY) ? 0.f : -M;
 
@@ -332,7 +374,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(neg_M + kKappa, neg_M + kKappa);
     uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < 2; ++k) {
       float pf[32];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -344,9 +386,9 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
           // the polynomial leaves a tiny positive value for a masked (-inf)
           // key: zero it in the tiles that have masked keys
           f2_unpack(f2_exp2_poly(z0, z1), pf[2 * i], pf[2 * i + 1]);
-          if (limit < kBlockN) {
-            if (32 * k + 2 * i >= limit) pf[2 * i] = 0.f;
-            if (32 * k + 2 * i + 1 >= limit) pf[2 * i + 1] = 0.f;
+          if (limit < h * 64 + 64) {
+            if (h * 64 + 32 * k + 2 * i >= limit) pf[2 * i] = 0.f;
+            if (h * 64 + 32 * k + 2 * i + 1 >= limit) pf[2 * i + 1] = 0.f;
           }
         } else {
           pf[2 * i] = ex2_approx(z0);
@@ -367,7 +409,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
         tmem_st16(s_taddr + 16 * k, pk);
       }
     }
-    float lt_vec;  // this tile's row sum (vector row sum only)
+    float lt_vec;  // this tile's half-row sum (vector row sum only)
     {
       float r0, r1;
       f2_unpack(f2_add(acc2[0], acc2[1]), r0, r1);
@@ -376,13 +418,15 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     if (spec) {
       // step 1 completes: does any warp of the tile raise the maximum?
       const float Mc_w = (tmax == -INFINITY) ? -INFINITY : ceilf(tmax * c);
-      const bool any = named_bar_or(gbar_id, kGbarN, dead || Mc_w > M);
+      const bool any = named_bar_or(gbar_id, gbar_n, dead || Mc_w > M);
       if (any) {
         // rare: exchange the raised maxima (or learn of an abort)
-        if (lane == 0) slot[wq] = Mc_w;
-        dead = named_bar_or(gbar_id, kGbarN, dead);
+        if (lane == 0) slot[warp] = Mc_w;
+        dead = named_bar_or(gbar_id, gbar_n, dead);
         if (dead) break;
-        M_new = fmaxf(M, fmaxf(fmaxf(slot[0], slot[1]), fmaxf(slot[2], slot[3])));
+        const float M_new =
+            fmaxf(M, fmaxf(fmaxf(fmaxf(slot[0], slot[1]), fmaxf(slot[2], slot[3])),
+                           fmaxf(fmaxf(slot[4], slot[5]), fmaxf(slot[6], slot[7]))));
         // M_new > M here: P~ was formed with the old offset.  Multiply it
         // (and its row sum) by 2^(m_old - m_new), exact in bf16; O takes the
         // same factor in the PV MMA (at most 15 binades) or from the vector
@@ -392,106 +436,106 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
         const int kb = min(static_cast<int>(M_new - M), 126);  // M, M_new whole binades
         alpha = __uint_as_float(static_cast<uint32_t>(127 - kb) << 23);  // 2^-kb
         vec_rescale = kb > 15;
-        const int kscale = vec_rescale ? 0 : kb;
-        if (wq == 0 && lane == 0) {
-          misc[4 + t] = static_cast<uint32_t>(kscale);
-          if (kb > 100) atomicOr(const_cast<uint32_t*>(misc + 2), 1u);
-        }
-        kscale_prev = kscale;
+        kscale = vec_rescale ? 0 : kb;
+        if (kb > 100 && warp == 0 && lane == 0) atomicOr(const_cast<uint32_t*>(misc + 2), 1u);
         const uint32_t a2 = pack_bf16x2(alpha, alpha);
         tmem_wait_st();
+        uint32_t pv[32];
+        tmem_ld32(s_taddr, pv);
+        tmem_wait_ld(pv);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t pv[32];
-          tmem_ld32(s_taddr + 32 * h, pv);
-          tmem_wait_ld(pv);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) pv[i] = bf16x2_mul(pv[i], a2);
-          tmem_st32(s_taddr + 32 * h, pv);
-        }
+        for (int i = 0; i < 32; ++i) pv[i] = bf16x2_mul(pv[i], a2);
+        tmem_st32(s_taddr, pv);
         lt_vec *= alpha;
         l *= alpha;
         if (kLTensor) delta *= alpha;
         M = M_new;
-      } else if (kscale_prev != 0) {
-        // the previous tile's PV scale is spent
-        if (wq == 0 && lane == 0) misc[4 + t] = 0u;
-        kscale_prev = 0;
       }
-      if (wq == 0 && lane == 0) trace_mark(p, 1, t, j, pass);
+      if (q == 0 && lane == 0) trace_mark(p, 1, h, j, pass);
     }
+    // the MMA issuer reads this buffer's PV scale once P_j is published (one
+    // word per buffer: the next tile's value may be written before it reads)
+    if (kMmaScale && warp == 0 && lane == 0) misc[4 + buf] = static_cast<uint32_t>(kscale);
     const float neg_Mn = (M == -INFINITY) ? 0.f : -M;
-    // steps 2-3 on the vector side: O <- alpha O in TMEM.  PV_{j-1} has
-    // completed (issued before S_j, whose completion was awaited) and PV_j
-    // waits for this warpgroup's P-full signal below.
+    // steps 2-3 on the vector side: O <- alpha O in TMEM, this warp's half of
+    // the columns, once O += P_{j-1} V has landed (PV_j waits for the P-full
+    // signal below).
     if (__any_sync(0xffffffffu, vec_rescale)) {
-      const uint64_t a2 = f2_pack(alpha, alpha);
+      if (!__all_sync(0xffffffffu, wait_bounded(bar(L::bOReady + (it - 1) % kSBufs),
+                                                ((it - 1) / kSBufs) & 1, p, abort_flag))) {
+        dead = true;
+      } else {
+        tc_fence_after();
+        const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
-      for (int k = 0; k < D / 32; ++k) {
-        uint32_t ov[32];
-        tmem_ld32(o_taddr + 32 * k, ov);
-        tmem_wait_ld(ov);
+        for (int k = 0; k < kHalfD / 32; ++k) {
+          uint32_t ov[32];
+          tmem_ld32(o_taddr + 32 * k, ov);
+          tmem_wait_ld(ov);
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float o0, o1;
-          f2_unpack(f2_mul(f2_pack(__uint_as_float(ov[i]), __uint_as_float(ov[i + 1])), a2), o0,
-                    o1);
-          ov[i] = __float_as_uint(o0);
-          ov[i + 1] = __float_as_uint(o1);
+          for (int i = 0; i < 32; i += 2) {
+            float o0, o1;
+            f2_unpack(f2_mul(f2_pack(__uint_as_float(ov[i]), __uint_as_float(ov[i + 1])), a2), o0,
+                      o1);
+            ov[i] = __float_as_uint(o0);
+            ov[i + 1] = __float_as_uint(o1);
+          }
+          tmem_st32(o_taddr + 32 * k, ov);
         }
-        tmem_st32(o_taddr + 32 * k, ov);
       }
     }
-    tmem_wait_st();
-    tc_fence_before();
-    __syncwarp();
-    if (wq == 0 && lane == 0) trace_mark(p, 2, t, j, pass);
-    if (lane == 0) mbar_arrive(bar(L::bPFull + t));
-
     if constexpr (kLTensor) {
-      // step 7 on the tensor pipe (P~ times ones, S column 64); the LSE also
-      // gets back the rounding of the tile's dominant term
+      // step 7 on the tensor pipe: the previous tile's row sum (P~ times
+      // ones), taken over to this tile's offset; the LSE also gets back the
+      // rounding of each tile's dominant term
+      if (!dead && j > 0 && !take_row_sum(it - 1, alpha)) dead = true;
       if (rowmax != -INFINITY) {
         const float pm = ex2_approx(fmaf(rowmax, c, neg_Mn + kKappa));
         delta += pm - (kE4M3 ? e4m3_round(pm) : bf16_round(pm));
       }
-      dead = !__all_sync(0xffffffffu, wait_bounded(bar(L::bRsFull + t), par, p, abort_flag));
-      if (dead) break;
-      tc_fence_after();
-      uint32_t lt;
-      tmem_ld1(s_taddr + 64, lt);
-      tmem_wait_ld1(lt);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::bLFree + t));
-      l += __uint_as_float(lt);
     } else {
       l += lt_vec;
     }
+    tmem_wait_st();
+    tc_fence_before();
+    __syncwarp();
+    if (q == 0 && lane == 0) trace_mark(p, 2, h, j, pass);
+    // a warp that gave up still signals; the MMA issuer sees the abort flag
+    if (lane == 0) mbar_arrive(bar(L::bPFull + buf));
+    if (dead) break;
   }
-  if constexpr (kGroup) {
-    // an aborted warp left the loop at K/V tile j after joining the group
-    // barriers of tiles 0..j; it joins the remaining ones so the other warps
-    // of the group are never left waiting there
-    if (dead) {
-      const bool spec = kMmaScale && !exact && M != -INFINITY;
-      for (++j; j < n_kv; ++j) {
-        named_bar_or(gbar_id, kGbarN, true);
-        if (spec) named_bar_or(gbar_id, kGbarN, true);
-      }
+  if (dead) {
+    // An aborted warp left the loop at K/V tile j.  If it left at a group
+    // barrier, every warp of its group left there too; otherwise (a wait of
+    // its own ran out after the group barriers of tile j) the others meet it
+    // at the next tile's first barrier, where the OR stops them.  From there
+    // on all of them join the same barriers, tile by tile, until the end.
+    const bool spec = mma_scale && M != -INFINITY;
+    for (++j; j < n_kv; ++j) {
+      named_bar_or(gbar_id, gbar_n, true);
+      if (spec) named_bar_or(gbar_id, gbar_n, true);
     }
   }
 
   bool ok = !dead;
   if (ok) ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bOFinal), pass & 1, p, abort_flag));
+  if (ok && kLTensor && n_kv > 0) ok = take_row_sum(it0 + n_kv - 1, 1.f);
+  // combine the two halves of every row (both warps of a pair always get here)
+  fin[(0 * 2 + h) * kBlockM + r] = m_row;
+  fin[(1 * 2 + h) * kBlockM + r] = l;
+  fin[(2 * 2 + h) * kBlockM + r] = delta;
+  named_bar_sync(kBarPair + q, 64);
+  const float m_full = fmaxf(m_row, fin[(0 * 2 + (h ^ 1)) * kBlockM + r]);
+  const float l_full = kLTensor ? l : l + fin[(1 * 2 + (h ^ 1)) * kBlockM + r];
+  const float delta_full = delta + fin[(2 * 2 + (h ^ 1)) * kBlockM + r];
   if (ok) {
     tc_fence_after();
     // detector for the all-underflow case: surrogate far above the exact
-    // maximum, or nothing left of the row sum
-    if (kTensor && pass == 0) {
+    // maximum, or nothing left of the row sum (counted once per row)
+    if (kTensor && pass == 0 && h == 0) {
       // (a row with no key in this split's range is empty, not flagged)
-      const bool flagged = row_g < p.Nq && m_row != -INFINITY &&
-                           (!(l > 0.f) || (M - m_row * c) > p.underflow_thresh);
+      const bool flagged = row_g < p.Nq && m_full != -INFINITY &&
+                           (!(l_full > 0.f) || (M - m_full * c) > p.underflow_thresh);
       const uint32_t ball = __ballot_sync(0xffffffffu, flagged);
       if (ball != 0 && lane == 0) {
         atomicOr(const_cast<uint32_t*>(misc + 2), 1u);
@@ -499,11 +543,11 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       }
     }
     // epilogue: O / l and LSE
-    const float inv_l = l > 0.f ? p.v_scale / l : 0.f;  // an empty row gets O = 0
+    const float inv_l = l_full > 0.f ? p.v_scale / l_full : 0.f;  // an empty row gets O = 0
     const size_t out_row = (static_cast<size_t>(split) * (p.B * p.H) + bh) * p.Nq + row_g;
-    float* orow = (p.o_part ? p.o_part : p.o) + out_row * D;
+    float* orow = (p.o_part ? p.o_part : p.o) + out_row * D + h * kHalfD;
 #pragma unroll
-    for (int k = 0; k < D / 32; ++k) {
+    for (int k = 0; k < kHalfD / 32; ++k) {
       uint32_t ov[32];
       tmem_ld32(o_taddr + 32 * k, ov);
       tmem_wait_ld(ov);
@@ -517,12 +561,12 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
         }
       }
     }
-    if (r == 0 && t == 0 && pass == 0 && p.trace != nullptr && blockIdx.x == 0)
+    if (r == 0 && h == 0 && pass == 0 && p.trace != nullptr && blockIdx.x == 0)
       p.trace[kTraceWords - 1] = static_cast<unsigned long long>(clock64());
-    if (row_g < p.Nq) {
-      const float lsum = kLTensor ? l + delta : l;
+    if (row_g < p.Nq && h == 0) {
+      const float lsum = kLTensor ? l_full + delta_full : l_full;
       (p.lse_part ? p.lse_part : p.lse)[out_row] =
-          l > 0.f ? (M - kKappa + __log2f(lsum)) * kLn2 : -INFINITY;
+          l_full > 0.f ? (M - kKappa + __log2f(lsum)) * kLn2 : -INFINITY;
     }
   }
   tc_fence_before();
@@ -540,7 +584,8 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
 template <int D, int kX, bool kLTensor, bool kE4M3>
 __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_constant__ FwdParams p) {
   using L = Smem<D, kE4M3>;
-  constexpr int S = L::kStages;
+  constexpr int SK = L::kKStages;
+  constexpr int SV = L::kVStages;
   constexpr bool kTensor = kX > 0;
   // X = 128 (bf16): the uniform rescale of O rides in the PV MMA
   constexpr bool kMmaScale = kX == 128 && !kE4M3;
@@ -584,25 +629,26 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
   // ---- set-up --------------------------------------------------------------
   if (threadIdx.x == 0) {
     mbar_init(bar(L::bQFull), 1);
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < SK; ++s) {
       mbar_init(bar(L::bKFull + s), 1);
       mbar_init(bar(L::bKEmpty + s), 1);
+    }
+    for (int s = 0; s < SV; ++s) {
       mbar_init(bar(L::bVFull + s), 1);
       mbar_init(bar(L::bVEmpty + s), 1);
     }
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(bar(L::bSFull + t), 1);
-      mbar_init(bar(L::bPFull + t), 4);
-      mbar_init(bar(L::bRsFull + t), 1);
-      mbar_init(bar(L::bLFree + t), 4);
-      mbar_init(bar(L::bRed + t), 4);
+    for (int b = 0; b < kSBufs; ++b) {
+      mbar_init(bar(L::bSFull + b), 1);
+      mbar_init(bar(L::bPFull + b), kSoftmaxWarps);
+      mbar_init(bar(L::bRsFull + b), 1);
+      mbar_init(bar(L::bLFree + b), kSoftmaxWarps);
+      mbar_init(bar(L::bOReady + b), 1);
     }
     mbar_init(bar(L::bOFinal), 1);
     mbar_init(bar(L::bDrain), 1);
     misc[1] = 0;
     misc[2] = 0;
-    misc[4] = 0;
-    misc[5] = 0;
+    for (int b = 0; b < kSBufs; ++b) misc[4 + b] = 0;
     fence_mbar_init();
   }
   if (threadIdx.x < 256) {  // the ones tile used as B of the row-sum MMA
@@ -628,146 +674,129 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
   if (warp >= kMmaWarp) {
     regs_dec<kCtrlRegs>();
     for (int pass = 0; pass < 2; ++pass) {
-      const bool tensor_pass = kTensor && pass == 0;
       const int it0 = pass * n_kv;
-      if (warp == kLoadWarp) {
-        // =================== TMA producer ===================
+      if (warp == kLoadWarp || warp == kLoadVWarp) {
+        // =================== TMA producers ===================
+        // warp 9: Q, then K_0, K_1, ...; warp 10: V_0, V_1, ...
         if (lane == 0) {
-          int k_issued = 0, v_issued = 0;
-          if (pass == 0) {
+          const bool is_k = warp == kLoadWarp;
+          const int S = is_k ? SK : SV;
+          const int full = is_k ? L::bKFull : L::bVFull;
+          const int empty = is_k ? L::bKEmpty : L::bVEmpty;
+          const int ring = is_k ? L::kK : L::kV;
+          const CUtensorMap* tm = is_k ? &p.tm_k : &p.tm_v;
+          int issued = 0;
+          if (pass == 0 && is_k) {
             tma_prefetch_desc(&p.tm_q);
             tma_prefetch_desc(&p.tm_k);
-            tma_prefetch_desc(&p.tm_v);
-            mbar_arrive_expect_tx(bar(L::bQFull), 2 * L::kTile);
-            for (int t = 0; t < 2; ++t)
-              for (int a = 0; a < L::kAtoms; ++a)
-                tma_load_3d(sb + L::kQ + t * L::kTile + a * 16384, &p.tm_q, bar(L::bQFull), a * L::kAtomCols,
-                            m0 + t * kBlockM, bh);
+            mbar_arrive_expect_tx(bar(L::bQFull), L::kTile);
+            for (int a = 0; a < L::kAtoms; ++a)
+              tma_load_3d(sb + L::kQ + a * 16384, &p.tm_q, bar(L::bQFull), a * L::kAtomCols, m0, bh);
           }
-          for (int j = 0; j < n_kv; ++j) {
-            const int it = it0 + j, st = it % S;
-            const uint32_t ph = (it / S) & 1;
-            if (!wait_bounded(bar(L::bKEmpty + st), ph ^ 1, p, abort_flag)) break;
-            mbar_arrive_expect_tx(bar(L::bKFull + st), L::kTile);
+          if (pass == 0 && !is_k) tma_prefetch_desc(&p.tm_v);
+          for (int jj = 0; jj < n_kv; ++jj) {
+            const int it = it0 + jj, st = it % S;
+            if (!wait_bounded(bar(empty + st), ((it / S) & 1) ^ 1, p, abort_flag)) break;
+            mbar_arrive_expect_tx(bar(full + st), L::kTile);
             for (int a = 0; a < L::kAtoms; ++a)
-              tma_load_3d(sb + L::kK + st * L::kTile + a * 16384, &p.tm_k, bar(L::bKFull + st),
-                          a * L::kAtomCols, kv_begin + j * kBlockN, bh);
-            k_issued = j + 1;
-            if (!wait_bounded(bar(L::bVEmpty + st), ph ^ 1, p, abort_flag)) break;
-            mbar_arrive_expect_tx(bar(L::bVFull + st), L::kTile);
-            for (int a = 0; a < L::kAtoms; ++a)
-              tma_load_3d(sb + L::kV + st * L::kTile + a * 16384, &p.tm_v, bar(L::bVFull + st),
-                          a * L::kAtomCols, kv_begin + j * kBlockN, bh);
-            v_issued = j + 1;
+              tma_load_3d(sb + ring + st * L::kTile + a * 16384, tm, bar(full + st),
+                          a * L::kAtomCols, kv_begin + jj * kBlockN, bh);
+            issued = jj + 1;
           }
           if (*abort_flag) {
             // let every copy already issued land before the CTA can exit
-            if (pass == 0) wait_drain(bar(L::bQFull), 0);
-            for (int j = max(0, k_issued - S); j < k_issued; ++j)
-              wait_drain(bar(L::bKFull + (it0 + j) % S), ((it0 + j) / S) & 1);
-            for (int j = max(0, v_issued - S); j < v_issued; ++j)
-              wait_drain(bar(L::bVFull + (it0 + j) % S), ((it0 + j) / S) & 1);
+            if (pass == 0 && is_k) wait_drain(bar(L::bQFull), 0);
+            for (int jj = max(0, issued - S); jj < issued; ++jj)
+              wait_drain(bar(full + (it0 + jj) % S), ((it0 + jj) / S) & 1);
           }
         }
         __syncwarp();
       } else if (warp == kMmaWarp) {
         // =================== MMA issuer ===================
-        if (lane == 0) {
+        // The whole warp runs this code with warp-uniform values; one elected
+        // lane issues each MMA and commit.
+        {
           constexpr uint32_t idesc_s = idesc_f32acc<kE4M3>(kBlockM, kBlockN, false);
           constexpr uint32_t idesc_pv = idesc_f32acc<kE4M3>(kBlockM, D, true);
           constexpr uint32_t idesc_rs = idesc_f32acc<kE4M3>(kBlockM, 16, false);
           const uint64_t ones_desc = sdesc_sw128(sb + L::kOnes, 16, 1024);
           bool ok = true;
-          auto issue_s = [&](int t, int st) {
-            const uint32_t qa = sb + L::kQ + t * L::kTile, ka = sb + L::kK + st * L::kTile;
+          // S_it = Q K^T into score buffer it % 3
+          auto issue_s = [&](int it) {
+            const uint32_t ka = sb + L::kK + (it % SK) * L::kTile;
   #pragma unroll
             for (int kk = 0; kk < D / L::kMmaK; ++kk) {
               // each 128-byte slab row holds four 32-byte K steps
               const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-              mma_ss<kE4M3>(tmem + t * kBlockN, sdesc_sw128(qa + off, 16, 1024),
+              mma_ss<kE4M3>(tmem + (it % kSBufs) * kBlockN, sdesc_sw128(sb + L::kQ + off, 16, 1024),
                             sdesc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
             }
           };
-          // O_t (+)= P_t V; with kscale > 0 the first K step also applies the
-          // uniform rescale O_t <- 2^-kscale O_t of Algorithm 1 steps 2-3.
-          auto issue_pv = [&](int t, int st, bool acc, int kscale) {
-            const uint32_t va = sb + L::kV + st * L::kTile;
+          // TMEM column of the A operand (P~) of K step g: the P~ of keys
+          // 64 h .. 64 h + 63 starts at column 64 h of the buffer
+          auto p_col = [&](int buf, int g) -> uint32_t {
+            return tmem + buf * kBlockN + (g / L::kStepsPerHalf) * 64 + (g % L::kStepsPerHalf) * 8;
+          };
+          // O (+)= P V; with kscale > 0 the first K step also applies the
+          // uniform rescale O <- 2^-kscale O of Algorithm 1 steps 2-3.
+          auto issue_pv = [&](int it, bool acc, int kscale) {
+            const uint32_t va = sb + L::kV + (it % SV) * L::kTile;
   #pragma unroll
-            for (int kk = 0; kk < kBlockN / L::kMmaK; ++kk) {
-              // P~ packs 2 (bf16) or 4 (e4m3) keys per TMEM column: 8 columns per K step
-              const uint32_t d_t = tmem + 2 * kBlockN + t * D, a_t = tmem + t * kBlockN + kk * 8;
-              const uint64_t bd = sdesc_sw128(va + kk * L::kPvStep, 16384, 1024);
-              if (kMmaScale && kk == 0 && acc && kscale > 0)
+            for (int g = 0; g < kBlockN / L::kMmaK; ++g) {
+              const uint32_t d_t = tmem + kOCol, a_t = p_col(it % kSBufs, g);
+              const uint64_t bd = sdesc_sw128(va + g * L::kPvStep, 16384, 1024);
+              if (kMmaScale && g == 0 && acc && kscale > 0)
                 mma_ts_scale_rt(d_t, a_t, bd, idesc_pv, kscale);
               else
-                mma_ts<kE4M3>(d_t, a_t, bd, idesc_pv, acc || kk > 0);
+                mma_ts<kE4M3>(d_t, a_t, bd, idesc_pv, acc || g > 0);
             }
           };
-          volatile uint32_t* pv_scale = misc + 4;
-          auto issue_rs = [&](int t) {
+          auto issue_rs = [&](int it) {
   #pragma unroll
-            for (int kk = 0; kk < kBlockN / L::kMmaK; ++kk)
-              mma_ts<kE4M3>(tmem + t * kBlockN + 64, tmem + t * kBlockN + kk * 8, ones_desc, idesc_rs,
-                            kk > 0);
+            for (int g = 0; g < kBlockN / L::kMmaK; ++g)
+              mma_ts<kE4M3>(tmem + (it % kSBufs) * kBlockN + 32, p_col(it % kSBufs, g), ones_desc,
+                            idesc_rs, g > 0);
+          };
+          // a score buffer is written again only once the tensor row sum
+          // that shared it has been read
+          auto buffer_free = [&](int it) -> bool {
+            if (!kLTensor || it < kSBufs) return true;
+            return __all_sync(0xffffffffu, wait_bounded(bar(L::bLFree + it % kSBufs),
+                                                        ((it - kSBufs) / kSBufs) & 1, p, abort_flag));
+          };
+          auto queue_s = [&](int it) -> bool {
+            if (!buffer_free(it)) return false;
+            if (!__all_sync(0xffffffffu,
+                            wait_bounded(bar(L::bKFull + it % SK), (it / SK) & 1, p, abort_flag)))
+              return false;
+            tc_fence_after();
+            issue_s(it);
+            mma_commit(bar(L::bSFull + it % kSBufs));
+            mma_commit(bar(L::bKEmpty + it % SK));
+            return true;
           };
 
-          if (pass == 0) ok = wait_bounded(bar(L::bQFull), 0, p, abort_flag);
-          if (ok) {
-            const int st = it0 % S;
-            ok = wait_bounded(bar(L::bKFull + st), (it0 / S) & 1, p, abort_flag);
-            if (ok) {
-              tc_fence_after();
-              issue_s(0, st);
-              mma_commit(bar(L::bSFull + 0));
-              issue_s(1, st);
-              mma_commit(bar(L::bSFull + 1));
-              mma_commit(bar(L::bKEmpty + st));
-            }
-          }
+          if (pass == 0) ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bQFull), 0, p, abort_flag));
+          for (int jj = 0; ok && jj < min(kSBufs, n_kv); ++jj) ok = queue_s(it0 + jj);
           for (int j = 0; ok && j < n_kv; ++j) {
-            const int it = it0 + j, st = it % S;
-            const uint32_t ph = (it / S) & 1, par = it & 1;
-            const bool more = j + 1 < n_kv;
-            const int st1 = (it + 1) % S;
-            const uint32_t ph1 = ((it + 1) / S) & 1;
-            if (!(ok = wait_bounded(bar(L::bVFull + st), ph, p, abort_flag))) break;
-            // tile 0
-            if (!(ok = wait_bounded(bar(L::bPFull + 0), par, p, abort_flag))) break;
-            trace_mark(p, 3, 0, j, pass);
+            const int it = it0 + j, buf = it % kSBufs;
+            if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bVFull + it % SV), (it / SV) & 1,
+                                                            p, abort_flag))))
+              break;
+            if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bPFull + buf), (it / kSBufs) & 1,
+                                                            p, abort_flag))))
+              break;
+            if (lane == 0) trace_mark(p, 3, 0, j, pass);
             tc_fence_after();
             if (kLTensor) {
-              issue_rs(0);
-              mma_commit(bar(L::bRsFull + 0));
+              issue_rs(it);
+              mma_commit(bar(L::bRsFull + buf));
             }
-            issue_pv(0, st, j > 0, (kMmaScale && pass == 0) ? static_cast<int>(pv_scale[0]) : 0);
-            if (more) {
-              if (!(ok = wait_bounded(bar(L::bKFull + st1), ph1, p, abort_flag))) break;
-              if (kLTensor && !(ok = wait_bounded(bar(L::bLFree + 0), par, p, abort_flag)))
-                break;
-              tc_fence_after();
-              issue_s(0, st1);
-              mma_commit(bar(L::bSFull + 0));
-            }
-            trace_mark(p, 4, 0, j, pass);
-            // tile 1
-            if (!(ok = wait_bounded(bar(L::bPFull + 1), par, p, abort_flag))) break;
-            trace_mark(p, 3, 1, j, pass);
-            tc_fence_after();
-            if (kLTensor) {
-              issue_rs(1);
-              mma_commit(bar(L::bRsFull + 1));
-            }
-            issue_pv(1, st, j > 0, (kMmaScale && pass == 0) ? static_cast<int>(pv_scale[1]) : 0);
-            mma_commit(bar(L::bVEmpty + st));
-            if (more) {
-              if (kLTensor && !(ok = wait_bounded(bar(L::bLFree + 1), par, p, abort_flag)))
-                break;
-              tc_fence_after();
-              issue_s(1, st1);
-              mma_commit(bar(L::bSFull + 1));
-              mma_commit(bar(L::bKEmpty + st1));
-            }
-            trace_mark(p, 4, 1, j, pass);
+            issue_pv(it, j > 0, (kMmaScale && pass == 0) ? static_cast<int>(misc[4 + buf]) : 0);
+            mma_commit(bar(L::bVEmpty + it % SV));
+            mma_commit(bar(L::bOReady + buf));
+            if (j + kSBufs < n_kv && !(ok = queue_s(it + kSBufs))) break;
+            if (lane == 0) trace_mark(p, 4, 0, j, pass);
           }
           if (ok) {
             mma_commit(bar(L::bOFinal));
@@ -788,7 +817,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
     regs_inc<kSoftmaxRegs>();
     for (int pass = 0; pass < 2; ++pass) {
       const int it0 = pass * n_kv;
-      // =================== softmax warpgroups ===================
+      // =================== softmax warps ===================
       // Pass 1 (only after a flagged pass 0) reruns the block with one-row
       // tiles, X = 1: every row's own maximum rounded up to a whole binade,
       // so no row can underflow (the vector fallback of the page's
