@@ -155,7 +155,7 @@ struct Smem {
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const FwdParams& p,
                                              volatile uint32_t* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   uint64_t polls = 1;
   while (true) {
@@ -722,14 +722,20 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
           const uint64_t ones_desc = sdesc_sw128(sb + L::kOnes, 16, 1024);
           bool ok = true;
           // S_it = Q K^T into score buffer it % 3
+          // Descriptors of the first K step of each operand; a step further
+          // only adds its byte offset >> 4 to the start-address field (shared
+          // memory stays below 256 KB, so the field never overflows).
+          const uint64_t q_desc = sdesc_sw128(sb + L::kQ, 16, 1024);
+          const uint64_t k_desc = sdesc_sw128(sb + L::kK, 16, 1024);
+          const uint64_t v_desc = sdesc_sw128(sb + L::kV, 16384, 1024);
           auto issue_s = [&](int it) {
-            const uint32_t ka = sb + L::kK + (it % SK) * L::kTile;
+            const uint64_t kd = k_desc + static_cast<uint32_t>(((it % SK) * L::kTile) >> 4);
+            const uint32_t d_t = tmem + (it % kSBufs) * kBlockN;
   #pragma unroll
             for (int kk = 0; kk < D / L::kMmaK; ++kk) {
               // each 128-byte slab row holds four 32-byte K steps
-              const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-              mma_ss<kE4M3>(tmem + (it % kSBufs) * kBlockN, sdesc_sw128(sb + L::kQ + off, 16, 1024),
-                            sdesc_sw128(ka + off, 16, 1024), idesc_s, kk > 0);
+              const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+              mma_ss<kE4M3>(d_t, q_desc + off, kd + off, idesc_s, kk > 0);
             }
           };
           // TMEM column of the A operand (P~) of K step g: the P~ of keys
@@ -740,11 +746,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
           // O (+)= P V; with kscale > 0 the first K step also applies the
           // uniform rescale O <- 2^-kscale O of Algorithm 1 steps 2-3.
           auto issue_pv = [&](int it, bool acc, int kscale) {
-            const uint32_t va = sb + L::kV + (it % SV) * L::kTile;
+            const uint64_t vd = v_desc + static_cast<uint32_t>(((it % SV) * L::kTile) >> 4);
   #pragma unroll
             for (int g = 0; g < kBlockN / L::kMmaK; ++g) {
               const uint32_t d_t = tmem + kOCol, a_t = p_col(it % kSBufs, g);
-              const uint64_t bd = sdesc_sw128(va + g * L::kPvStep, 16384, 1024);
+              const uint64_t bd = vd + static_cast<uint32_t>((g * L::kPvStep) >> 4);
               if (kMmaScale && g == 0 && acc && kscale > 0)
                 mma_ts_scale_rt(d_t, a_t, bd, idesc_pv, kscale);
               else
