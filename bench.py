@@ -236,8 +236,8 @@ def phase_trace(fat, torch, w, dev, variant, l_mode, stream, sm_mhz, peak_tflops
     """One traced launch: per-iteration clock stamps of the first thread block.
 
     Returns the median steady-state iteration period (one K/V tile against
-    the block's 128 query rows), the median softmax time per half of the keys
-    (S received -> P published), and the
+    the block's 128 query rows), the median softmax time per K/V tile (S
+    received -> P published, by the set of softmax warps that takes it), and the
     vector-interval ratio: the share of an iteration in which the tensor pipe
     has no work because it waits for the softmax, estimated as
     1 - (ideal tensor cycles of the iteration) / (measured period), with the
@@ -253,12 +253,14 @@ def phase_trace(fat, torch, w, dev, variant, l_mode, stream, sm_mhz, peak_tflops
     stream.synchronize()
     t = tr.cpu().numpy().astype(np.int64)
     ev = t[:10 * I].reshape(5, 2, I)
-    n = int((ev[0, 0] > 0).sum())
+    n = int((ev[3, 0] > 0).sum())
     if n < 12:
         return None
     mid = slice(4, n - 3)
     period = float(np.median(np.diff(ev[3, 0])[mid]))
-    softmax = float(np.median((ev[2] - ev[0])[:, mid]))
+    # the two softmax sets take alternate K/V tiles (set t the tiles j = t mod 2)
+    soft = np.concatenate([(ev[2, t] - ev[0, t])[t:n:2][2:-2] for t in (0, 1)])
+    softmax = float(np.median(soft))
     out = {"period_cycles": period, "softmax_cycles": softmax, "iterations": n}
     if sm_mhz:
         n_sm = torch.cuda.get_device_properties(dev["q"].device).multi_processor_count

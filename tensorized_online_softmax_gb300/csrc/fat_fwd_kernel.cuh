@@ -15,16 +15,15 @@
 //               waits for a slot of the other (K runs three tiles ahead).
 //   warp 8      MMA issuer (one thread): S_j = Q K_j^T into buffer j % 3,
 //               O += P_j V_j, and (row sum on the tensor pipe) l_j = P_j 1.
-//   warps 0-7   softmax: warp w owns TMEM lanes 32 (w % 4) .. +31 (one row
-//               per thread) and keys 64 (w / 4) .. +63 of each K/V tile (one
-//               half of every row): row maximum, X-row tile maximum, O
-//               rescale, P = exp2(Z).
+//   warps 0-7   softmax in two sets of four: set w / 4 takes every other K/V
+//               tile; warp w owns TMEM lanes 32 (w % 4) .. +31 (one row per
+//               thread): row maximum, X-row tile maximum, O rescale,
+//               P = exp2(Z).
 //
 // TMEM (512 columns x 128 lanes, fp32): score buffers [0,128), [128,256),
-// [256,384); O at [384, 384 + D).  P_j overwrites the scores it came from,
-// each half in place (bf16: columns 64h .. 64h+31 of the buffer, two keys per
-// column; e4m3: 64h .. 64h+15, four keys per column); the tensor row sum lands
-// in column 32 of the buffer.
+// [256,384); O at [384, 384 + D).  P_j overwrites the scores it came from
+// (bf16: columns 0-63 of the buffer, two keys per column; e4m3: 0-31, four
+// keys per column); the tensor row sum lands in column 64 of the buffer.
 #pragma once
 
 #include <cuda.h>
@@ -61,9 +60,9 @@ constexpr float kLn2 = 0.6931471805599453f;
 constexpr int kPolyPairs = 0;
 
 // named barriers (0 is __syncthreads)
-constexpr uint32_t kBarPair = 1;  // + quarter: the two warps sharing 32 rows (64 threads)
-constexpr uint32_t kBarHalf = 5;  // + 64-row half: four warps (128 threads), X = 64
-constexpr uint32_t kBarTile = 7;  // all eight softmax warps (256 threads), X = 128
+constexpr uint32_t kBarPair = 1;   // + quarter: the two warps (one per set) of 32 rows
+constexpr uint32_t kBarSet = 5;    // + set: the set's four warps (X = 128)
+constexpr uint32_t kBarGroup = 7;  // + 2 set + half: two warps of a set (X = 64)
 
 struct FwdParams {
   CUtensorMap tm_q;
@@ -92,7 +91,8 @@ struct FwdParams {
 
 // Phase trace of CTA 0, SM clock (clock64) stamps, pass 0 only:
 //   word (e * 2 + t) * kTraceIters + j for event e, K/V tile j, and t = the
-//   half of the keys (softmax events, written by warps 0 and 4) or 0 (MMA):
+//   softmax set that takes tile j (softmax events, written by warps 0 and
+//   4) or 0 (MMA):
 //   e = 0 softmax got S_j, 1 softmax has m_hat, 2 softmax publishes P_j,
 //       3 MMA issuer sees P_j, 4 MMA issuer has queued O += P_j V, S_{j+3};
 //   word kTraceWords - 2 / - 1: kernel start / softmax epilogue done.
@@ -116,7 +116,6 @@ struct Smem {
   static constexpr int kAtomCols = 128 / kElt;        // elements per slab row
   static constexpr int kMmaK = 32 / kElt;             // K of one MMA (bf16 16, e4m3 32)
   static constexpr int kPvStep = kMmaK * 128;         // bytes of V rows per PV K step
-  static constexpr int kStepsPerHalf = 64 / kMmaK;    // PV K steps per 64-key half
   static_assert(kAtoms >= 1, "rows must span at least one 128-byte slab");
   static constexpr int kQ = 0;
   static constexpr int kK = kTile;                     // K ring
@@ -130,20 +129,21 @@ struct Smem {
   static constexpr int bVFull = bKEmpty + kKStages;
   static constexpr int bVEmpty = bVFull + kVStages;
   static constexpr int bSFull = bVEmpty + kVStages;  // [kSBufs]
-  static constexpr int bPFull = bSFull + kSBufs;     // [kSBufs], 8 arrivals
+  static constexpr int bPFull = bSFull + kSBufs;     // [kSBufs], 4 arrivals (one set)
   static constexpr int bRsFull = bPFull + kSBufs;    // [kSBufs]
-  static constexpr int bLFree = bRsFull + kSBufs;    // [kSBufs], 8 arrivals
+  static constexpr int bLFree = bRsFull + kSBufs;    // [kSBufs], 4 arrivals
   // [kSBufs]: O += P_it V landed, it % 3 (per buffer, so that a waiter is
   // never two phases behind: PV_{it-3} has completed once S_it has)
   static constexpr int bOReady = bLFree + kSBufs;
   static constexpr int bOFinal = bOReady + kSBufs;
   static constexpr int bDrain = bOFinal + 1;
-  static constexpr int kNumBars = bDrain + 1;
-  static constexpr int kRed = kBars + 8 * kNumBars;  // float [2 parity][8 warps]
-  static constexpr int kRowRed = kRed + 64;          // float [2 parity][2 halves][128 rows]
-  static constexpr int kFin = kRowRed + 2048;        // float [3][2 halves][128 rows]
+  static constexpr int bMReady = bDrain + 1;         // [2 sets], 4 arrivals: offset published
+  static constexpr int kNumBars = bMReady + 2;
+  static constexpr int kRed = kBars + 8 * kNumBars;  // float [2 sets][2 parity][4 warps]
+  static constexpr int kMRow = kRed + 64;            // float [2 sets][128 rows]: offsets
+  static constexpr int kFin = kMRow + 1024;          // float [4][2 sets][128 rows]
   // u32: tmem base, abort, redo, -, PV scale of each score buffer [3]
-  static constexpr int kMisc = kFin + 3072;
+  static constexpr int kMisc = kFin + 4096;
   static constexpr int kBytes = kMisc + 64;
   static constexpr int kAlloc = kBytes + 1024;       // slack for 1024-byte alignment
   static_assert(kK % 1024 == 0 && kV % 1024 == 0 && kOnes % 1024 == 0, "tiles 1 KB aligned");
@@ -184,8 +184,13 @@ __device__ __forceinline__ float bf16_round(float x) {
 }
 
 // ---------------------------------------------------------------------------
-// softmax warps: warp w owns TMEM lanes 32 (w % 4) .. +31 (row i of the tile
-// = lane i) and keys 64 h .. 64 h + 63 of every K/V tile, h = w / 4.
+// softmax warps: two sets of four.  Set s = w / 4 takes the K/V tiles j with
+// j % 2 == s, and warp w owns TMEM lanes 32 (w % 4) .. +31: one row per
+// thread, all 128 keys of the tile.  The sets work on alternate tiles, so on
+// each SM sub-partition one warp's TMEM loads and maxima run beside the
+// other's exponentials.  The offset of the online softmax passes from tile
+// to tile, i.e. from set to set, through shared memory (one value per row)
+// and one mbarrier per set.
 //   kX > 0   tensorized online softmax with the surrogate maximum over kX-row
 //            tiles (X is a compile-time constant so no runtime branching sits
 //            in the hot loop); `exact` (the fallback pass) uses each row's own
@@ -205,90 +210,112 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
   // terms use the format's range; the factor cancels in O / l and is taken
   // off LSE.
   constexpr float kKappa = kE4M3 ? 8.f : 0.f;
-  constexpr int kHalfD = D / 2;  // O columns this warp rescales and writes
+  constexpr int kHalfD = D / 2;  // O columns this set rescales and writes
   volatile uint32_t* abort_flag = misc + 1;
   auto bar = [&](int i) -> uint32_t { return sb + L::kBars + 8 * i; };
   const int q = warp & 3;        // quarter of the tile (TMEM lanes 32 q ..)
-  const int h = warp >> 2;       // half of the keys
+  const int set = warp >> 2;     // K/V tiles j with j % 2 == set
+  const int other = set ^ 1;
   const int r = q * 32 + lane;   // row within the tile
   const int row_g = m0 + r;
   const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-  const uint32_t o_taddr = tmem + lane_base + kOCol + h * kHalfD;
+  const uint32_t o_taddr = tmem + lane_base + kOCol;
   const float c = p.c;
-  float* red = reinterpret_cast<float*>(smem + L::kRed);
-  float* rowred = reinterpret_cast<float*>(smem + L::kRowRed);
-  float* fin = reinterpret_cast<float*>(smem + L::kFin);
-  // Barrier of the group that shares a surrogate maximum: the pair of warps
-  // holding the same 32 rows (X <= 32, the fallback pass and the vector
-  // variant), four warps (X = 64) or all eight (X = 128).
-  const bool pair_mode = kX <= 32 || exact;
-  const uint32_t gbar_id = pair_mode ? kBarPair + q : (kX == 64 ? kBarHalf + (q >> 1) : kBarTile);
-  const uint32_t gbar_n = pair_mode ? 64 : (kX == 64 ? 128 : 256);
+  float* red = reinterpret_cast<float*>(smem + L::kRed);    // [2 sets][2 parity][4 warps]
+  float* mrow = reinterpret_cast<float*>(smem + L::kMRow);  // [2 sets][128 rows]
+  float* fin = reinterpret_cast<float*>(smem + L::kFin);    // [4][2 sets][128 rows]
+  // Warps of the set that share a surrogate maximum: none besides this one
+  // for X <= 32, the fallback pass and the vector variant; two for X = 64,
+  // the set's four for X = 128.
+  const bool solo = kX <= 32 || exact;
+  const uint32_t gbar_id = kX == 64 ? kBarGroup + set * 2 + (q >> 1) : kBarSet + set;
+  const uint32_t gbar_n = kX == 64 ? 64 : 128;
   const bool mma_scale = kMmaScale && !exact;
+  // the other set's tiles in one pass (completions of its offset barrier)
+  const int n_other = other == 0 ? (n_kv + 1) / 2 : n_kv / 2;
 
-  float M = -INFINITY;      // offset of the exponent, binades (exact row max * c in vec mode)
-  float m_row = -INFINITY;  // running maximum of this half row (whole row in pair mode), logits
-  float l = 0.f;            // running sum of this half row (tensor row sum: whole row)
-  float delta = 0.f;        // tensorized row sum: rounding of each tile's dominant term
-  bool dead = false;        // a bounded wait of this warp (or of its group) ran out
-  int j = 0;
-  // Tensor row sum of an earlier K/V tile (read one tile late so the read
-  // never waits), added with the given rescale factor.
-  auto take_row_sum = [&](int itp, float factor) -> bool {
+  float M = -INFINITY;    // offset of this set's latest tile (per row; uniform over
+                          // the X-row group in the surrogate modes), binades
+  float m_row = -INFINITY;  // exact maximum of this row over this set's tiles, logits
+  float l = 0.f;          // this set's part of the row sum, relative to M
+  float delta = 0.f;      // tensor row sum: rounding of each tile's dominant term
+  bool dead = false;      // a bounded wait of this warp (or of its group) ran out
+  int j = set;
+  int k_local = 0;        // this set's tiles so far in this pass
+  // Tensor row sum of this set's previous tile (read one tile late so the
+  // read never waits); it refers to the offset M of that tile.
+  int rs_pending = -1;
+  auto take_row_sum = [&](int itp) -> bool {
     if (!__all_sync(0xffffffffu, wait_bounded(bar(L::bRsFull + itp % kSBufs),
                                               (itp / kSBufs) & 1, p, abort_flag)))
       return false;
     tc_fence_after();
     uint32_t lt;
-    tmem_ld1(tmem + lane_base + (itp % kSBufs) * kBlockN + 32, lt);
+    tmem_ld1(tmem + lane_base + (itp % kSBufs) * kBlockN + 64, lt);
     tmem_wait_ld1(lt);
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(L::bLFree + itp % kSBufs));
-    l += __uint_as_float(lt) * factor;
+    l += __uint_as_float(lt);
     return true;
   };
+  // offset of tile jj - 1 (the other set's), once that set has settled it
+  auto prev_offset = [&](int jj) -> float {
+    if (jj == 0) return -INFINITY;
+    const int kk = (jj - 1) / 2;  // the other set's tile count
+    if (!__all_sync(0xffffffffu, wait_bounded(bar(L::bMReady + other),
+                                              (pass * n_other + kk) & 1, p, abort_flag))) {
+      dead = true;
+      return -INFINITY;
+    }
+    return mrow[other * kBlockM + r];
+  };
+  auto publish_offset = [&](float Mj) {
+    mrow[set * kBlockM + r] = Mj;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(L::bMReady + set));
+  };
 
-  for (; j < n_kv; ++j) {
+  for (; j < n_kv; j += 2, ++k_local) {
     const int it = it0 + j;
     const int buf = it % kSBufs;
-    const uint32_t par = it & 1;
-    const uint32_t s_taddr = tmem + lane_base + buf * kBlockN + h * 64;
+    const uint32_t par = k_local & 1;
+    const uint32_t s_taddr = tmem + lane_base + buf * kBlockN;
     dead = !__all_sync(0xffffffffu,
                        wait_bounded(bar(L::bSFull + buf), (it / kSBufs) & 1, p, abort_flag));
-    if (q == 0 && lane == 0) trace_mark(p, 0, h, j, pass);
-    // X = 128 (bf16), from the second K/V tile on: steps 4-6 start from the
-    // previous tile's surrogate maximum, and step 1 (the maximum over the
-    // eight warps of the tile) is settled afterwards.  Usually no warp raises
-    // the maximum, which one OR over the tile barrier establishes; a tile that
-    // does raise it has its P~ scaled by the exact power of two
-    // 2^(m_old - m_new).  The P~ that reaches the MMA is the same as when the
-    // maximum is known first.  M is uniform over the tile, and so is this
+    if (q == 0 && lane == 0) trace_mark(p, 0, set, j, pass);
+    // X = 128 (bf16), from this set's second tile on: steps 4-6 start from
+    // the offset of the set's previous tile, and step 1 (the maximum over the
+    // four warps, with the offset of tile j - 1) is settled afterwards.
+    // Usually nothing raises the offset, which one OR over the set's barrier
+    // establishes; a tile that does has its P~ scaled by the exact power of
+    // two 2^(m_old - m_new).  The P~ that reaches the MMA is the same as when
+    // the maximum is known first.  M is uniform over the set, and so is this
     // choice.
     const bool spec = mma_scale && M != -INFINITY;
-    uint32_t s[2][32];
+    uint32_t s[4][32];
     float rowmax = -INFINITY;
     int limit = kBlockN;  // keys of this K/V tile the row may see
     if (!dead) {
       tc_fence_after();
-      tmem_ld32(s_taddr, s[0]);
-      tmem_ld32(s_taddr + 32, s[1]);
-      tmem_wait_ld(s[0]);
-      tmem_wait_ld(s[1]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) tmem_ld32(s_taddr + 32 * k, s[k]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) tmem_wait_ld(s[k]);
       // mask: keys >= N, keys after the query (causal), padding rows
       const int kv0 = kv_begin + j * kBlockN;
       limit = (row_g < p.Nq) ? (p.causal ? min(kv_end, row_g + kv_off + 1) : kv_end) - kv0 : 0;
-      if (limit < h * 64 + 64) {
+      if (limit < kBlockN) {
 #pragma unroll
-        for (int k = 0; k < 2; ++k)
+        for (int k = 0; k < 4; ++k)
 #pragma unroll
           for (int i = 0; i < 32; ++i)
-            if (h * 64 + 32 * k + i >= limit) s[k][i] = __float_as_uint(-INFINITY);
+            if (32 * k + i >= limit) s[k][i] = __float_as_uint(-INFINITY);
       }
-      // half-row maximum as a tree of independent 3-input maxima
-      float mx[4];
+      // row maximum as a tree of independent 3-input maxima
+      float mx[8];
 #pragma unroll
-      for (int a = 0; a < 4; ++a) {
+      for (int a = 0; a < 8; ++a) {
         const int k = a >> 1, b = (a & 1) * 16;
         mx[a] = fmax3(__uint_as_float(s[k][b]), __uint_as_float(s[k][b + 1]),
                       __uint_as_float(s[k][b + 2]));
@@ -297,10 +324,11 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
           mx[a] = fmax3(mx[a], __uint_as_float(s[k][b + i]), __uint_as_float(s[k][b + i + 1]));
         mx[a] = fmaxf(mx[a], __uint_as_float(s[k][b + 15]));
       }
-      rowmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      rowmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7])));
+      m_row = fmaxf(m_row, rowmax);
     }
-    // Algorithm 1 step 1: maximum of the row maxima over the X-row tile.  This
-    // warp's part first (its 32 half rows, or 16-row groups for X = 16) ...
+    // Algorithm 1 step 1: maximum of the row maxima over the X-row tile: this
+    // warp's part (its 32 rows, or 16-row groups for X = 16) ...
     float tmax = rowmax;
     if constexpr (kX == 16) {
 #pragma unroll
@@ -308,73 +336,51 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     } else if constexpr (kX >= 32) {
       tmax = warp_max(rowmax);
     }
-    // ... then across the warps of the group, through shared memory.  Every
-    // warp of a group joins the same sequence of group barriers, aborted or
-    // not (one per K/V tile; two on a speculative tile that raises the
-    // maximum or aborts; see the drain loop below), and the OR spreads an
-    // abort to the whole group.
-    float* slot = red + par * 8;
+    // ... and across the warps of the group (X = 64, 128) through shared
+    // memory.  Every warp of a group joins the same sequence of group
+    // barriers, aborted or not (one per tile; two on a speculative tile that
+    // raises the offset or aborts; see the drain loop below), and the OR
+    // spreads an abort to the whole group.
+    float* slot = red + (set * 2 + par) * 4;
     auto group_max = [&](float v) -> float {
-      if (pair_mode) {
-        rowred[(par * 2 + h) * kBlockM + r] = v;
-        dead = named_bar_or(gbar_id, gbar_n, dead);
-        return dead ? v : fmaxf(v, rowred[(par * 2 + (h ^ 1)) * kBlockM + r]);
-      }
-      if (lane == 0) slot[warp] = v;
+      if (lane == 0) slot[q] = v;
       dead = named_bar_or(gbar_id, gbar_n, dead);
       if (dead) return v;
-      if (kX == 64) {
-        const int w0 = q & 2;
-        return fmaxf(fmaxf(slot[w0], slot[w0 + 1]), fmaxf(slot[w0 + 4], slot[w0 + 5]));
-      }
-      return fmaxf(fmaxf(fmaxf(slot[0], slot[1]), fmaxf(slot[2], slot[3])),
-                   fmaxf(fmaxf(slot[4], slot[5]), fmaxf(slot[6], slot[7])));
+      if (kX == 64) return fmaxf(slot[q & 2], slot[(q & 2) + 1]);
+      return fmaxf(fmaxf(slot[0], slot[1]), fmaxf(slot[2], slot[3]));
     };
 
-    float alpha = 1.f;  // steps 2-3: exp(m_old - m_new)
-    bool vec_rescale = false;
-    int kscale = 0;     // uniform rescale 2^-kscale applied by the PV MMA
+    float E;            // offset of this tile's exponentials (binades)
+    float M_prev = -INFINITY;  // offset of tile j - 1 (O refers to it before PV_j)
+    float M_new = -INFINITY;   // offset of tile j
     if (!spec) {
-      // the fallback pass and the vector variant combine the two halves of
-      // each row; the surrogate modes combine the group's maxima
-      const float gm = group_max((pair_mode && (exact || !kTensor)) ? rowmax : tmax);
+      // the group maximum first (the fallback pass and the vector variant:
+      // each row's own), then the offset of tile j - 1
+      const float gm = solo ? ((exact || !kTensor) ? rowmax : tmax) : group_max(tmax);
       if (dead) break;
-      float M_new;
+      M_prev = prev_offset(j);
+      if (dead) break;
       if constexpr (kTensor) {
         // the surrogate maximum is kept as a whole number of binades so the
         // rescale factor is an exact power of two; the fallback pass uses
         // one-row tiles (each row's own maximum)
-        m_row = fmaxf(m_row, exact ? gm : rowmax);
-        M_new = fmaxf(M, (gm == -INFINITY) ? -INFINITY : ceilf(gm * c));
+        M_new = fmaxf(M_prev, (gm == -INFINITY) ? -INFINITY : ceilf(gm * c));
       } else {
-        m_row = fmaxf(m_row, gm);
-        M_new = (m_row == -INFINITY) ? -INFINITY : m_row * c;
+        M_new = fmaxf(M_prev, (gm == -INFINITY) ? -INFINITY : gm * c);
       }
-      const bool grow = j > 0 && M_new > M;
-      alpha = (M_new == -INFINITY) ? 1.f : ex2_approx(M - M_new);
-      vec_rescale = grow;
-      // With X = 128 the whole tile shares the factor 2^-k and the tensor
-      // pipe applies it inside the next O += P V (scale-input-d).
-      if (mma_scale && grow && M_new - M <= 15.f) {
-        kscale = static_cast<int>(M_new - M);
-        vec_rescale = false;
-      }
-      if (j > 0) {
-        l *= alpha;
-        if (kLTensor) delta *= alpha;
-      }
-      M = M_new;
-      if (q == 0 && lane == 0) trace_mark(p, 1, h, j, pass);
+      publish_offset(M_new);
+      E = M_new;
+      if (q == 0 && lane == 0) trace_mark(p, 1, set, j, pass);
     } else {
-      m_row = fmaxf(m_row, rowmax);
+      E = M;
     }
-    const float neg_M = (M == -INFINITY) ? 0.f : -M;
+    const float neg_E = (E == -INFINITY) ? 0.f : -E;
 
     // steps 4-6: Z = c S - m_hat, P~ = exp2(Z), stored as bf16 (e4m3) over S
-    const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(neg_M + kKappa, neg_M + kKappa);
+    const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(neg_E + kKappa, neg_E + kKappa);
     uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < 4; ++k) {
       float pf[32];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -386,9 +392,9 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
           // the polynomial leaves a tiny positive value for a masked (-inf)
           // key: zero it in the tiles that have masked keys
           f2_unpack(f2_exp2_poly(z0, z1), pf[2 * i], pf[2 * i + 1]);
-          if (limit < h * 64 + 64) {
-            if (h * 64 + 32 * k + 2 * i >= limit) pf[2 * i] = 0.f;
-            if (h * 64 + 32 * k + 2 * i + 1 >= limit) pf[2 * i + 1] = 0.f;
+          if (limit < kBlockN) {
+            if (32 * k + 2 * i >= limit) pf[2 * i] = 0.f;
+            if (32 * k + 2 * i + 1 >= limit) pf[2 * i + 1] = 0.f;
           }
         } else {
           pf[2 * i] = ex2_approx(z0);
@@ -409,58 +415,75 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
         tmem_st16(s_taddr + 16 * k, pk);
       }
     }
-    float lt_vec;  // this tile's half-row sum (vector row sum only)
+    float lt_vec;  // this tile's row sum (vector row sum only), relative to E
     {
       float r0, r1;
       f2_unpack(f2_add(acc2[0], acc2[1]), r0, r1);
       lt_vec = r0 + r1;
     }
+    // step 7 on the tensor pipe: the row sum of this set's previous tile
+    // (relative to that tile's offset M).  It is taken before any wait on the
+    // tensor pipe below: the MMA issuer frees that tile's buffer only after
+    // this read, and queues O += P_{j-1} V behind that.
+    if (kLTensor && rs_pending >= 0 && !dead) {
+      if (!take_row_sum(rs_pending)) dead = true;
+    }
+
     if (spec) {
-      // step 1 completes: does any warp of the tile raise the maximum?
+      // step 1 completes: the offset of tile j - 1, then does anything raise
+      // this set's offset?
+      M_prev = prev_offset(j);
       const float Mc_w = (tmax == -INFINITY) ? -INFINITY : ceilf(tmax * c);
-      const bool any = named_bar_or(gbar_id, gbar_n, dead || Mc_w > M);
+      const bool any = named_bar_or(gbar_id, gbar_n, dead || Mc_w > M || M_prev != M);
+      M_new = M;
       if (any) {
         // rare: exchange the raised maxima (or learn of an abort)
-        if (lane == 0) slot[warp] = Mc_w;
+        if (lane == 0) slot[q] = Mc_w;
         dead = named_bar_or(gbar_id, gbar_n, dead);
         if (dead) break;
-        const float M_new =
-            fmaxf(M, fmaxf(fmaxf(fmaxf(slot[0], slot[1]), fmaxf(slot[2], slot[3])),
-                           fmaxf(fmaxf(slot[4], slot[5]), fmaxf(slot[6], slot[7]))));
-        // M_new > M here: P~ was formed with the old offset.  Multiply it
-        // (and its row sum) by 2^(m_old - m_new), exact in bf16; O takes the
-        // same factor in the PV MMA (at most 15 binades) or from the vector
-        // side.  A jump above 100 binades can only come from logits that far
-        // apart; the block is then redone with per-row maxima (the fallback
-        // pass).
-        const int kb = min(static_cast<int>(M_new - M), 126);  // M, M_new whole binades
-        alpha = __uint_as_float(static_cast<uint32_t>(127 - kb) << 23);  // 2^-kb
-        vec_rescale = kb > 15;
-        kscale = vec_rescale ? 0 : kb;
-        if (kb > 100 && warp == 0 && lane == 0) atomicOr(const_cast<uint32_t*>(misc + 2), 1u);
-        const uint32_t a2 = pack_bf16x2(alpha, alpha);
-        tmem_wait_st();
-        uint32_t pv[32];
-        tmem_ld32(s_taddr, pv);
-        tmem_wait_ld(pv);
+        M_new = fmaxf(M_prev, fmaxf(fmaxf(slot[0], slot[1]), fmaxf(slot[2], slot[3])));
+        if (M_new > M) {
+          // P~ was formed with the old offset: multiply it (and its row sum)
+          // by 2^(m_old - m_new), exact in bf16.  A jump above 100 binades
+          // can only come from logits that far apart; the block is then
+          // redone with per-row maxima (the fallback pass).
+          const int kb = min(static_cast<int>(M_new - M), 126);  // whole binades
+          const float a = __uint_as_float(static_cast<uint32_t>(127 - kb) << 23);  // 2^-kb
+          if (kb > 100 && q == 0 && lane == 0) atomicOr(const_cast<uint32_t*>(misc + 2), 1u);
+          const uint32_t a2 = pack_bf16x2(a, a);
+          tmem_wait_st();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) pv[i] = bf16x2_mul(pv[i], a2);
-        tmem_st32(s_taddr, pv);
-        lt_vec *= alpha;
-        l *= alpha;
-        if (kLTensor) delta *= alpha;
-        M = M_new;
+          for (int hh = 0; hh < 2; ++hh) {
+            uint32_t pv[32];
+            tmem_ld32(s_taddr + 32 * hh, pv);
+            tmem_wait_ld(pv);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) pv[i] = bf16x2_mul(pv[i], a2);
+            tmem_st32(s_taddr + 32 * hh, pv);
+          }
+          lt_vec *= a;
+        }
       }
-      if (q == 0 && lane == 0) trace_mark(p, 1, h, j, pass);
+      publish_offset(M_new);
+      if (q == 0 && lane == 0) trace_mark(p, 1, set, j, pass);
     }
-    // the MMA issuer reads this buffer's PV scale once P_j is published (one
-    // word per buffer: the next tile's value may be written before it reads)
-    if (kMmaScale && warp == 0 && lane == 0) misc[4 + buf] = static_cast<uint32_t>(kscale);
-    const float neg_Mn = (M == -INFINITY) ? 0.f : -M;
-    // steps 2-3 on the vector side: O <- alpha O in TMEM, this warp's half of
-    // the columns, once O += P_{j-1} V has landed (PV_j waits for the P-full
-    // signal below).
+
+    // steps 2-3: O (which refers to the offset of tile j - 1) takes the
+    // factor exp(m_prev - m_new).  X = 128: the same factor for the whole
+    // tile, applied by the tensor pipe inside O += P V (scale-input-d) when it
+    // is at most 15 binades; otherwise (and for the other modes) O is scaled
+    // in TMEM from the vector side once O += P_{j-1} V has landed (PV_j waits
+    // for the P-full signal below).
+    const bool grow = j > 0 && M_new > M_prev;
+    int kscale = 0;
+    bool vec_rescale = grow;
+    if (mma_scale && grow && M_new - M_prev <= 15.f) {
+      kscale = static_cast<int>(M_new - M_prev);
+      vec_rescale = false;
+    }
+    if (kMmaScale && q == 0 && lane == 0) misc[4 + buf] = static_cast<uint32_t>(kscale);
     if (__any_sync(0xffffffffu, vec_rescale)) {
+      const float alpha = grow ? ex2_approx(M_prev - M_new) : 1.f;
       if (!__all_sync(0xffffffffu, wait_bounded(bar(L::bOReady + (it - 1) % kSBufs),
                                                 ((it - 1) / kSBufs) & 1, p, abort_flag))) {
         dead = true;
@@ -468,7 +491,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
         tc_fence_after();
         const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll
-        for (int k = 0; k < kHalfD / 32; ++k) {
+        for (int k = 0; k < D / 32; ++k) {
           uint32_t ov[32];
           tmem_ld32(o_taddr + 32 * k, ov);
           tmem_wait_ld(ov);
@@ -484,34 +507,39 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
         }
       }
     }
+    // step 7: this set's row sum, carried from its previous tile's offset to
+    // this tile's
+    if (M_new != -INFINITY && M != -INFINITY) {
+      const float f = ex2_approx(M - M_new);
+      l *= f;
+      if (kLTensor) delta *= f;
+    }
     if constexpr (kLTensor) {
-      // step 7 on the tensor pipe: the previous tile's row sum (P~ times
-      // ones), taken over to this tile's offset; the LSE also gets back the
-      // rounding of each tile's dominant term
-      if (!dead && j > 0 && !take_row_sum(it - 1, alpha)) dead = true;
+      rs_pending = it;
       if (rowmax != -INFINITY) {
-        const float pm = ex2_approx(fmaf(rowmax, c, neg_Mn + kKappa));
+        const float pm = ex2_approx(fmaf(rowmax, c, kKappa - M_new));
         delta += pm - (kE4M3 ? e4m3_round(pm) : bf16_round(pm));
       }
     } else {
       l += lt_vec;
     }
+    M = M_new;
     tmem_wait_st();
     tc_fence_before();
     __syncwarp();
-    if (q == 0 && lane == 0) trace_mark(p, 2, h, j, pass);
+    if (q == 0 && lane == 0) trace_mark(p, 2, set, j, pass);
     // a warp that gave up still signals; the MMA issuer sees the abort flag
     if (lane == 0) mbar_arrive(bar(L::bPFull + buf));
     if (dead) break;
   }
-  if (dead) {
-    // An aborted warp left the loop at K/V tile j.  If it left at a group
+  if (dead && !solo) {
+    // An aborted warp left the loop at tile j.  If it left at a group
     // barrier, every warp of its group left there too; otherwise (a wait of
     // its own ran out after the group barriers of tile j) the others meet it
     // at the next tile's first barrier, where the OR stops them.  From there
     // on all of them join the same barriers, tile by tile, until the end.
     const bool spec = mma_scale && M != -INFINITY;
-    for (++j; j < n_kv; ++j) {
+    for (j += 2; j < n_kv; j += 2) {
       named_bar_or(gbar_id, gbar_n, true);
       if (spec) named_bar_or(gbar_id, gbar_n, true);
     }
@@ -519,37 +547,45 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
 
   bool ok = !dead;
   if (ok) ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bOFinal), pass & 1, p, abort_flag));
-  if (ok && kLTensor && n_kv > 0) ok = take_row_sum(it0 + n_kv - 1, 1.f);
-  // combine the two halves of every row (both warps of a pair always get here)
-  fin[(0 * 2 + h) * kBlockM + r] = m_row;
-  fin[(1 * 2 + h) * kBlockM + r] = l;
-  fin[(2 * 2 + h) * kBlockM + r] = delta;
+  if (ok && kLTensor && rs_pending >= 0) ok = take_row_sum(rs_pending);
+  // combine the two sets' parts of every row (both warps of a pair get here)
+  fin[(0 * 2 + set) * kBlockM + r] = m_row;
+  fin[(1 * 2 + set) * kBlockM + r] = l;
+  fin[(2 * 2 + set) * kBlockM + r] = delta;
+  fin[(3 * 2 + set) * kBlockM + r] = M;
   named_bar_sync(kBarPair + q, 64);
-  const float m_full = fmaxf(m_row, fin[(0 * 2 + (h ^ 1)) * kBlockM + r]);
-  const float l_full = kLTensor ? l : l + fin[(1 * 2 + (h ^ 1)) * kBlockM + r];
-  const float delta_full = delta + fin[(2 * 2 + (h ^ 1)) * kBlockM + r];
+  const float m_o = fin[(0 * 2 + other) * kBlockM + r];
+  const float l_o = fin[(1 * 2 + other) * kBlockM + r];
+  const float d_o = fin[(2 * 2 + other) * kBlockM + r];
+  const float M_o = fin[(3 * 2 + other) * kBlockM + r];
+  const float m_full = fmaxf(m_row, m_o);
+  const float M_fin = fmaxf(M, M_o);  // the offset of the last tile (offsets only grow)
+  const float f_me = (M == -INFINITY) ? 0.f : ex2_approx(M - M_fin);
+  const float f_o = (M_o == -INFINITY) ? 0.f : ex2_approx(M_o - M_fin);
+  const float l_full = l * f_me + l_o * f_o;
+  const float delta_full = delta * f_me + d_o * f_o;
   if (ok) {
     tc_fence_after();
     // detector for the all-underflow case: surrogate far above the exact
     // maximum, or nothing left of the row sum (counted once per row)
-    if (kTensor && pass == 0 && h == 0) {
+    if (kTensor && pass == 0 && set == 0) {
       // (a row with no key in this split's range is empty, not flagged)
       const bool flagged = row_g < p.Nq && m_full != -INFINITY &&
-                           (!(l_full > 0.f) || (M - m_full * c) > p.underflow_thresh);
+                           (!(l_full > 0.f) || (M_fin - m_full * c) > p.underflow_thresh);
       const uint32_t ball = __ballot_sync(0xffffffffu, flagged);
       if (ball != 0 && lane == 0) {
         atomicOr(const_cast<uint32_t*>(misc + 2), 1u);
         if (p.fallback_rows) atomicAdd(p.fallback_rows, __popc(ball));
       }
     }
-    // epilogue: O / l and LSE
+    // epilogue: O / l (this set's half of the columns) and LSE
     const float inv_l = l_full > 0.f ? p.v_scale / l_full : 0.f;  // an empty row gets O = 0
     const size_t out_row = (static_cast<size_t>(split) * (p.B * p.H) + bh) * p.Nq + row_g;
-    float* orow = (p.o_part ? p.o_part : p.o) + out_row * D + h * kHalfD;
+    float* orow = (p.o_part ? p.o_part : p.o) + out_row * D + set * kHalfD;
 #pragma unroll
     for (int k = 0; k < kHalfD / 32; ++k) {
       uint32_t ov[32];
-      tmem_ld32(o_taddr + 32 * k, ov);
+      tmem_ld32(o_taddr + set * kHalfD + 32 * k, ov);
       tmem_wait_ld(ov);
       if (row_g < p.Nq) {
 #pragma unroll
@@ -561,12 +597,12 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
         }
       }
     }
-    if (r == 0 && h == 0 && pass == 0 && p.trace != nullptr && blockIdx.x == 0)
+    if (r == 0 && set == 0 && pass == 0 && p.trace != nullptr && blockIdx.x == 0)
       p.trace[kTraceWords - 1] = static_cast<unsigned long long>(clock64());
-    if (row_g < p.Nq && h == 0) {
+    if (row_g < p.Nq && set == 0) {
       const float lsum = kLTensor ? l_full + delta_full : l_full;
       (p.lse_part ? p.lse_part : p.lse)[out_row] =
-          l_full > 0.f ? (M - kKappa + __log2f(lsum)) * kLn2 : -INFINITY;
+          l_full > 0.f ? (M_fin - kKappa + __log2f(lsum)) * kLn2 : -INFINITY;
     }
   }
   tc_fence_before();
@@ -639,13 +675,15 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
     }
     for (int b = 0; b < kSBufs; ++b) {
       mbar_init(bar(L::bSFull + b), 1);
-      mbar_init(bar(L::bPFull + b), kSoftmaxWarps);
+      mbar_init(bar(L::bPFull + b), kSoftmaxWarps / 2);
       mbar_init(bar(L::bRsFull + b), 1);
-      mbar_init(bar(L::bLFree + b), kSoftmaxWarps);
+      mbar_init(bar(L::bLFree + b), kSoftmaxWarps / 2);
       mbar_init(bar(L::bOReady + b), 1);
     }
     mbar_init(bar(L::bOFinal), 1);
     mbar_init(bar(L::bDrain), 1);
+    mbar_init(bar(L::bMReady + 0), kSoftmaxWarps / 2);
+    mbar_init(bar(L::bMReady + 1), kSoftmaxWarps / 2);
     misc[1] = 0;
     misc[2] = 0;
     for (int b = 0; b < kSBufs; ++b) misc[4 + b] = 0;
@@ -738,11 +776,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
               mma_ss<kE4M3>(d_t, q_desc + off, kd + off, idesc_s, kk > 0);
             }
           };
-          // TMEM column of the A operand (P~) of K step g: the P~ of keys
-          // 64 h .. 64 h + 63 starts at column 64 h of the buffer
-          auto p_col = [&](int buf, int g) -> uint32_t {
-            return tmem + buf * kBlockN + (g / L::kStepsPerHalf) * 64 + (g % L::kStepsPerHalf) * 8;
-          };
+          // TMEM column of the A operand (P~) of K step g: 8 columns per step
+          auto p_col = [&](int buf, int g) -> uint32_t { return tmem + buf * kBlockN + g * 8; };
           // O (+)= P V; with kscale > 0 the first K step also applies the
           // uniform rescale O <- 2^-kscale O of Algorithm 1 steps 2-3.
           auto issue_pv = [&](int it, bool acc, int kscale) {
@@ -760,7 +795,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
           auto issue_rs = [&](int it) {
   #pragma unroll
             for (int g = 0; g < kBlockN / L::kMmaK; ++g)
-              mma_ts<kE4M3>(tmem + (it % kSBufs) * kBlockN + 32, p_col(it % kSBufs, g), ones_desc,
+              mma_ts<kE4M3>(tmem + (it % kSBufs) * kBlockN + 64, p_col(it % kSBufs, g), ones_desc,
                             idesc_rs, g > 0);
           };
           // a score buffer is written again only once the tensor row sum

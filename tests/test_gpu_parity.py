@@ -231,9 +231,9 @@ def test_bad_arguments_on_device(cuda_device):
 @pytest.mark.parametrize("variant", ["tensor", "vec"])
 def test_phase_trace_is_ordered(cuda_device, variant):
     """The clock stamps of the first thread block follow the pipeline order:
-    S received <= m_hat known <= P published (each half of the keys) <= MMA
-    issuer saw P <= MMA issuer queued the next work, per K/V tile, and the
-    result is unchanged by tracing."""
+    S received <= m_hat known <= P published (by the softmax set that takes
+    the tile) <= MMA issuer saw P <= MMA issuer queued the next work, per K/V
+    tile, and the result is unchanged by tracing."""
     w = gen.Workload("trace", 1, 2, 2048, 128, True, 128, seed=21)
     inp = to_dev(gen.make_inputs(w))
     tr = torch.zeros(fat.TRACE_WORDS, dtype=torch.int64, device="cuda")
@@ -245,12 +245,14 @@ def test_phase_trace_is_ordered(cuda_device, variant):
     t = tr.cpu().numpy()
     ev = t[:10 * fat.TRACE_ITERS].reshape(5, 2, fat.TRACE_ITERS)
     n_kv = 2048 // 128  # the first block holds the last 128 query rows
-    assert (ev[0, 0, :n_kv] > 0).all() and (ev[0, 0, n_kv:] == 0).all()
-    for tt in (0, 1):  # the two halves of the keys
-        e = ev[:, tt, :n_kv]
+    assert (ev[3, 0, :n_kv] > 0).all() and (ev[3, 0, n_kv:] == 0).all()
+    for tt in (0, 1):  # the two softmax sets take alternate K/V tiles
+        e = ev[:, tt, tt:n_kv:2]
+        assert (e[0] > 0).all() and (ev[0, tt, 1 - tt:n_kv:2] == 0).all()
         assert (e[1] >= e[0]).all() and (e[2] >= e[1]).all()
         assert (np.diff(e[0]) > 0).all()
-        # the MMA issuer sees P_j only once both halves have published it
-        assert (ev[3, 0, :n_kv] >= e[2]).all()
+        # the MMA issuer sees P_j only once its set has published it
+        assert (ev[3, 0, tt:n_kv:2] >= e[2]).all()
     assert (ev[4, 0, :n_kv] >= ev[3, 0, :n_kv]).all()
+    assert (np.diff(ev[3, 0, :n_kv]) > 0).all()
     assert t[-1] > t[-2] > 0
