@@ -205,7 +205,6 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
                                              int kv_end, int kv_off) {
   using L = Smem<D, kE4M3>;
   constexpr bool kTensor = kX > 0;
-  constexpr bool kMmaScale = kX == 128 && !kE4M3;
   // e4m3 P~ is formed as 2^(Z + kKappa) <= 2^8 < 448 so that its largest
   // terms use the format's range; the factor cancels in O / l and is taken
   // off LSE.
@@ -230,7 +229,6 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
   const bool solo = kX <= 32 || exact;
   const uint32_t gbar_id = kX == 64 ? kBarGroup + set * 2 + (q >> 1) : kBarSet + set;
   const uint32_t gbar_n = kX == 64 ? 64 : 128;
-  const bool mma_scale = kMmaScale && !exact;
   // the other set's tiles in one pass (completions of its offset barrier)
   const int n_other = other == 0 ? (n_kv + 1) / 2 : n_kv / 2;
 
@@ -284,15 +282,6 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     dead = !__all_sync(0xffffffffu,
                        wait_bounded(bar(L::bSFull + buf), (it / kSBufs) & 1, p, abort_flag));
     if (q == 0 && lane == 0) trace_mark(p, 0, set, j, pass);
-    // X = 128 (bf16), from this set's second tile on: steps 4-6 start from
-    // the offset of the set's previous tile, and step 1 (the maximum over the
-    // four warps, with the offset of tile j - 1) is settled afterwards.
-    // Usually nothing raises the offset, which one OR over the set's barrier
-    // establishes; a tile that does has its P~ scaled by the exact power of
-    // two 2^(m_old - m_new).  The P~ that reaches the MMA is the same as when
-    // the maximum is known first.  M is uniform over the set, and so is this
-    // choice.
-    const bool spec = mma_scale && M != -INFINITY;
     uint32_t s[4][32];
     float rowmax = -INFINITY;
     int limit = kBlockN;  // keys of this K/V tile the row may see
@@ -337,44 +326,45 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       tmax = warp_max(rowmax);
     }
     // ... and across the warps of the group (X = 64, 128) through shared
-    // memory.  Every warp of a group joins the same sequence of group
-    // barriers, aborted or not (one per tile; two on a speculative tile that
-    // raises the offset or aborts; see the drain loop below), and the OR
-    // spreads an abort to the whole group.
+    // memory.  Every warp of a group joins one group barrier per tile,
+    // aborted or not (see the drain loop below); an aborted warp posts NaN,
+    // which tells the others to stop.
     float* slot = red + (set * 2 + par) * 4;
     auto group_max = [&](float v) -> float {
-      if (lane == 0) slot[q] = v;
-      dead = named_bar_or(gbar_id, gbar_n, dead);
-      if (dead) return v;
-      if (kX == 64) return fmaxf(slot[q & 2], slot[(q & 2) + 1]);
-      return fmaxf(fmaxf(slot[0], slot[1]), fmaxf(slot[2], slot[3]));
+      if (lane == 0) slot[q] = dead ? __uint_as_float(0x7fc00000u) : v;
+      named_bar_sync(gbar_id, gbar_n);
+      float a, b;
+      if (kX == 64) {
+        a = slot[q & 2];
+        b = slot[(q & 2) + 1];
+      } else {
+        a = fmaxf(slot[0], slot[1]);
+        b = fmaxf(slot[2], slot[3]);
+        if (isnan(slot[0]) || isnan(slot[1]) || isnan(slot[2]) || isnan(slot[3])) dead = true;
+      }
+      if (isnan(a) || isnan(b)) dead = true;
+      return fmaxf(a, b);
     };
 
-    float E;            // offset of this tile's exponentials (binades)
-    float M_prev = -INFINITY;  // offset of tile j - 1 (O refers to it before PV_j)
-    float M_new = -INFINITY;   // offset of tile j
-    if (!spec) {
-      // the group maximum first (the fallback pass and the vector variant:
-      // each row's own), then the offset of tile j - 1
-      const float gm = solo ? ((exact || !kTensor) ? rowmax : tmax) : group_max(tmax);
-      if (dead) break;
-      M_prev = prev_offset(j);
-      if (dead) break;
-      if constexpr (kTensor) {
-        // the surrogate maximum is kept as a whole number of binades so the
-        // rescale factor is an exact power of two; the fallback pass uses
-        // one-row tiles (each row's own maximum)
-        M_new = fmaxf(M_prev, (gm == -INFINITY) ? -INFINITY : ceilf(gm * c));
-      } else {
-        M_new = fmaxf(M_prev, (gm == -INFINITY) ? -INFINITY : gm * c);
-      }
-      publish_offset(M_new);
-      E = M_new;
-      if (q == 0 && lane == 0) trace_mark(p, 1, set, j, pass);
+    // the group maximum (the fallback pass and the vector variant: each
+    // row's own), then the offset of tile j - 1, which O refers to until
+    // PV_j
+    const float gm = solo ? ((exact || !kTensor) ? rowmax : tmax) : group_max(tmax);
+    if (dead) break;
+    const float M_prev = prev_offset(j);
+    if (dead) break;
+    float M_new;  // offset of tile j (binades)
+    if constexpr (kTensor) {
+      // the surrogate maximum is kept as a whole number of binades so the
+      // rescale factor is an exact power of two; the fallback pass uses
+      // one-row tiles (each row's own maximum)
+      M_new = fmaxf(M_prev, (gm == -INFINITY) ? -INFINITY : ceilf(gm * c));
     } else {
-      E = M;
+      M_new = fmaxf(M_prev, (gm == -INFINITY) ? -INFINITY : gm * c);
     }
-    const float neg_E = (E == -INFINITY) ? 0.f : -E;
+    publish_offset(M_new);
+    if (q == 0 && lane == 0) trace_mark(p, 1, set, j, pass);
+    const float neg_E = (M_new == -INFINITY) ? 0.f : -M_new;
 
     // steps 4-6: Z = c S - m_hat, P~ = exp2(Z), stored as bf16 (e4m3) over S
     const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(neg_E + kKappa, neg_E + kKappa);
@@ -429,59 +419,13 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       if (!take_row_sum(rs_pending)) dead = true;
     }
 
-    if (spec) {
-      // step 1 completes: the offset of tile j - 1, then does anything raise
-      // this set's offset?
-      M_prev = prev_offset(j);
-      const float Mc_w = (tmax == -INFINITY) ? -INFINITY : ceilf(tmax * c);
-      const bool any = named_bar_or(gbar_id, gbar_n, dead || Mc_w > M || M_prev != M);
-      M_new = M;
-      if (any) {
-        // rare: exchange the raised maxima (or learn of an abort)
-        if (lane == 0) slot[q] = Mc_w;
-        dead = named_bar_or(gbar_id, gbar_n, dead);
-        if (dead) break;
-        M_new = fmaxf(M_prev, fmaxf(fmaxf(slot[0], slot[1]), fmaxf(slot[2], slot[3])));
-        if (M_new > M) {
-          // P~ was formed with the old offset: multiply it (and its row sum)
-          // by 2^(m_old - m_new), exact in bf16.  A jump above 100 binades
-          // can only come from logits that far apart; the block is then
-          // redone with per-row maxima (the fallback pass).
-          const int kb = min(static_cast<int>(M_new - M), 126);  // whole binades
-          const float a = __uint_as_float(static_cast<uint32_t>(127 - kb) << 23);  // 2^-kb
-          if (kb > 100 && q == 0 && lane == 0) atomicOr(const_cast<uint32_t*>(misc + 2), 1u);
-          const uint32_t a2 = pack_bf16x2(a, a);
-          tmem_wait_st();
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            uint32_t pv[32];
-            tmem_ld32(s_taddr + 32 * hh, pv);
-            tmem_wait_ld(pv);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) pv[i] = bf16x2_mul(pv[i], a2);
-            tmem_st32(s_taddr + 32 * hh, pv);
-          }
-          lt_vec *= a;
-        }
-      }
-      publish_offset(M_new);
-      if (q == 0 && lane == 0) trace_mark(p, 1, set, j, pass);
-    }
-
     // steps 2-3: O (which refers to the offset of tile j - 1) takes the
-    // factor exp(m_prev - m_new).  X = 128: the same factor for the whole
-    // tile, applied by the tensor pipe inside O += P V (scale-input-d) when it
-    // is at most 15 binades; otherwise (and for the other modes) O is scaled
-    // in TMEM from the vector side once O += P_{j-1} V has landed (PV_j waits
-    // for the P-full signal below).
+    // factor exp(m_prev - m_new), from the vector side and only when the
+    // offset grew -- for X = 128 one factor for the whole tile, a rare event
+    // once the running maximum has settled -- once O += P_{j-1} V has landed
+    // (PV_j waits for the P-full signal below).
     const bool grow = j > 0 && M_new > M_prev;
-    int kscale = 0;
-    bool vec_rescale = grow;
-    if (mma_scale && grow && M_new - M_prev <= 15.f) {
-      kscale = static_cast<int>(M_new - M_prev);
-      vec_rescale = false;
-    }
-    if (kMmaScale && q == 0 && lane == 0) misc[4 + buf] = static_cast<uint32_t>(kscale);
+    const bool vec_rescale = grow;
     if (__any_sync(0xffffffffu, vec_rescale)) {
       const float alpha = grow ? ex2_approx(M_prev - M_new) : 1.f;
       if (!__all_sync(0xffffffffu, wait_bounded(bar(L::bOReady + (it - 1) % kSBufs),
@@ -533,15 +477,14 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     if (dead) break;
   }
   if (dead && !solo) {
-    // An aborted warp left the loop at tile j.  If it left at a group
+    // An aborted warp left the loop at tile j.  If it left at the group
     // barrier, every warp of its group left there too; otherwise (a wait of
-    // its own ran out after the group barriers of tile j) the others meet it
-    // at the next tile's first barrier, where the OR stops them.  From there
-    // on all of them join the same barriers, tile by tile, until the end.
-    const bool spec = mma_scale && M != -INFINITY;
-    for (j += 2; j < n_kv; j += 2) {
-      named_bar_or(gbar_id, gbar_n, true);
-      if (spec) named_bar_or(gbar_id, gbar_n, true);
+    // its own ran out after the group barrier of tile j) the others meet it
+    // at the next tile's barrier, where its NaN stops them.  From there on
+    // all of them join the same barriers, tile by tile, until the end.
+    for (j += 2, ++k_local; j < n_kv; j += 2, ++k_local) {
+      if (lane == 0) red[(set * 2 + (k_local & 1)) * 4 + q] = __uint_as_float(0x7fc00000u);
+      named_bar_sync(gbar_id, gbar_n);
     }
   }
 
@@ -623,8 +566,6 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
   constexpr int SK = L::kKStages;
   constexpr int SV = L::kVStages;
   constexpr bool kTensor = kX > 0;
-  // X = 128 (bf16): the uniform rescale of O rides in the PV MMA
-  constexpr bool kMmaScale = kX == 128 && !kE4M3;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -686,7 +627,6 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
     mbar_init(bar(L::bMReady + 1), kSoftmaxWarps / 2);
     misc[1] = 0;
     misc[2] = 0;
-    for (int b = 0; b < kSBufs; ++b) misc[4 + b] = 0;
     fence_mbar_init();
   }
   if (threadIdx.x < 256) {  // the ones tile used as B of the row-sum MMA
@@ -778,18 +718,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
           };
           // TMEM column of the A operand (P~) of K step g: 8 columns per step
           auto p_col = [&](int buf, int g) -> uint32_t { return tmem + buf * kBlockN + g * 8; };
-          // O (+)= P V; with kscale > 0 the first K step also applies the
-          // uniform rescale O <- 2^-kscale O of Algorithm 1 steps 2-3.
-          auto issue_pv = [&](int it, bool acc, int kscale) {
+          // O (+)= P V
+          auto issue_pv = [&](int it, bool acc) {
             const uint64_t vd = v_desc + static_cast<uint32_t>(((it % SV) * L::kTile) >> 4);
   #pragma unroll
             for (int g = 0; g < kBlockN / L::kMmaK; ++g) {
               const uint32_t d_t = tmem + kOCol, a_t = p_col(it % kSBufs, g);
               const uint64_t bd = vd + static_cast<uint32_t>((g * L::kPvStep) >> 4);
-              if (kMmaScale && g == 0 && acc && kscale > 0)
-                mma_ts_scale_rt(d_t, a_t, bd, idesc_pv, kscale);
-              else
-                mma_ts<kE4M3>(d_t, a_t, bd, idesc_pv, acc || g > 0);
+              mma_ts<kE4M3>(d_t, a_t, bd, idesc_pv, acc || g > 0);
             }
           };
           auto issue_rs = [&](int it) {
@@ -833,7 +769,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
               issue_rs(it);
               mma_commit(bar(L::bRsFull + buf));
             }
-            issue_pv(it, j > 0, (kMmaScale && pass == 0) ? static_cast<int>(misc[4 + buf]) : 0);
+            issue_pv(it, j > 0);
             mma_commit(bar(L::bVEmpty + it % SV));
             mma_commit(bar(L::bOReady + buf));
             if (j + kSBufs < n_kv && !(ok = queue_s(it + kSBufs))) break;

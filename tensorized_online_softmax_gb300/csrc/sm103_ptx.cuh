@@ -180,32 +180,6 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
   }
 }
 
-// D[tmem] = A[tmem] * B[smem]^T + 2^-kScale * D[tmem]   (kind::f16 only; the
-// optional scale-input-d operand, 1 <= kScale <= 15)
-template <int kScale>
-__device__ __forceinline__ void mma_ts_scaled(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                              uint32_t idesc) {
-  asm volatile(
-      "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, 1, 0;\n\t"
-      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p, %4;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "n"(kScale)
-      : "memory");
-}
-
-// Runtime-selected scale 1..15 (a jump table over the immediates).
-__device__ __forceinline__ void mma_ts_scale_rt(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                                uint32_t idesc, int k) {
-  switch (k) {
-#define FAT_SCALE_CASE(n) \
-  case n: mma_ts_scaled<n>(d_tmem, a_tmem, bdesc, idesc); break;
-    FAT_SCALE_CASE(1) FAT_SCALE_CASE(2) FAT_SCALE_CASE(3) FAT_SCALE_CASE(4) FAT_SCALE_CASE(5)
-    FAT_SCALE_CASE(6) FAT_SCALE_CASE(7) FAT_SCALE_CASE(8) FAT_SCALE_CASE(9) FAT_SCALE_CASE(10)
-    FAT_SCALE_CASE(11) FAT_SCALE_CASE(12) FAT_SCALE_CASE(13) FAT_SCALE_CASE(14) FAT_SCALE_CASE(15)
-#undef FAT_SCALE_CASE
-    default: break;
-  }
-}
-
 // Arrive (once) on an mbarrier when every tcgen05 operation this thread issued
 // before has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -373,14 +347,6 @@ __device__ __forceinline__ float e4m3_round(float x) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(b) : "f"(0.f), "f"(x));
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(b));
   return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
-}
-
-// Element-wise product of two bf16 pairs (exact when b is a power of two and
-// the result stays normal).
-__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
