@@ -135,7 +135,8 @@ int fat_attn_fwd_splitkv(const void* q, const void* k, const void* v, float* o, 
 /* Workspace size for fat_attn_fwd_splitkv (0 for invalid arguments). */
 size_t fat_attn_splitkv_workspace_bytes(int B, int H, int Nq, int d, int num_splits);
 
-/* A split count giving about one thread block per SM of the current device. */
+/* A split count giving about eight thread blocks per SM of the current device
+ * (at least four 128-key tiles per split). */
 int fat_attn_splitkv_default_splits(int B, int H, int Nq, int Nk);
 
 /*

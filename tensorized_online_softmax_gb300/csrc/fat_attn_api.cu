@@ -234,9 +234,12 @@ int fat_attn_splitkv_default_splits(int B, int H, int Nq, int Nk) {
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long items = static_cast<long long>(B) * H * ((Nq + fat::kRowsPerCta - 1) / fat::kRowsPerCta);
-  long long s = (sms + items - 1) / items;  // about one thread block per SM
+  // About eight thread blocks per SM (one is resident at a time): enough
+  // waves that the last one is a small part of the run and that every SM
+  // keeps K/V loads in flight; each split keeps at least four K/V tiles.
+  long long s = (8ll * sms + items - 1) / items;
   const long long tiles = (Nk + fat::kBlockN - 1) / fat::kBlockN;
-  if (s > tiles) s = tiles;
+  if (s > tiles / 4) s = tiles / 4;
   if (s > kMaxSplits) s = kMaxSplits;
   return static_cast<int>(s < 1 ? 1 : s);
 }
