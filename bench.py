@@ -44,8 +44,8 @@ L2_FLUSH_BYTES = 256 << 20
 MEASURED_TRAFFIC = {
     "workload": "b2h16n8192d128_causal",
     "variant": "tensor",
-    "bytes": 552.8e6 + 96.3e6,
-    "csrc_sha256": "0ed2b4d77596ad4612cb46ce733d016ca809ff88f5a04d4c32b9151aa8f28be2",
+    "bytes": 905.186e6 + 98.999e6,
+    "csrc_sha256": "ce7314cafb50a20f2f91bdb7b6427b6b4f464fe1bfe56107abb9f101659d5ed9",
 }
 
 
