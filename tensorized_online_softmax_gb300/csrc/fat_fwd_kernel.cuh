@@ -139,7 +139,7 @@ struct Smem {
   static constexpr int bDrain = bOFinal + 1;
   static constexpr int bMReady = bDrain + 1;         // [2 sets], 4 arrivals: offset published
   static constexpr int kNumBars = bMReady + 2;
-  static constexpr int kRed = kBars + 8 * kNumBars;  // float [2 sets][2 parity][4 warps]
+  static constexpr int kRed = (kBars + 8 * kNumBars + 15) & ~15;  // float [2 sets][2 parity][4 warps]
   static constexpr int kMRow = kRed + 64;            // float [2 sets][128 rows]: offsets
   static constexpr int kFin = kMRow + 1024;          // float [4][2 sets][128 rows]
   // u32: tmem base, abort, redo, -, PV scale of each score buffer [3]
@@ -326,41 +326,55 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       tmax = warp_max(rowmax);
     }
     // ... and across the warps of the group (X = 64, 128) through shared
-    // memory.  Every warp of a group joins one group barrier per tile,
-    // aborted or not (see the drain loop below); an aborted warp posts NaN,
-    // which tells the others to stop.
+    // memory.  Every warp of a group joins the same group barriers, aborted
+    // or not (see the drain loop below): one OR per tile, and the exchange
+    // after it when the OR is set; an aborted warp posts NaN there, which
+    // tells the others to stop.
     float* slot = red + (set * 2 + par) * 4;
     auto group_max = [&](float v) -> float {
       if (lane == 0) slot[q] = dead ? __uint_as_float(0x7fc00000u) : v;
       named_bar_sync(gbar_id, gbar_n);
-      float a, b;
+      float m;
       if (kX == 64) {
-        a = slot[q & 2];
-        b = slot[(q & 2) + 1];
+        const float2 ab = *reinterpret_cast<const float2*>(slot + (q & 2));
+        m = fmax_nan(ab.x, ab.y);
       } else {
-        a = fmaxf(slot[0], slot[1]);
-        b = fmaxf(slot[2], slot[3]);
-        if (isnan(slot[0]) || isnan(slot[1]) || isnan(slot[2]) || isnan(slot[3])) dead = true;
+        const float4 s4 = *reinterpret_cast<const float4*>(slot);
+        m = fmax_nan(fmax_nan(s4.x, s4.y), fmax_nan(s4.z, s4.w));
       }
-      if (isnan(a) || isnan(b)) dead = true;
-      return fmaxf(a, b);
+      if (isnan(m)) dead = true;
+      return m;
     };
 
-    // the group maximum (the fallback pass and the vector variant: each
-    // row's own), then the offset of tile j - 1, which O refers to until
-    // PV_j
-    const float gm = solo ? ((exact || !kTensor) ? rowmax : tmax) : group_max(tmax);
-    if (dead) break;
-    const float M_prev = prev_offset(j);
-    if (dead) break;
-    float M_new;  // offset of tile j (binades)
-    if constexpr (kTensor) {
-      // the surrogate maximum is kept as a whole number of binades so the
-      // rescale factor is an exact power of two; the fallback pass uses
-      // one-row tiles (each row's own maximum)
-      M_new = fmaxf(M_prev, (gm == -INFINITY) ? -INFINITY : ceilf(gm * c));
+    // the offset of tile j - 1 (O refers to it until PV_j), then this tile's
+    float M_prev, M_new;  // binades
+    if (!solo) {
+      // X = 64 / 128: the surrogate maximum is kept as a whole number of
+      // binades (so the rescale factor is an exact power of two), and one OR
+      // over the group's barrier settles whether any warp raises it -- rarely
+      // once the running maximum has settled; only then are the warps'
+      // maxima exchanged.  A warp that gave up votes yes and posts NaN.
+      M_prev = prev_offset(j);
+      const float Mc = (tmax == -INFINITY) ? -INFINITY : ceilf(tmax * c);
+      const bool any = named_bar_or(gbar_id, gbar_n, dead || Mc > M_prev);
+      M_new = M_prev;
+      if (any) {
+        const float gmc = group_max(Mc);
+        if (dead) break;
+        M_new = fmaxf(M_prev, gmc);
+      }
     } else {
-      M_new = fmaxf(M_prev, (gm == -INFINITY) ? -INFINITY : gm * c);
+      // X <= 32 within the warp; the fallback pass and the vector variant
+      // each row's own maximum (the fallback pass rounded up to a binade)
+      const float gm = (exact || !kTensor) ? rowmax : tmax;
+      if (dead) break;
+      M_prev = prev_offset(j);
+      if (dead) break;
+      if constexpr (kTensor) {
+        M_new = fmaxf(M_prev, (gm == -INFINITY) ? -INFINITY : ceilf(gm * c));
+      } else {
+        M_new = fmaxf(M_prev, (gm == -INFINITY) ? -INFINITY : gm * c);
+      }
     }
     publish_offset(M_new);
     if (q == 0 && lane == 0) trace_mark(p, 1, set, j, pass);
@@ -483,6 +497,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     // at the next tile's barrier, where its NaN stops them.  From there on
     // all of them join the same barriers, tile by tile, until the end.
     for (j += 2, ++k_local; j < n_kv; j += 2, ++k_local) {
+      named_bar_or(gbar_id, gbar_n, true);
       if (lane == 0) red[(set * 2 + (k_local & 1)) * 4 + q] = __uint_as_float(0x7fc00000u);
       named_bar_sync(gbar_id, gbar_n);
     }

@@ -324,6 +324,11 @@ __device__ __forceinline__ uint64_t f2_exp2_poly(float z0, float z1) {
   return f2_pack(__uint_as_float(r0), __uint_as_float(r1));
 }
 
+__device__ __forceinline__ float fmax_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
 // max of three floats in one instruction
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float r;
