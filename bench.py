@@ -1,7 +1,7 @@
 """Benchmark of the fused attention forward pass (tensorized online softmax) on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--all]
+                    [--workload NAME] [--all] [--sweep]
 
 One step = one pass of the whole hot path (one fat_attn_fwd call) over the
 workload; the default workload is the long-sequence causal shape
@@ -375,6 +375,65 @@ def run_all(args):
                           "frac_hbm": kv_bytes / ms / 1e6 / peaks["hbm_gbs"]}), flush=True)
 
 
+def run_sweep(args):
+    """The pages' sweep (FA-T summary A4, Fig. 8): 16384 tokens (B * N) and
+    hidden size 2048 (H * d), N in 512 .. 8192, d in {64, 128}, causal and
+    non-causal, FP16-FP32 and FP8-FP32 (e4m3 with d = 128), both softmax
+    variants; one JSON line per shape (a Fig.-8-style table)."""
+    import torch
+
+    import tensorized_online_softmax_gb300 as fat
+    from tensorized_online_softmax_gb300 import inputs as gen
+
+    device = torch.device("cuda", 0)
+    peaks = load_peaks()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+    steps = max(5, min(args.steps, 30))
+
+    def timeit(fn):
+        for _ in range(3):
+            flush.zero_()
+            fn()
+        tot = 0.0
+        for _ in range(steps):
+            flush.zero_()
+            s0, s1 = torch.cuda.Event(True), torch.cuda.Event(True)
+            s0.record()
+            fn()
+            s1.record()
+            s1.synchronize()
+            tot += s0.elapsed_time(s1)
+        return tot / steps
+
+    for dtype in ("fp16", "e4m3"):
+        for d in (64, 128):
+            if dtype == "e4m3" and d != 128:
+                continue
+            for N in (512, 1024, 2048, 4096, 8192):
+                for causal in (False, True):
+                    B, H = 16384 // N, 2048 // d
+                    w = gen.Workload(f"sweep_{dtype}_n{N}_d{d}", B, H, N, d, causal, 128,
+                                     dtype=dtype, seed=3000 + N + d)
+                    inp = gen.make_inputs(w)
+                    q, k, v = (inp[n].to(device) for n in ("q", "k", "v"))
+                    kw = {"dtype": dtype}
+                    if dtype == "e4m3":
+                        kw["descales"] = (inp["q_descale"], inp["k_descale"], inp["v_descale"])
+                    arms = {}
+                    for variant in ("tensor", "vec"):
+                        ms = timeit(lambda: fat.attn_fwd(q, k, v, causal, w.scale, w.X,
+                                                         variant=variant, **kw))
+                        arms[variant] = {"ms": ms, "tflops": w.flops / ms / 1e9}
+                    peak = peaks["bf16_tflops"] * (2.0 if dtype == "e4m3" else 1.0)
+                    print(json.dumps({
+                        "sweep": "tokens16384_hidden2048", "dtype": dtype, "B": B, "H": H, "N": N,
+                        "d": d, "causal": causal, "X": w.X, "arms": arms,
+                        "tensor_speedup_vs_vec": arms["vec"]["ms"] / arms["tensor"]["ms"],
+                        "peak_tflops": peak, "frac_tensor": arms["tensor"]["tflops"] / peak}),
+                        flush=True)
+                    del q, k, v, inp
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -387,8 +446,13 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--all", action="store_true",
                     help="one line per workload (results tables) instead of the benchmark line")
+    ap.add_argument("--sweep", action="store_true",
+                    help="the pages' fp16 / fp8 sweep, one line per shape")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.all:
         run_all(args)
         return

@@ -55,7 +55,11 @@ typedef enum {
 } fat_status;
 
 typedef enum { FAT_VARIANT_TENSOR = 0, FAT_VARIANT_VEC = 1 } fat_variant;
-typedef enum { FAT_DTYPE_BF16 = 0, FAT_DTYPE_E4M3 = 1 } fat_dtype;
+/* Input type of q, k, v (fat_attn_fwd_ex): bf16; e4m3 with per-tensor
+ * descales (d = 128 only); fp16 (the FA-T summary's FP16-FP32 setting, A4).
+ * P~ takes the input type for the O += P~ V MMA (fp16 P~ as 2^(Z+15), e4m3 as
+ * 2^(Z+8), to use those formats' ranges; the factor is taken off LSE). */
+typedef enum { FAT_DTYPE_BF16 = 0, FAT_DTYPE_E4M3 = 1, FAT_DTYPE_FP16 = 2 } fat_dtype;
 
 /*
  * Where the row sum l of Algorithm 1 step 7 is formed in the tensorized
@@ -177,8 +181,9 @@ typedef struct fat_params {
   int variant;                        /* fat_variant */
   int dtype;                          /* fat_dtype */
   int l_mode;                         /* fat_lmode (tensorized variant only) */
-  float q_descale, k_descale, v_descale; /* e4m3 only; ignored for bf16 */
-  float underflow_log2_threshold;     /* <= 0: default (64 binades for bf16 P, 6 for e4m3 P) */
+  float q_descale, k_descale, v_descale; /* e4m3 only; ignored otherwise */
+  float underflow_log2_threshold;     /* <= 0: default (64 binades for bf16 P~, 29 for fp16,
+                                         14 for e4m3) */
   int* fallback_rows;                 /* nullable device int: += number of rows recomputed */
   unsigned long long wait_poll_limit; /* 0: no cap on polls of one device wait */
   unsigned long long wait_timeout_ns; /* 0: default of 4 s per device wait */
@@ -190,12 +195,14 @@ typedef struct fat_params {
 } fat_params;
 
 /*
- * Trace layout: word (e * 2 + t) * FAT_TRACE_ITERS + j holds the clock of
- * event e for query tile t (0/1) at K/V tile j (< FAT_TRACE_ITERS), first
- * pass only: e = 0 softmax received S_j; 1 softmax computed m_hat; 2 softmax
- * published P_j; 3 MMA issuer saw P_j; 4 MMA issuer queued O += P_j V and
- * S_{j+1}.  Word FAT_TRACE_WORDS-2: kernel start; FAT_TRACE_WORDS-1: end of
- * the softmax loop.  Words of events that did not happen are left untouched.
+ * Trace layout (first thread block, first pass): word
+ * (e * 2 + t) * FAT_TRACE_ITERS + j holds the clock of event e at K/V tile j
+ * (< FAT_TRACE_ITERS); t = the softmax set that takes tile j (j % 2) for the
+ * softmax events, 0 for the MMA issuer's: e = 0 softmax received S_j; 1
+ * softmax computed m_hat; 2 softmax published P_j; 3 MMA issuer saw P_j; 4
+ * MMA issuer queued O += P_j V and S_{j+3}.  Word FAT_TRACE_WORDS-2: kernel
+ * start; FAT_TRACE_WORDS-1: end of the softmax epilogue.  Words of events
+ * that did not happen are left untouched.
  */
 #define FAT_TRACE_ITERS 128
 #define FAT_TRACE_WORDS (5 * 2 * FAT_TRACE_ITERS + 2)

@@ -35,7 +35,7 @@ FAT_ERR_DEVICE_TIMEOUT = -5
 FAT_ERR_ARCH = -6
 
 VARIANTS = {"tensor": 0, "vec": 1}
-DTYPES = {"bf16": 0, "e4m3": 1}
+DTYPES = {"bf16": 0, "e4m3": 1, "fp16": 2}
 LMODES = {"vector": 0, "tensor": 1}
 TRACE_ITERS = 128
 TRACE_WORDS = 5 * 2 * TRACE_ITERS + 2
@@ -160,8 +160,9 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, X: int =
              l_mode: str = "vector", trace=None):
     """Fused attention forward.  Returns ``(o, lse)`` (fp32 [B,H,N,d], fp32 [B,H,N]).
 
-    ``q, k, v``: contiguous CUDA tensors [B, H, N, d] (bf16, or float8_e4m3fn
-    with ``dtype="e4m3"`` and per-tensor ``descales``).  ``scale`` defaults to
+    ``q, k, v``: contiguous CUDA tensors [B, H, N, d] (bf16; fp16 with
+    ``dtype="fp16"``; or float8_e4m3fn with ``dtype="e4m3"`` and per-tensor
+    ``descales``).  ``scale`` defaults to
     1/sqrt(d).  ``fallback_rows`` is an optional int32 CUDA tensor of one
     element that the kernel increments by the number of rows it recomputed.
     ``l_mode="tensor"`` forms the row sum on the tensor pipe (see fat_lmode in
@@ -171,7 +172,8 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, X: int =
     import torch
 
     lib = load_library()
-    allowed = (torch.bfloat16,) if dtype == "bf16" else (torch.float8_e4m3fn,)
+    allowed = {"bf16": (torch.bfloat16,), "fp16": (torch.float16,),
+               "e4m3": (torch.float8_e4m3fn,)}[dtype]
     _check_inputs(q, k, v, allowed)
     B, H, N, d = q.shape
     if scale is None:

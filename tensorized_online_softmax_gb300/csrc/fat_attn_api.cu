@@ -45,7 +45,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 // [B*H, N, d] view of a contiguous [B, H, N, d] tensor, boxes of 128 rows x
 // 128 bytes, 128-byte swizzle (the layout the tcgen05 descriptors expect).
 // Rows past N read as zero.
-bool encode_qkv_map(CUtensorMap* tm, const void* ptr, int d, int N, int BH, int elt_bytes) {
+bool encode_qkv_map(CUtensorMap* tm, const void* ptr, int d, int N, int BH, int elt_bytes,
+                    CUtensorMapDataType dt) {
   auto enc = encoder();
   if (!enc) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
@@ -54,8 +55,6 @@ bool encode_qkv_map(CUtensorMap* tm, const void* ptr, int d, int N, int BH, int 
                                  static_cast<cuuint64_t>(N) * d * elt_bytes};
   const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / elt_bytes), 128, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
-  const CUtensorMapDataType dt =
-      elt_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   return enc(tm, dt, 3, const_cast<void*>(ptr), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -122,7 +121,8 @@ int run_fwd(const fat_params* p, int Nq, int Nk, int splits, void* workspace,
   if (p->X != 16 && p->X != 32 && p->X != 64 && p->X != 128) return FAT_ERR_INVALID_ARG;
   if (!(p->scale > 0.f) || !std::isfinite(p->scale)) return FAT_ERR_INVALID_ARG;
   if (p->variant != FAT_VARIANT_TENSOR && p->variant != FAT_VARIANT_VEC) return FAT_ERR_INVALID_ARG;
-  if (p->dtype != FAT_DTYPE_BF16 && p->dtype != FAT_DTYPE_E4M3) return FAT_ERR_INVALID_ARG;
+  if (p->dtype != FAT_DTYPE_BF16 && p->dtype != FAT_DTYPE_E4M3 && p->dtype != FAT_DTYPE_FP16)
+    return FAT_ERR_INVALID_ARG;
   if (p->l_mode != FAT_LMODE_VECTOR && p->l_mode != FAT_LMODE_TENSOR) return FAT_ERR_INVALID_ARG;
   if (splits < 1 || splits > kMaxSplits) return FAT_ERR_INVALID_ARG;
   const long long BH = static_cast<long long>(p->B) * p->H;
@@ -159,10 +159,14 @@ int run_fwd(const fat_params* p, int Nq, int Nk, int splits, void* workspace,
   if (arch != FAT_OK) return arch;
 
   fat::FwdParams fp;
+  const bool f16 = p->dtype == FAT_DTYPE_FP16;
   const int elt = e4m3 ? 1 : 2;
-  if (!encode_qkv_map(&fp.tm_q, p->q, p->d, Nq, static_cast<int>(BH), elt) ||
-      !encode_qkv_map(&fp.tm_k, p->k, p->d, Nk, static_cast<int>(BH), elt) ||
-      !encode_qkv_map(&fp.tm_v, p->v, p->d, Nk, static_cast<int>(BH), elt))
+  const CUtensorMapDataType tdt = e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                  : (f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                         : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+  if (!encode_qkv_map(&fp.tm_q, p->q, p->d, Nq, static_cast<int>(BH), elt, tdt) ||
+      !encode_qkv_map(&fp.tm_k, p->k, p->d, Nk, static_cast<int>(BH), elt, tdt) ||
+      !encode_qkv_map(&fp.tm_v, p->v, p->d, Nk, static_cast<int>(BH), elt, tdt))
     return FAT_ERR_LAUNCH;
   fp.o = p->o;
   fp.lse = p->lse;
@@ -182,8 +186,9 @@ int run_fwd(const fat_params* p, int Nq, int Nk, int splits, void* workspace,
   fp.c = e4m3 ? p->scale * p->q_descale * p->k_descale * fat::kLog2e : p->scale * fat::kLog2e;
   fp.v_scale = e4m3 ? p->v_descale : 1.f;
   // bf16 P~ keeps fp32's exponent range (2^-64 leaves 62 binades); e4m3 P~ =
-  // 2^(Z+8) has its smallest normal at 2^-6, i.e. Z = -14
-  const float t_default = e4m3 ? 14.f : 64.f;
+  // 2^(Z+8) has its smallest normal at 2^-6, i.e. Z = -14; fp16 P~ = 2^(Z+15)
+  // at 2^-14, i.e. Z = -29
+  const float t_default = e4m3 ? 14.f : (f16 ? 29.f : 64.f);
   fp.underflow_thresh =
       p->underflow_log2_threshold > 0.f ? p->underflow_log2_threshold : t_default;
   fp.poll_limit = p->wait_poll_limit;
@@ -199,6 +204,12 @@ int run_fwd(const fat_params* p, int Nq, int Nk, int splits, void* workspace,
   if (e4m3)
     st = l_tensor ? fat::dispatch_e4m3_d128_ltensor(fp, X, dev, grid, n_splits, p->stream)
                   : fat::dispatch_e4m3_d128_lvec(fp, X, dev, grid, n_splits, p->stream);
+  else if (f16 && p->d == 128)
+    st = l_tensor ? fat::dispatch_f16_d128_ltensor(fp, X, dev, grid, n_splits, p->stream)
+                  : fat::dispatch_f16_d128_lvec(fp, X, dev, grid, n_splits, p->stream);
+  else if (f16)
+    st = l_tensor ? fat::dispatch_f16_d64_ltensor(fp, X, dev, grid, n_splits, p->stream)
+                  : fat::dispatch_f16_d64_lvec(fp, X, dev, grid, n_splits, p->stream);
   else if (p->d == 128)
     st = l_tensor ? fat::dispatch_bf16_d128_ltensor(fp, X, dev, grid, n_splits, p->stream)
                   : fat::dispatch_bf16_d128_lvec(fp, X, dev, grid, n_splits, p->stream);

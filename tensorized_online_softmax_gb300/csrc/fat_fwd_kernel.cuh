@@ -51,6 +51,10 @@ constexpr int kSoftmaxRegs = 224;
 static_assert(256 * kSoftmaxRegs + 128 * kCtrlRegs <= kNumThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr uint32_t kTmemCols = 512;
+// input types (template argument kDt)
+constexpr int kDtBf16 = 0;
+constexpr int kDtE4M3 = 1;
+constexpr int kDtF16 = 2;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 // Of the 16 element pairs in each 32-column chunk of a half row, this many
@@ -182,6 +186,7 @@ __device__ __forceinline__ void wait_drain(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ float bf16_round(float x) {
   return __bfloat162float(__float2bfloat16_rn(x));
 }
+__device__ __forceinline__ float f16_round(float x) { return __half2float(__float2half_rn(x)); }
 
 // ---------------------------------------------------------------------------
 // softmax warps: two sets of four.  Set s = w / 4 takes the K/V tiles j with
@@ -197,18 +202,19 @@ __device__ __forceinline__ float bf16_round(float x) {
 //            maximum instead, rounded up to a whole binade.
 //   kX == 0  the vector-softmax ablation: exact per-row maximum.
 // ---------------------------------------------------------------------------
-template <int D, int kX, bool kLTensor, bool kE4M3>
+template <int D, int kX, bool kLTensor, int kDt>
 __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, uint32_t sb,
                                              uint32_t tmem, volatile uint32_t* misc, int warp,
                                              int lane, int m0, int bh, int n_kv, int it0,
                                              int pass, bool exact, int split, int kv_begin,
                                              int kv_end, int kv_off) {
+  constexpr bool kE4M3 = kDt == kDtE4M3;
   using L = Smem<D, kE4M3>;
   constexpr bool kTensor = kX > 0;
-  // e4m3 P~ is formed as 2^(Z + kKappa) <= 2^8 < 448 so that its largest
-  // terms use the format's range; the factor cancels in O / l and is taken
-  // off LSE.
-  constexpr float kKappa = kE4M3 ? 8.f : 0.f;
+  // e4m3 (fp16) P~ is formed as 2^(Z + kKappa) <= 2^8 < 448 (2^15 < 65504)
+  // so that its terms use the format's range; the factor cancels in O / l and
+  // is taken off LSE.  bf16 has fp32's exponent range and needs none.
+  constexpr float kKappa = kE4M3 ? 8.f : (kDt == kDtF16 ? 15.f : 0.f);
   constexpr int kHalfD = D / 2;  // O columns this set rescales and writes
   volatile uint32_t* abort_flag = misc + 1;
   auto bar = [&](int i) -> uint32_t { return sb + L::kBars + 8 * i; };
@@ -415,7 +421,9 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       } else {
         uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16x2(pf[2 * i], pf[2 * i + 1]);
+        for (int i = 0; i < 16; ++i)
+          pk[i] = kDt == kDtF16 ? pack_f16x2(pf[2 * i], pf[2 * i + 1])
+                                : pack_bf16x2(pf[2 * i], pf[2 * i + 1]);
         tmem_st16(s_taddr + 16 * k, pk);
       }
     }
@@ -476,7 +484,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       rs_pending = it;
       if (rowmax != -INFINITY) {
         const float pm = ex2_approx(fmaf(rowmax, c, kKappa - M_new));
-        delta += pm - (kE4M3 ? e4m3_round(pm) : bf16_round(pm));
+        delta += pm - (kE4M3 ? e4m3_round(pm) : (kDt == kDtF16 ? f16_round(pm) : bf16_round(pm)));
       }
     } else {
       l += lt_vec;
@@ -574,9 +582,11 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
 // kLTensor: (kTensor only) the row sum of step 7 on the tensor pipe as
 //           P~ (bf16) times a block of ones; otherwise an fp32 sum of the
 //           unrounded P~ on the vector units.
-// kE4M3:    e4m3 inputs, kind::f8f6f4 MMAs, e4m3 P~ (otherwise bf16).
-template <int D, int kX, bool kLTensor, bool kE4M3>
+// kDt:      input type: kDtBf16 (kind::f16 MMAs, bf16 P~), kDtF16 (kind::f16,
+//           fp16 P~) or kDtE4M3 (kind::f8f6f4, e4m3 P~).
+template <int D, int kX, bool kLTensor, int kDt>
 __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_constant__ FwdParams p) {
+  constexpr bool kE4M3 = kDt == kDtE4M3;
   using L = Smem<D, kE4M3>;
   constexpr int SK = L::kKStages;
   constexpr int SV = L::kVStages;
@@ -645,8 +655,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
     fence_mbar_init();
   }
   if (threadIdx.x < 256) {  // the ones tile used as B of the row-sum MMA
-    // 1.0 in bf16 (0x3F80) or e4m3 (0x38)
-    const uint32_t one = kE4M3 ? 0x38383838u : 0x3F803F80u;
+    // 1.0 in bf16 (0x3F80), fp16 (0x3C00) or e4m3 (0x38)
+    const uint32_t one = kE4M3 ? 0x38383838u : (kDt == kDtF16 ? 0x3C003C00u : 0x3F803F80u);
     reinterpret_cast<uint2*>(smem + L::kOnes)[threadIdx.x] = make_uint2(one, one);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -709,9 +719,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
         // The whole warp runs this code with warp-uniform values; one elected
         // lane issues each MMA and commit.
         {
-          constexpr uint32_t idesc_s = idesc_f32acc<kE4M3>(kBlockM, kBlockN, false);
-          constexpr uint32_t idesc_pv = idesc_f32acc<kE4M3>(kBlockM, D, true);
-          constexpr uint32_t idesc_rs = idesc_f32acc<kE4M3>(kBlockM, 16, false);
+          // A/B format codes: bf16 1; fp16 0 (kind::f16); e4m3 0 (kind::f8f6f4)
+          constexpr uint32_t kFmt = kDt == kDtBf16 ? 1u : 0u;
+          constexpr uint32_t idesc_s = idesc_f32acc<kFmt>(kBlockM, kBlockN, false);
+          constexpr uint32_t idesc_pv = idesc_f32acc<kFmt>(kBlockM, D, true);
+          constexpr uint32_t idesc_rs = idesc_f32acc<kFmt>(kBlockM, 16, false);
           const uint64_t ones_desc = sdesc_sw128(sb + L::kOnes, 16, 1024);
           bool ok = true;
           // S_it = Q K^T into score buffer it % 3
@@ -814,7 +826,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
       // tiles, X = 1: every row's own maximum rounded up to a whole binade,
       // so no row can underflow (the vector fallback of the page's
       // all-underflow discussion, on the same code path).
-      softmax_role<D, kX, kLTensor, kE4M3>(p, smem, sb, tmem, misc, warp, lane, m0, bh, n_kv, it0,
+      softmax_role<D, kX, kLTensor, kDt>(p, smem, sb, tmem, misc, warp, lane, m0, bh, n_kv, it0,
                                            pass, /*exact=*/pass == 1, split, kv_begin, kv_end,
                                            kv_off);
       __syncthreads();

@@ -2,5 +2,5 @@
 #include "fat_launch.cuh"
 
 namespace fat {
-FAT_DEFINE_DISPATCH(dispatch_bf16_d128_ltensor, 128, true, false)
+FAT_DEFINE_DISPATCH(dispatch_bf16_d128_ltensor, 128, true, kDtBf16)
 }  // namespace fat

@@ -2,5 +2,5 @@
 #include "fat_launch.cuh"
 
 namespace fat {
-FAT_DEFINE_DISPATCH(dispatch_bf16_d128_lvec, 128, false, false)
+FAT_DEFINE_DISPATCH(dispatch_bf16_d128_lvec, 128, false, kDtBf16)
 }  // namespace fat

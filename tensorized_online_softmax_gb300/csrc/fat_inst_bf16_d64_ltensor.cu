@@ -2,5 +2,5 @@
 #include "fat_launch.cuh"
 
 namespace fat {
-FAT_DEFINE_DISPATCH(dispatch_bf16_d64_ltensor, 64, true, false)
+FAT_DEFINE_DISPATCH(dispatch_bf16_d64_ltensor, 64, true, kDtBf16)
 }  // namespace fat

@@ -2,5 +2,5 @@
 #include "fat_launch.cuh"
 
 namespace fat {
-FAT_DEFINE_DISPATCH(dispatch_e4m3_d128_ltensor, 128, true, true)
+FAT_DEFINE_DISPATCH(dispatch_e4m3_d128_ltensor, 128, true, kDtE4M3)
 }  // namespace fat

@@ -2,5 +2,5 @@
 #include "fat_launch.cuh"
 
 namespace fat {
-FAT_DEFINE_DISPATCH(dispatch_e4m3_d128_lvec, 128, false, true)
+FAT_DEFINE_DISPATCH(dispatch_e4m3_d128_lvec, 128, false, kDtE4M3)
 }  // namespace fat

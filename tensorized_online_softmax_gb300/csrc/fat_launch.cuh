@@ -12,11 +12,11 @@ namespace fat {
 constexpr int kMaxDevices = 64;
 
 // Returns 0 or the fat_status code FAT_ERR_LAUNCH (-4).
-template <int D, int kX, bool kLTensor, bool kE4M3>
+template <int D, int kX, bool kLTensor, int kDt>
 int launch_fwd(const FwdParams& fp, int dev, int grid, int splits, cudaStream_t stream) {
   static int ready[kMaxDevices];  // per device: attributes checked and set
-  auto kern = fat_fwd_kernel<D, kX, kLTensor, kE4M3>;
-  const int smem = Smem<D, kE4M3>::kAlloc;
+  auto kern = fat_fwd_kernel<D, kX, kLTensor, kDt>;
+  const int smem = Smem<D, kDt == kDtE4M3>::kAlloc;
   if (!ready[dev]) {
     // The warpgroup register split inside the kernel assumes exactly
     // kLaunchRegs registers per thread at launch; anything else could make
@@ -46,18 +46,22 @@ FAT_DECLARE_DISPATCH(dispatch_bf16_d64_lvec)
 FAT_DECLARE_DISPATCH(dispatch_bf16_d64_ltensor)
 FAT_DECLARE_DISPATCH(dispatch_e4m3_d128_lvec)
 FAT_DECLARE_DISPATCH(dispatch_e4m3_d128_ltensor)
+FAT_DECLARE_DISPATCH(dispatch_f16_d128_lvec)
+FAT_DECLARE_DISPATCH(dispatch_f16_d128_ltensor)
+FAT_DECLARE_DISPATCH(dispatch_f16_d64_lvec)
+FAT_DECLARE_DISPATCH(dispatch_f16_d64_ltensor)
 #undef FAT_DECLARE_DISPATCH
 
-#define FAT_DEFINE_DISPATCH(name, D, LT, E4M3)                                  \
+#define FAT_DEFINE_DISPATCH(name, D, LT, DT)                                  \
   int name(const FwdParams& fp, int X, int dev, int grid, int splits, cudaStream_t stream) { \
     switch (X) {                                                                 \
       case 0:                                                                    \
-        if constexpr (!(LT)) return launch_fwd<D, 0, false, E4M3>(fp, dev, grid, splits, stream); \
+        if constexpr (!(LT)) return launch_fwd<D, 0, false, DT>(fp, dev, grid, splits, stream); \
         return -1;                                                               \
-      case 16: return launch_fwd<D, 16, LT, E4M3>(fp, dev, grid, splits, stream);        \
-      case 32: return launch_fwd<D, 32, LT, E4M3>(fp, dev, grid, splits, stream);        \
-      case 64: return launch_fwd<D, 64, LT, E4M3>(fp, dev, grid, splits, stream);        \
-      case 128: return launch_fwd<D, 128, LT, E4M3>(fp, dev, grid, splits, stream);      \
+      case 16: return launch_fwd<D, 16, LT, DT>(fp, dev, grid, splits, stream);        \
+      case 32: return launch_fwd<D, 32, LT, DT>(fp, dev, grid, splits, stream);        \
+      case 64: return launch_fwd<D, 64, LT, DT>(fp, dev, grid, splits, stream);        \
+      case 128: return launch_fwd<D, 128, LT, DT>(fp, dev, grid, splits, stream);      \
       default: return -1;                                                        \
     }                                                                            \
   }

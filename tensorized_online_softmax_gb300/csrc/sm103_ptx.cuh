@@ -126,13 +126,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
   return d;
 }
 
-// Instruction descriptor for kind::f16 (bf16 x bf16 -> f32) and kind::f8f6f4
-// (e4m3 x e4m3 -> f32): D format F32 at bit 4, A/B formats at bits 7 and 10,
-// B major-ness at bit 16 (0 = K-major, 1 = MN-major), N >> 3 at bit 17,
-// M >> 4 at bit 24.
-template <bool kE4M3>
+// Instruction descriptor for kind::f16 (bf16 or fp16 inputs -> f32) and
+// kind::f8f6f4 (e4m3 -> f32): D format F32 at bit 4, A/B format codes at
+// bits 7 and 10 (kind::f16: 0 fp16, 1 bf16; kind::f8f6f4: 0 e4m3), B
+// major-ness at bit 16 (0 = K-major, 1 = MN-major), N >> 3 at bit 17, M >> 4
+// at bit 24.
+template <uint32_t kFmt>
 __host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool b_mn_major) {
-  return (1u << 4) | ((kE4M3 ? 0u : 1u) << 7) | ((kE4M3 ? 0u : 1u) << 10) |
+  return (1u << 4) | (kFmt << 7) | (kFmt << 10) |
          ((b_mn_major ? 1u : 0u) << 16) | ((static_cast<uint32_t>(N) >> 3) << 17) |
          ((static_cast<uint32_t>(M) >> 4) << 24);
 }
@@ -352,6 +353,12 @@ __device__ __forceinline__ float e4m3_round(float x) {
   asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(b) : "f"(0.f), "f"(x));
   asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(b));
   return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

@@ -45,7 +45,7 @@ class Workload:
     d: int
     causal: bool
     X: int
-    dtype: str = "bf16"  # "bf16" or "e4m3"
+    dtype: str = "bf16"  # "bf16", "fp16" or "e4m3"
     kind: str = "normal"  # "normal", "stress" or "growth"
     seed: int = 0
     shift_coord: float = 15.5  # stress only
@@ -128,6 +128,8 @@ def make_inputs(w: Workload):
         k[..., w.d - 1] = (w.growth_nats / w.scale) * tile
     if w.dtype == "bf16":
         out.update(q=q.to(torch.bfloat16), k=k.to(torch.bfloat16), v=v.to(torch.bfloat16))
+    elif w.dtype == "fp16":
+        out.update(q=q.to(torch.float16), k=k.to(torch.float16), v=v.to(torch.float16))
     elif w.dtype == "e4m3":
         for name, t in (("q", q), ("k", k), ("v", v)):
             s = float(t.abs().max()) / E4M3_MAX
