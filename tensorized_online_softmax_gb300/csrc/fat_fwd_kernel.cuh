@@ -685,7 +685,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
           const bool is_k = warp == kLoadWarp;
           const int S = is_k ? SK : SV;
           const int full = is_k ? L::bKFull : L::bVFull;
-          const int empty = is_k ? L::bKEmpty : L::bVEmpty;
+          // with as many V stages as score buffers, "V stage free" and "O +=
+          // P V landed" are the same event: one barrier serves both
+          const int empty = is_k ? L::bKEmpty : (SV == kSBufs ? L::bOReady : L::bVEmpty);
           const int ring = is_k ? L::kK : L::kV;
           const CUtensorMap* tm = is_k ? &p.tm_k : &p.tm_v;
           int issued = 0;
@@ -797,7 +799,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
               mma_commit(bar(L::bRsFull + buf));
             }
             issue_pv(it, j > 0);
-            mma_commit(bar(L::bVEmpty + it % SV));
+            if (SV != kSBufs) mma_commit(bar(L::bVEmpty + it % SV));
             mma_commit(bar(L::bOReady + buf));
             if (j + kSBufs < n_kv && !(ok = queue_s(it + kSBufs))) break;
             if (lane == 0) trace_mark(p, 4, 0, j, pass);
