@@ -385,6 +385,13 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     publish_offset(M_new);
     if (q == 0 && lane == 0) trace_mark(p, 1, set, j, pass);
     const float neg_E = (M_new == -INFINITY) ? 0.f : -M_new;
+    // step 7 on the tensor pipe: the row sum of this set's previous tile
+    // (relative to that tile's offset M), taken before the exponentials and
+    // before any wait on the tensor pipe: the MMA issuer reuses that tile's
+    // score buffer (and queues O += P_{j-1} V behind it) only after this read.
+    if (kLTensor && rs_pending >= 0 && !dead) {
+      if (!take_row_sum(rs_pending)) dead = true;
+    }
 
     // steps 4-6: Z = c S - m_hat, P~ = exp2(Z), stored as bf16 (e4m3) over S
     const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(neg_E + kKappa, neg_E + kKappa);
@@ -432,13 +439,6 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       float r0, r1;
       f2_unpack(f2_add(acc2[0], acc2[1]), r0, r1);
       lt_vec = r0 + r1;
-    }
-    // step 7 on the tensor pipe: the row sum of this set's previous tile
-    // (relative to that tile's offset M).  It is taken before any wait on the
-    // tensor pipe below: the MMA issuer frees that tile's buffer only after
-    // this read, and queues O += P_{j-1} V behind that.
-    if (kLTensor && rs_pending >= 0 && !dead) {
-      if (!take_row_sum(rs_pending)) dead = true;
     }
 
     // steps 2-3: O (which refers to the offset of tile j - 1) takes the
