@@ -57,11 +57,6 @@ constexpr int kDtE4M3 = 1;
 constexpr int kDtF16 = 2;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
-// Of the 16 element pairs in each 32-column chunk of a half row, this many
-// take 2^z from the FMA-pipe polynomial (f2_exp2_poly) and the rest from MUFU
-// ex2: one MUFU ex2 costs a warp 8 issue cycles of its pipe (16 results per SM
-// per cycle), the polynomial about 5 single-cycle instructions per element.
-constexpr int kPolyPairs = 0;
 
 // named barriers (0 is __syncthreads)
 constexpr uint32_t kBarPair = 1;   // + quarter: the two warps (one per set) of 32 rows
@@ -405,18 +400,8 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
                                           __uint_as_float(s[k][2 * i + 1])), c2, nm2);
         float z0, z1;
         f2_unpack(z, z0, z1);
-        if ((i * kPolyPairs) % 16 < kPolyPairs) {
-          // the polynomial leaves a tiny positive value for a masked (-inf)
-          // key: zero it in the tiles that have masked keys
-          f2_unpack(f2_exp2_poly(z0, z1), pf[2 * i], pf[2 * i + 1]);
-          if (limit < kBlockN) {
-            if (32 * k + 2 * i >= limit) pf[2 * i] = 0.f;
-            if (32 * k + 2 * i + 1 >= limit) pf[2 * i + 1] = 0.f;
-          }
-        } else {
-          pf[2 * i] = ex2_approx(z0);
-          pf[2 * i + 1] = ex2_approx(z1);
-        }
+        pf[2 * i] = ex2_approx(z0);
+        pf[2 * i + 1] = ex2_approx(z1);
         if (!kLTensor) acc2[i & 1] = f2_add(acc2[i & 1], f2_pack(pf[2 * i], pf[2 * i + 1]));
       }
       if constexpr (kE4M3) {

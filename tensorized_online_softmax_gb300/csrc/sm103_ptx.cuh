@@ -299,32 +299,6 @@ __device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
   return r;
 }
-// 2^z for a pair of floats on the FMA and integer pipes, leaving the MUFU
-// unit to the other elements of a row.  Cody and Waite's argument split:
-// n = round(z) (the fp32 add of 1.5 * 2^23 rounds to an integer and leaves it
-// in the low mantissa bits), f = z - n in [-1/2, 1/2]; 2^f by a degree-3
-// polynomial (coefficients from a Lawson minimax fit of the relative error on
-// [-1/2, 1/2], max relative error 7.5e-5); n is then added to the exponent
-// field.  z is clamped to -126 first, so inputs below that (and -inf) give a
-// value under 2^-125 instead of 0.
-__device__ __forceinline__ uint64_t f2_exp2_poly(float z0, float z1) {
-  constexpr float kRound = 12582912.f;  // 1.5 * 2^23
-  const uint64_t zc = f2_pack(fmaxf(z0, -126.f), fmaxf(z1, -126.f));
-  const uint64_t t = f2_add(zc, f2_pack(kRound, kRound));
-  const uint64_t n = f2_add(t, f2_pack(-kRound, -kRound));
-  const uint64_t f = f2_fma(n, f2_pack(-1.f, -1.f), zc);
-  uint64_t q = f2_fma(f, f2_pack(0.0551716685f, 0.0551716685f),
-                      f2_pack(0.242611125f, 0.242611125f));
-  q = f2_fma(q, f, f2_pack(0.693260968f, 0.693260968f));
-  q = f2_fma(q, f, f2_pack(0.999928057f, 0.999928057f));
-  float q0, q1, t0, t1;
-  f2_unpack(q, q0, q1);
-  f2_unpack(t, t0, t1);
-  const uint32_t r0 = __float_as_uint(q0) + (__float_as_uint(t0) << 23);
-  const uint32_t r1 = __float_as_uint(q1) + (__float_as_uint(t1) << 23);
-  return f2_pack(__uint_as_float(r0), __uint_as_float(r1));
-}
-
 __device__ __forceinline__ float fmax_nan(float a, float b) {
   float r;
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
