@@ -60,6 +60,22 @@ bool encode_qkv_map(CUtensorMap* tm, const void* ptr, int d, int N, int BH, int 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 O viewed as [rows, N, d]: 32-column x 128-row boxes, 128-byte
+// swizzle (the layout the kernel stages O in).
+bool encode_o_map(CUtensorMap* tm, float* ptr, int d, int N, long long rows) {
+  auto enc = encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                                 static_cast<cuuint64_t>(N) * d * 4};
+  const cuuint32_t box[3] = {32, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 int check_device(int* dev_out) {
@@ -167,6 +183,9 @@ int run_fwd(const fat_params* p, int Nq, int Nk, int splits, void* workspace,
   if (!encode_qkv_map(&fp.tm_q, p->q, p->d, Nq, static_cast<int>(BH), elt, tdt) ||
       !encode_qkv_map(&fp.tm_k, p->k, p->d, Nk, static_cast<int>(BH), elt, tdt) ||
       !encode_qkv_map(&fp.tm_v, p->v, p->d, Nk, static_cast<int>(BH), elt, tdt))
+    return FAT_ERR_LAUNCH;
+  if (!encode_o_map(&fp.tm_o, o_part ? o_part : p->o, p->d, Nq,
+                    (o_part ? static_cast<long long>(n_splits) : 1ll) * BH))
     return FAT_ERR_LAUNCH;
   fp.o = p->o;
   fp.lse = p->lse;

@@ -67,6 +67,7 @@ struct FwdParams {
   CUtensorMap tm_q;
   CUtensorMap tm_k;
   CUtensorMap tm_v;
+  CUtensorMap tm_o;        // fp32 O (or the split partials) as [rows, N_q, d], 32 x 128 boxes
   float* o;
   float* lse;
   int* fallback_rows;
@@ -529,33 +530,50 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
         if (p.fallback_rows) atomicAdd(p.fallback_rows, __popc(ball));
       }
     }
-    // epilogue: O / l (this set's half of the columns) and LSE
+    // epilogue: O / l, this set's half of the columns, staged in shared
+    // memory (the K ring, idle now) as 128-byte-swizzled boxes of 32 columns
+    // x 128 rows for the TMA store below
     const float inv_l = l_full > 0.f ? p.v_scale / l_full : 0.f;  // an empty row gets O = 0
-    const size_t out_row = (static_cast<size_t>(split) * (p.B * p.H) + bh) * p.Nq + row_g;
-    float* orow = (p.o_part ? p.o_part : p.o) + out_row * D + set * kHalfD;
 #pragma unroll
     for (int k = 0; k < kHalfD / 32; ++k) {
       uint32_t ov[32];
       tmem_ld32(o_taddr + set * kHalfD + 32 * k, ov);
       tmem_wait_ld(ov);
-      if (row_g < p.Nq) {
+      const uint32_t box = sb + L::kK + (set * (kHalfD / 32) + k) * 16384 + r * 128;
+      if (row_g < p.Nq) {  // (rows past N_q are clipped by the store anyway)
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 v4 =
-              make_float4(__uint_as_float(ov[i]) * inv_l, __uint_as_float(ov[i + 1]) * inv_l,
-                          __uint_as_float(ov[i + 2]) * inv_l, __uint_as_float(ov[i + 3]) * inv_l);
-          *reinterpret_cast<float4*>(orow + 32 * k + i) = v4;
-        }
+        for (int cc = 0; cc < 8; ++cc)
+          st_shared_v4(box + ((cc ^ (r & 7)) << 4), __uint_as_float(ov[4 * cc]) * inv_l,
+                       __uint_as_float(ov[4 * cc + 1]) * inv_l,
+                       __uint_as_float(ov[4 * cc + 2]) * inv_l,
+                       __uint_as_float(ov[4 * cc + 3]) * inv_l);
       }
     }
-    if (r == 0 && set == 0 && pass == 0 && p.trace != nullptr && blockIdx.x == 0)
-      p.trace[kTraceWords - 1] = static_cast<unsigned long long>(clock64());
+    fence_async_shared();
     if (row_g < p.Nq && set == 0) {
+      const size_t out_row = (static_cast<size_t>(split) * (p.B * p.H) + bh) * p.Nq + row_g;
       const float lsum = kLTensor ? l_full + delta_full : l_full;
       (p.lse_part ? p.lse_part : p.lse)[out_row] =
           l_full > 0.f ? (M_fin - kKappa + __log2f(lsum)) * kLn2 : -INFINITY;
     }
   }
+  // One thread of the set stores its boxes once all four warps have staged
+  // their rows (rows past N_q are clipped by the tensor map) and waits until
+  // the copy has read shared memory, which a second pass would reuse.  Every
+  // warp of the set joins this barrier; a warp that gave up vetoes the store.
+  const bool veto = named_bar_or(kBarSet + set, 128, !ok);
+  if (!veto && q == 0 && lane == 0) {
+    const int row_block = p.o_part ? split * (p.B * p.H) + bh : bh;
+#pragma unroll
+    for (int k = 0; k < kHalfD / 32; ++k) {
+      const int b = set * (kHalfD / 32) + k;
+      tma_store_3d(&p.tm_o, sb + L::kK + b * 16384, b * 32, m0, row_block);
+    }
+    bulk_commit();
+    bulk_wait_read();
+  }
+  if (r == 0 && set == 0 && pass == 0 && p.trace != nullptr && blockIdx.x == 0)
+    p.trace[kTraceWords - 1] = static_cast<unsigned long long>(clock64());
   tc_fence_before();
 }
 
