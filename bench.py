@@ -276,7 +276,8 @@ def config_dict(w, variant, l2="flushed before every timed step (256 MiB write)"
             "X": w.X, "dtype": w.dtype, "variant": variant, "l2": l2}
 
 
-def time_variant(fat, torch, w, dev, args, variant, flush, stream, l_mode="vector"):
+def time_variant(fat, torch, w, dev, args, variant, flush, stream, l_mode="vector",
+                 z_mode="vector"):
     """Device time (ms) of each of args.steps launches, L2 flushed before each."""
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
@@ -289,7 +290,7 @@ def time_variant(fat, torch, w, dev, args, variant, flush, stream, l_mode="vecto
                              dev["v_descale"], w.causal, w.scale, w.X, out=out, stream=stream)
         else:
             fat.attn_fwd(dev["q"], dev["k"], dev["v"], w.causal, w.scale, w.X, variant=variant,
-                         out=out, stream=stream, l_mode=l_mode)
+                         out=out, stream=stream, l_mode=l_mode, z_mode=z_mode)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -485,8 +486,8 @@ def main():
     stream = torch.cuda.Stream(device)
     peaks = load_peaks()
 
-    def timed(variant, sample_clocks, l_mode="vector"):
-        gen_ = time_variant(fat, torch, w, dev, args, variant, flush, stream, l_mode)
+    def timed(variant, sample_clocks, l_mode="vector", z_mode="vector"):
+        gen_ = time_variant(fat, torch, w, dev, args, variant, flush, stream, l_mode, z_mode)
         next(gen_)  # warm-up done
         if pg:
             pg.barrier()
@@ -521,6 +522,18 @@ def main():
                     "tensor_speedup_vs_vec": v_avg / avg_ms,
                     "tensor_lsum_value": w.flops / (l_avg * 1e-3) / 1e12,
                     "tensor_lsum_ms_per_step": l_avg}
+        if w.X == 128:
+            # the subtraction of Z on the tensor pipe, alone and together with
+            # the tensor row sum (the pages' "AllTensor" arm); FLOPs counted
+            # as for the other arms (the extra bias K step is not counted)
+            zt, _, _ = timed("tensor", False, "vector", "tensor")
+            at, _, _ = timed("tensor", False, "tensor", "tensor")
+            z_avg = sum(zt) / len(zt)
+            a_avg = sum(at) / len(at)
+            ablation.update({"tensor_zmma_value": w.flops / (z_avg * 1e-3) / 1e12,
+                             "tensor_zmma_ms_per_step": z_avg,
+                             "alltensor_value": w.flops / (a_avg * 1e-3) / 1e12,
+                             "alltensor_ms_per_step": a_avg})
 
     # end to end through the public API with host buffers: H2D of q, k, v from
     # pinned memory, the call, D2H of o and lse, every step

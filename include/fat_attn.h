@@ -72,19 +72,35 @@ typedef enum { FAT_DTYPE_BF16 = 0, FAT_DTYPE_E4M3 = 1, FAT_DTYPE_FP16 = 2 } fat_
 typedef enum { FAT_LMODE_VECTOR = 0, FAT_LMODE_TENSOR = 1 } fat_lmode;
 
 /*
+ * Where the subtraction of Algorithm 1 steps 4-5 (Z = log2(e) * scale * S -
+ * m_hat) happens in the tensorized variant.  FAT_ZMODE_VECTOR (default): one
+ * packed FMA per pair of scores on the vector units.  FAT_ZMODE_TENSOR (the
+ * tensor-pipe half of the "AllTensor" variant of the page's ablation, Fig. 10):
+ * S = Q K^T gets one more 16-deep K step, a bias tile against a tile of ones,
+ * so the MMA itself writes S + b with b = -m_ref / (log2(e) * scale) rounded
+ * to bf16, m_ref being the surrogate maximum settled three K/V tiles earlier
+ * (the latest one known when that S is queued).  The multiply by
+ * log2(e) * scale and the remaining offset log2(e) * scale * b + m_hat stay
+ * one packed FMA per pair, so no vector instruction is saved, and the MMA does 1/8 (d = 128)
+ * or 1/4 (d = 64) more work on S.  Requires the tensorized variant, X = 128
+ * and bf16 inputs; anything else returns FAT_ERR_UNSUPPORTED.
+ */
+typedef enum { FAT_ZMODE_VECTOR = 0, FAT_ZMODE_TENSOR = 1 } fat_zmode;
+
+/*
  * Tensorized online softmax (section A2 of the page above).
  *   - m_hat: per X-row tile, the maximum of the row maxima seen so far
  *     (Algorithm 1 step 1), kept as an integer number of binades so that the
  *     rescale factor exp(m_hat_old - m_hat) of steps 2-3 is an exact power of
  *     two shared by the tile;
  *   - Z = log2(e) * scale * S - m_hat, P~ = exp2(Z) (steps 4-6);
- *   - with X = 128 the factor 2^-k is applied by the tensor pipe inside the
- *     next O += P~ V (the MMA's input-scaling operand); otherwise O is
- *     rescaled in tensor memory by the vector units, and only when m_hat grew;
+ *   - O is rescaled in tensor memory by the vector units, once per tile and
+ *     only when m_hat grew (for X = 128 one factor for the whole tile);
  *   - the row sum l of step 7 is an fp32 sum on the vector units (see
  *     fat_lmode for the tensor-pipe alternative);
  *   - rows whose surrogate maximum exceeds their exact maximum by more than
- *     the underflow threshold (default 64 binades for bf16 P~, 14 for e4m3),
+ *     the underflow threshold (default 64 binades for bf16 P~, 29 for fp16,
+ *     14 for e4m3),
  *     or whose sum is zero, are detected; their 128-row block is recomputed
  *     with one-row tiles (X = 1: each row's own maximum rounded up to a whole
  *     binade, so no row can underflow) -- the optional fallback of the
@@ -192,6 +208,7 @@ typedef struct fat_params {
    * stamps of the first thread block's pipeline phases, for measuring how
    * long the tensor pipe waits for the softmax (see fat_trace_layout below) */
   unsigned long long* trace;
+  int z_mode;                         /* fat_zmode (tensorized variant only) */
 } fat_params;
 
 /*

@@ -140,6 +140,11 @@ int run_fwd(const fat_params* p, int Nq, int Nk, int splits, void* workspace,
   if (p->dtype != FAT_DTYPE_BF16 && p->dtype != FAT_DTYPE_E4M3 && p->dtype != FAT_DTYPE_FP16)
     return FAT_ERR_INVALID_ARG;
   if (p->l_mode != FAT_LMODE_VECTOR && p->l_mode != FAT_LMODE_TENSOR) return FAT_ERR_INVALID_ARG;
+  if (p->z_mode != FAT_ZMODE_VECTOR && p->z_mode != FAT_ZMODE_TENSOR) return FAT_ERR_INVALID_ARG;
+  const bool z_tensor = p->z_mode == FAT_ZMODE_TENSOR;
+  if (z_tensor &&
+      (p->variant != FAT_VARIANT_TENSOR || p->X != 128 || p->dtype != FAT_DTYPE_BF16))
+    return FAT_ERR_UNSUPPORTED;
   if (splits < 1 || splits > kMaxSplits) return FAT_ERR_INVALID_ARG;
   const long long BH = static_cast<long long>(p->B) * p->H;
   const long long n_mblocks = (Nq + fat::kRowsPerCta - 1) / fat::kRowsPerCta;
@@ -220,7 +225,10 @@ int run_fwd(const fat_params* p, int Nq, int Nk, int splits, void* workspace,
   const bool l_tensor = tensor && p->l_mode == FAT_LMODE_TENSOR;
   const int X = tensor ? p->X : 0;  // X = 0: the vector-softmax kernel
   int st;
-  if (e4m3)
+  if (z_tensor)
+    st = p->d == 128 ? fat::dispatch_bf16_zt_d128(fp, l_tensor, dev, grid, n_splits, p->stream)
+                     : fat::dispatch_bf16_zt_d64(fp, l_tensor, dev, grid, n_splits, p->stream);
+  else if (e4m3)
     st = l_tensor ? fat::dispatch_e4m3_d128_ltensor(fp, X, dev, grid, n_splits, p->stream)
                   : fat::dispatch_e4m3_d128_lvec(fp, X, dev, grid, n_splits, p->stream);
   else if (f16 && p->d == 128)

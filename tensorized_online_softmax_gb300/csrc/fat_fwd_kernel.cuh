@@ -104,7 +104,7 @@ __device__ __forceinline__ void trace_mark(const FwdParams& p, int e, int t, int
     p.trace[(e * 2 + t) * kTraceIters + j] = static_cast<unsigned long long>(clock64());
 }
 
-template <int D, bool kE4M3 = false>
+template <int D, bool kE4M3 = false, bool kZT = false>
 struct Smem {
   static constexpr int kElt = kE4M3 ? 1 : 2;          // bytes per input element
   static constexpr int kTile = kBlockM * D * kElt;    // bytes of one 128 x D tile
@@ -121,7 +121,12 @@ struct Smem {
   static constexpr int kK = kTile;                     // K ring
   static constexpr int kV = kK + kKStages * kTile;     // V ring
   static constexpr int kOnes = kV + kVStages * kTile;  // 16 rows x 128 B of ones (2 KB)
-  static constexpr int kBars = kOnes + 2048;
+  // Z on the tensor pipe (kZT): per score buffer a 128 x 16 bf16 bias tile
+  // (the A of one more K step of S = Q K^T) and one 128 x 16 tile of ones
+  // (its B); K-major without swizzle, 4 KB each
+  static constexpr int kZBias = kOnes + 2048;
+  static constexpr int kZOnes = kZBias + 3 * 4096;
+  static constexpr int kBars = kZT ? kZOnes + 4096 : kOnes + 2048;
   // barrier slots
   static constexpr int bQFull = 0;
   static constexpr int bKFull = 1;
@@ -142,7 +147,8 @@ struct Smem {
   static constexpr int kRed = (kBars + 8 * kNumBars + 15) & ~15;  // float [2 sets][2 parity][4 warps]
   static constexpr int kMRow = kRed + 64;            // float [2 sets][128 rows]: offsets
   static constexpr int kFin = kMRow + 1024;          // float [4][2 sets][128 rows]
-  // u32: tmem base, abort, redo, -, PV scale of each score buffer [3]
+  // u32: tmem base, abort, redo, -, then (kZT) as floats the bias held by
+  // each score buffer's bias tile [3]
   static constexpr int kMisc = kFin + 4096;
   static constexpr int kBytes = kMisc + 64;
   static constexpr int kAlloc = kBytes + 1024;       // slack for 1024-byte alignment
@@ -198,14 +204,14 @@ __device__ __forceinline__ float f16_round(float x) { return __half2float(__floa
 //            maximum instead, rounded up to a whole binade.
 //   kX == 0  the vector-softmax ablation: exact per-row maximum.
 // ---------------------------------------------------------------------------
-template <int D, int kX, bool kLTensor, int kDt>
+template <int D, int kX, bool kLTensor, int kDt, bool kZT>
 __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, uint32_t sb,
                                              uint32_t tmem, volatile uint32_t* misc, int warp,
                                              int lane, int m0, int bh, int n_kv, int it0,
                                              int pass, bool exact, int split, int kv_begin,
                                              int kv_end, int kv_off) {
   constexpr bool kE4M3 = kDt == kDtE4M3;
-  using L = Smem<D, kE4M3>;
+  using L = Smem<D, kE4M3, kZT>;
   constexpr bool kTensor = kX > 0;
   // e4m3 (fp16) P~ is formed as 2^(Z + kKappa) <= 2^8 < 448 (2^15 < 65504)
   // so that its terms use the format's range; the factor cancels in O / l and
@@ -225,6 +231,8 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
   float* red = reinterpret_cast<float*>(smem + L::kRed);    // [2 sets][2 parity][4 warps]
   float* mrow = reinterpret_cast<float*>(smem + L::kMRow);  // [2 sets][128 rows]
   float* fin = reinterpret_cast<float*>(smem + L::kFin);    // [4][2 sets][128 rows]
+  // (kZT) the bias b held by each score buffer's bias tile, in raw score units
+  volatile float* zvals = reinterpret_cast<volatile float*>(misc + 4);
   // Warps of the set that share a surrogate maximum: none besides this one
   // for X <= 32, the fallback pass and the vector variant; two for X = 64,
   // the set's four for X = 128.
@@ -316,8 +324,11 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
         mx[a] = fmaxf(mx[a], __uint_as_float(s[k][b + 15]));
       }
       rowmax = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7])));
-      m_row = fmaxf(m_row, rowmax);
+      if constexpr (!kZT) m_row = fmaxf(m_row, rowmax);
     }
+    // (kZT: these are maxima of S + b; b is taken off below, once known)
+    const float rowmax_raw = rowmax;
+    float zb = 0.f;  // (kZT) the bias in this tile's scores
     // Algorithm 1 step 1: maximum of the row maxima over the X-row tile: this
     // warp's part (its 32 rows, or 16-row groups for X = 16) ...
     float tmax = rowmax;
@@ -357,6 +368,14 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       // once the running maximum has settled; only then are the warps'
       // maxima exchanged.  A warp that gave up votes yes and posts NaN.
       M_prev = prev_offset(j);
+      if constexpr (kZT) {
+        // written three tiles ago by the other set, before it published the
+        // offset just read (or zero from the start of the pass)
+        zb = zvals[buf];
+        rowmax -= zb;
+        tmax -= zb;
+        m_row = fmaxf(m_row, rowmax);
+      }
       const float Mc = (tmax == -INFINITY) ? -INFINITY : ceilf(tmax * c);
       const bool any = named_bar_or(gbar_id, gbar_n, dead || Mc > M_prev);
       M_new = M_prev;
@@ -368,10 +387,16 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     } else {
       // X <= 32 within the warp; the fallback pass and the vector variant
       // each row's own maximum (the fallback pass rounded up to a binade)
-      const float gm = (exact || !kTensor) ? rowmax : tmax;
       if (dead) break;
       M_prev = prev_offset(j);
       if (dead) break;
+      if constexpr (kZT) {  // (the fallback pass: the bias tiles hold zero)
+        zb = zvals[buf];
+        rowmax -= zb;
+        tmax -= zb;
+        m_row = fmaxf(m_row, rowmax);
+      }
+      const float gm = (exact || !kTensor) ? rowmax : tmax;
       if constexpr (kTensor) {
         M_new = fmaxf(M_prev, (gm == -INFINITY) ? -INFINITY : ceilf(gm * c));
       } else {
@@ -379,6 +404,24 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
       }
     }
     publish_offset(M_new);
+    if constexpr (kZT) {
+      // The bias of S_{j+3}, which the MMA issuer queues into this score
+      // buffer once P~_j is published: -M_new in raw score units, as bf16
+      // (zero in the fallback pass).  The tile is rewritten only when the
+      // value changes; the set's four warps read the old value before the
+      // group barrier above.
+      const float bz = (!solo && M_new != -INFINITY)
+                           ? __bfloat162float(__float2bfloat16_rn(-M_new / c))
+                           : 0.f;
+      if (bz != zb) {
+        const uint32_t w = pack_bf16x2(bz * 0.0625f, bz * 0.0625f);  // 16 equal terms make b
+        const uint32_t dst = sb + L::kZBias + buf * 4096 + r * 32;
+        st_shared_v4u(dst, w, w, w, w);
+        st_shared_v4u(dst + 16, w, w, w, w);
+        fence_async_shared();
+        if (q == 0 && lane == 0) zvals[buf] = bz;
+      }
+    }
     if (q == 0 && lane == 0) trace_mark(p, 1, set, j, pass);
     const float neg_E = (M_new == -INFINITY) ? 0.f : -M_new;
     // step 7 on the tensor pipe: the row sum of this set's previous tile
@@ -390,7 +433,9 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     }
 
     // steps 4-6: Z = c S - m_hat, P~ = exp2(Z), stored as bf16 (e4m3) over S
-    const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(neg_E + kKappa, neg_E + kKappa);
+    // (kZT: c (S + b) - (c b + m_hat))
+    const float nm = (kZT ? fmaf(-c, zb, neg_E) : neg_E) + kKappa;
+    const uint64_t c2 = f2_pack(c, c), nm2 = f2_pack(nm, nm);
     uint64_t acc2[2] = {f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
@@ -469,7 +514,8 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     if constexpr (kLTensor) {
       rs_pending = it;
       if (rowmax != -INFINITY) {
-        const float pm = ex2_approx(fmaf(rowmax, c, kKappa - M_new));
+        // the dominant term exactly as the exponentials above formed it
+        const float pm = ex2_approx(fmaf(rowmax_raw, c, nm));
         delta += pm - (kE4M3 ? e4m3_round(pm) : (kDt == kDtF16 ? f16_round(pm) : bf16_round(pm)));
       }
     } else {
@@ -572,6 +618,15 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     bulk_commit();
     bulk_wait_read();
   }
+  if (kZT && pass == 0) {
+    // the fallback pass (if any) starts from zero bias tiles; every S MMA of
+    // this pass has completed (O final was signalled after the last one)
+    const int t = warp * 32 + lane;
+    for (int i = t; i < 3 * 4096 / 16; i += kSoftmaxWarps * 32)
+      st_shared_v4u(sb + L::kZBias + 16 * i, 0u, 0u, 0u, 0u);
+    if (t < kSBufs) zvals[t] = 0.f;
+    fence_async_shared();
+  }
   if (r == 0 && set == 0 && pass == 0 && p.trace != nullptr && blockIdx.x == 0)
     p.trace[kTraceWords - 1] = static_cast<unsigned long long>(clock64());
   tc_fence_before();
@@ -587,10 +642,17 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
 //           unrounded P~ on the vector units.
 // kDt:      input type: kDtBf16 (kind::f16 MMAs, bf16 P~), kDtF16 (kind::f16,
 //           fp16 P~) or kDtE4M3 (kind::f8f6f4, e4m3 P~).
-template <int D, int kX, bool kLTensor, int kDt>
+// kZT:      (bf16, X = 128 only) the subtraction of Algorithm 1 steps 4-5 on
+//           the tensor pipe: S = Q K^T gets one more 16-deep K step, a bias
+//           tile (every entry b / 16, b = -m_ref / (log2(e) scale) rounded to
+//           bf16) against a tile of ones, so the MMA writes S + b; m_ref is
+//           the surrogate maximum settled three tiles earlier (the latest one
+//           known when S is queued), and the vector side folds in the rest.
+template <int D, int kX, bool kLTensor, int kDt, bool kZT = false>
 __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_constant__ FwdParams p) {
+  static_assert(!kZT || (kX == 128 && kDt == kDtBf16), "Z on the tensor pipe: bf16, X = 128");
   constexpr bool kE4M3 = kDt == kDtE4M3;
-  using L = Smem<D, kE4M3>;
+  using L = Smem<D, kE4M3, kZT>;
   constexpr int SK = L::kKStages;
   constexpr int SV = L::kVStages;
   constexpr bool kTensor = kX > 0;
@@ -656,6 +718,16 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
     misc[1] = 0;
     misc[2] = 0;
     fence_mbar_init();
+  }
+  if constexpr (kZT) {
+    // zero bias tiles (12 KB, a bias of 0 for the first three S tiles) and the
+    // ones tile (4 KB of bf16 1.0) right after them
+    for (int i = threadIdx.x; i < 1024; i += kNumThreads) {
+      const uint32_t w = i >= 768 ? 0x3F803F80u : 0u;
+      st_shared_v4u(sb + L::kZBias + 16 * i, w, w, w, w);
+    }
+    if (threadIdx.x < 3) reinterpret_cast<volatile float*>(misc + 4)[threadIdx.x] = 0.f;
+    fence_async_shared();
   }
   if (threadIdx.x < 256) {  // the ones tile used as B of the row-sum MMA
     // 1.0 in bf16 (0x3F80), fp16 (0x3C00) or e4m3 (0x38)
@@ -738,6 +810,11 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
           const uint64_t q_desc = sdesc_sw128(sb + L::kQ, 16, 1024);
           const uint64_t k_desc = sdesc_sw128(sb + L::kK, 16, 1024);
           const uint64_t v_desc = sdesc_sw128(sb + L::kV, 16384, 1024);
+          // (kZT) bias and ones tiles: 16-byte core matrices 128 B apart along
+          // K, 8-row groups 256 B apart; every entry of a tile is equal, so
+          // only the tile's 4 KB extent matters
+          const uint64_t zbias_desc = sdesc_plain(sb + L::kZBias, 128, 256);
+          const uint64_t zones_desc = sdesc_plain(sb + L::kZOnes, 128, 256);
           auto issue_s = [&](int it) {
             const uint64_t kd = k_desc + static_cast<uint32_t>(((it % SK) * L::kTile) >> 4);
             const uint32_t d_t = tmem + (it % kSBufs) * kBlockN;
@@ -747,6 +824,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
               const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
               mma_ss<kE4M3>(d_t, q_desc + off, kd + off, idesc_s, kk > 0);
             }
+            if constexpr (kZT)
+              mma_ss<false>(d_t, zbias_desc + static_cast<uint32_t>(((it % kSBufs) * 4096) >> 4),
+                            zones_desc, idesc_s, 1u);
           };
           // TMEM column of the A operand (P~) of K step g: 8 columns per step
           auto p_col = [&](int buf, int g) -> uint32_t { return tmem + buf * kBlockN + g * 8; };
@@ -831,7 +911,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
       // tiles, X = 1: every row's own maximum rounded up to a whole binade,
       // so no row can underflow (the vector fallback of the page's
       // all-underflow discussion, on the same code path).
-      softmax_role<D, kX, kLTensor, kDt>(p, smem, sb, tmem, misc, warp, lane, m0, bh, n_kv, it0,
+      softmax_role<D, kX, kLTensor, kDt, kZT>(p, smem, sb, tmem, misc, warp, lane, m0, bh, n_kv, it0,
                                            pass, /*exact=*/pass == 1, split, kv_begin, kv_end,
                                            kv_off);
       __syncthreads();

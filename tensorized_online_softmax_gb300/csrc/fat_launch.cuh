@@ -12,11 +12,11 @@ namespace fat {
 constexpr int kMaxDevices = 64;
 
 // Returns 0 or the fat_status code FAT_ERR_LAUNCH (-4).
-template <int D, int kX, bool kLTensor, int kDt>
+template <int D, int kX, bool kLTensor, int kDt, bool kZT = false>
 int launch_fwd(const FwdParams& fp, int dev, int grid, int splits, cudaStream_t stream) {
   static int ready[kMaxDevices];  // per device: attributes checked and set
-  auto kern = fat_fwd_kernel<D, kX, kLTensor, kDt>;
-  const int smem = Smem<D, kDt == kDtE4M3>::kAlloc;
+  auto kern = fat_fwd_kernel<D, kX, kLTensor, kDt, kZT>;
+  const int smem = Smem<D, kDt == kDtE4M3, kZT>::kAlloc;
   if (!ready[dev]) {
     // The warpgroup register split inside the kernel assumes exactly
     // kLaunchRegs registers per thread at launch; anything else could make
@@ -51,6 +51,13 @@ FAT_DECLARE_DISPATCH(dispatch_f16_d128_ltensor)
 FAT_DECLARE_DISPATCH(dispatch_f16_d64_lvec)
 FAT_DECLARE_DISPATCH(dispatch_f16_d64_ltensor)
 #undef FAT_DECLARE_DISPATCH
+
+// Z on the tensor pipe (bf16, X = 128): d in {64, 128}, either row-sum mode.
+// Returns -1 for a d without an instance.
+int dispatch_bf16_zt_d128(const FwdParams& fp, bool l_tensor, int dev, int grid, int splits,
+                          cudaStream_t stream);
+int dispatch_bf16_zt_d64(const FwdParams& fp, bool l_tensor, int dev, int grid, int splits,
+                         cudaStream_t stream);
 
 #define FAT_DEFINE_DISPATCH(name, D, LT, DT)                                  \
   int name(const FwdParams& fp, int X, int dev, int grid, int splits, cudaStream_t stream) { \

@@ -80,6 +80,23 @@ def test_ex_validation(lib):
     assert lib.fat_attn_fwd_ex(ctypes.byref(p)) == fat.FAT_ERR_INVALID_ARG
 
 
+def test_z_mode_validation(lib):
+    """Z on the tensor pipe exists for the tensorized variant, X = 128 and
+    bf16 inputs only; other requests are refused before any device call."""
+    base = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000, B=1, H=1, N=128, d=128,
+                causal=0, scale=0.125, X=128, variant=0, dtype=0)
+    for kw, want in [(dict(z_mode=2), fat.FAT_ERR_INVALID_ARG),
+                     (dict(z_mode=-1), fat.FAT_ERR_INVALID_ARG),
+                     (dict(z_mode=1, X=64), fat.FAT_ERR_UNSUPPORTED),
+                     (dict(z_mode=1, X=16), fat.FAT_ERR_UNSUPPORTED),
+                     (dict(z_mode=1, variant=1), fat.FAT_ERR_UNSUPPORTED),
+                     (dict(z_mode=1, dtype=2), fat.FAT_ERR_UNSUPPORTED),
+                     (dict(z_mode=1, dtype=1, q_descale=1.0, k_descale=1.0, v_descale=1.0),
+                      fat.FAT_ERR_UNSUPPORTED)]:
+        p = fat.FatParams(**dict(base, **kw))
+        assert lib.fat_attn_fwd_ex(ctypes.byref(p)) == want, kw
+
+
 def test_params_struct_layout_matches_header(tmp_path):
     """ctypes mirror of fat_params has the C compiler's size and offsets."""
     cuda_inc = "/usr/local/cuda/include"

@@ -1,13 +1,11 @@
 """Parity when the running maximum grows from one K/V tile to the next.
 
-With X = 128 the kernel forms a tile's exponentials from the previous tile's
-surrogate maximum while the four warps of the tile still exchange their row
-maxima, and scales P~ by 2^(m_old - m_new) when the tile raised the maximum.
+The surrogate maximum of an X-row tile is settled before its exponentials,
+and O takes the factor 2^(m_old - m_new) on the vector side whenever it grew.
 These inputs raise every row's logits by a fixed amount per 128-key tile, so
-each K/V tile after the first takes that correction: a few binades (the
-rescale of O rides in the PV MMA), more than 15 binades (O is rescaled on the
-vector side), and more than 100 binades (the block is redone with per-row
-maxima).  A shrinking sequence (the first tile dominates) never corrects.
+each K/V tile after the first raises it: by a few binades, by 20, and by more
+than 100 (each tile's terms then leave the earlier ones far out of range).  A
+shrinking sequence (the first tile dominates) never raises it.
 """
 import math
 
