@@ -13,6 +13,9 @@ It wraps ``oracle.c`` (plain C, double precision, pthreads) through ctypes:
   Tensorized Attention by Exploiting Tensor-Vector Parallelism" (section A2,
   tensorized online softmax) with the surrogate maximum over X-row tiles.
 
+The backward pass's oracle (gradients of the same definition) is
+:mod:`oracle.backward` (numpy, float64).
+
 All arrays are float64 numpy arrays, row-major [B, H, N, d] (LSE [B, H, N]).
 ``scale`` is passed as a Python float; callers that mirror a float32 ABI
 argument pass ``float(np.float32(scale))``.
