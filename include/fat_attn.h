@@ -226,6 +226,32 @@ typedef struct fat_params {
 
 int fat_attn_fwd_ex(const fat_params* p);
 
+/*
+ * Backward pass by recomputation (the v1 recap of the FA-T blog, "从融合到
+ * 张量化：FlashAttention 演进脉络": only O and the softmax statistics are kept
+ * from the forward pass).  For O = softmax(scale Q K^T [+ causal]) V and an
+ * upstream gradient dout, writes the gradients of sum(O * dout):
+ *   P = exp(scale S - LSE), D_i = sum_d dout_id O_id,
+ *   dV = P^T dout, dS = P * (dout V^T - D), dQ = scale dS K, dK = scale dS^T Q.
+ * q, k, v, dout: bf16 [B, H, N, d]; o, lse: the fp32 outputs of a forward
+ * call on the same q, k, v (any variant: they are exact up to rounding);
+ * dq, dk, dv: fp32 [B, H, N, d], overwritten (dq is cleared on `stream`
+ * first and accumulated across key blocks with atomic adds, so its low-order
+ * bits may differ from run to run).  d is 64 or 128.  P and dS enter their
+ * MMAs as bf16, with fp32 accumulation.  workspace: device memory owned by
+ * the caller, at least fat_attn_bwd_workspace_bytes(B, H, N) bytes (D and
+ * log2(e) LSE per row); calls sharing it must not overlap on the device.
+ * q, k, v, dout, o, dq, dk, dv must be 16-byte aligned, lse 4-byte aligned.
+ * Returns a fat_status; nothing is launched when validation fails.
+ */
+int fat_attn_bwd(const void* q, const void* k, const void* v, const float* o, const float* lse,
+                 const void* dout, float* dq, float* dk, float* dv, int B, int H, int N, int d,
+                 int causal, float scale, void* workspace, size_t workspace_bytes,
+                 cudaStream_t stream);
+
+/* Workspace size for fat_attn_bwd (0 for invalid arguments). */
+size_t fat_attn_bwd_workspace_bytes(int B, int H, int N);
+
 /* Human-readable name of a fat_status value (static string). */
 const char* fat_status_string(int status);
 

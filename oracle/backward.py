@@ -104,3 +104,27 @@ def attn_bwd_sampled(q, k, v, do, causal: bool, scale: float, qrows, krows):
         ds = p * (do @ v[j] - D)
         dk[j] = scale * (ds @ q)
     return dq, dk, dv
+
+
+def attn_bwd_abs_products(q, k, v, do, causal: bool, scale: float):
+    """For each gradient element, the sum of the absolute values of the
+    products that form it: (scale |dS| |K|, scale |dS|^T |Q|, P^T |dO|) for
+    (dq, dk, dv).
+
+    A gradient formed from operands one of which carries a relative rounding
+    error of at most e per entry is within e times this sum of the exact
+    gradient (the bound the GPU parity tests apply for bf16 P and dS)."""
+    q, k, v, do = (np.asarray(a, dtype=np.float64) for a in (q, k, v, do))
+    B, H, N, d = q.shape
+    bq, bk, bv = (np.zeros_like(q) for _ in range(3))
+    for b in range(B):
+        for h in range(H):
+            p, _ = _head_probs(q[b, h], k[b, h], causal, scale)
+            o = p @ v[b, h]
+            dp = do[b, h] @ v[b, h].T
+            D = (do[b, h] * o).sum(axis=1)
+            ads = np.abs(p * (dp - D[:, None]))
+            bq[b, h] = scale * (ads @ np.abs(k[b, h]))
+            bk[b, h] = scale * (ads.T @ np.abs(q[b, h]))
+            bv[b, h] = p.T @ np.abs(do[b, h])
+    return bq, bk, bv

@@ -21,6 +21,7 @@ from . import _build
 
 __all__ = [
     "FatError", "load_library", "attn_fwd", "attn_fwd_vec", "attn_fwd_fp8", "attn_fwd_splitkv",
+    "attn_bwd",
     "check_device_error", "status_string", "ABI_SYMBOLS", "FAT_OK",
     "FAT_ERR_INVALID_ARG", "FAT_ERR_UNSUPPORTED", "FAT_ERR_ALIGNMENT", "FAT_ERR_LAUNCH",
     "FAT_ERR_DEVICE_TIMEOUT", "FAT_ERR_ARCH",
@@ -46,6 +47,7 @@ ABI_SYMBOLS = (
     "fat_attn_fwd", "fat_attn_fwd_vec", "fat_attn_fwd_fp8", "fat_attn_fwd_splitkv",
     "fat_attn_splitkv_workspace_bytes", "fat_attn_splitkv_default_splits",
     "fat_attn_fwd_splitkv_noalloc", "fat_attn_fwd_ex",
+    "fat_attn_bwd", "fat_attn_bwd_workspace_bytes",
     "fat_status_string", "fat_check_device_error",
 )
 
@@ -116,6 +118,11 @@ def load_library(build_if_missing: bool = True):
         lib.fat_attn_fwd_splitkv_noalloc.restype = I
         lib.fat_attn_fwd_ex.argtypes = [ctypes.POINTER(FatParams)]
         lib.fat_attn_fwd_ex.restype = I
+        lib.fat_attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, F, P,
+                                     ctypes.c_size_t, P]
+        lib.fat_attn_bwd.restype = I
+        lib.fat_attn_bwd_workspace_bytes.argtypes = [I, I, I]
+        lib.fat_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
         lib.fat_status_string.argtypes = [I]
         lib.fat_status_string.restype = ctypes.c_char_p
         lib.fat_check_device_error.argtypes = [P]
@@ -265,6 +272,47 @@ def attn_fwd_splitkv(q, k, v, causal: bool = False, scale: float | None = None, 
     if st != FAT_OK:
         raise FatError(st, "fat_attn_fwd_splitkv")
     return o, lse
+
+
+def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None, *,
+             workspace=None, out=None, stream=None):
+    """Backward pass: gradients of sum(O * dout) with respect to q, k, v.
+
+    ``q, k, v, dout``: contiguous bf16 CUDA tensors [B, H, N, d]; ``o, lse``:
+    the fp32 outputs of a forward call on the same inputs.  ``workspace`` (a
+    CUDA uint8 tensor) is allocated here if not given.  Returns fp32
+    ``(dq, dk, dv)``.
+    """
+    import torch
+
+    lib = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v), ("dout", dout)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be a bf16 CUDA tensor")
+        if t.dim() != 4 or not t.is_contiguous() or t.shape != q.shape:
+            raise ValueError(f"{name} must be a contiguous [B, H, N, d] tensor")
+    B, H, N, d = q.shape
+    if (o.dtype != torch.float32 or o.shape != q.shape or not o.is_contiguous() or
+            lse.dtype != torch.float32 or lse.shape != (B, H, N) or not lse.is_contiguous()):
+        raise ValueError("o must be fp32 [B, H, N, d] and lse fp32 [B, H, N]")
+    if scale is None:
+        scale = d ** -0.5
+    with torch.cuda.device(q.device):
+        nbytes = lib.fat_attn_bwd_workspace_bytes(B, H, N)
+        if workspace is None:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=q.device)
+        if out is None:
+            dq, dk, dv = (torch.empty((B, H, N, d), dtype=torch.float32, device=q.device)
+                          for _ in range(3))
+        else:
+            dq, dk, dv = out
+        st = lib.fat_attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                              lse.data_ptr(), dout.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                              dv.data_ptr(), B, H, N, d, int(bool(causal)), float(scale),
+                              workspace.data_ptr(), workspace.numel(), _stream_handle(stream))
+    if st != FAT_OK:
+        raise FatError(st, "fat_attn_bwd")
+    return dq, dk, dv
 
 
 def check_device_error(stream=None) -> int:

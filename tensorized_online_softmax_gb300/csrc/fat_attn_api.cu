@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "../../include/fat_attn.h"
+#include "fat_bwd_kernel.cuh"
 #include "fat_launch.cuh"
 
 namespace {
@@ -413,6 +414,76 @@ int fat_check_device_error(cudaStream_t stream) {
       return FAT_ERR_LAUNCH;
     return FAT_ERR_DEVICE_TIMEOUT;
   }
+  return FAT_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Backward pass
+// ---------------------------------------------------------------------------
+namespace {
+long long bwd_npad(int N) { return (static_cast<long long>(N) + 127) / 128 * 128; }
+}  // namespace
+
+extern "C" {
+
+size_t fat_attn_bwd_workspace_bytes(int B, int H, int N) {
+  if (B < 1 || H < 1 || N < 1) return 0;
+  return static_cast<size_t>(2ll * B * H * bwd_npad(N) * 4 + 256);
+}
+
+int fat_attn_bwd(const void* q, const void* k, const void* v, const float* o, const float* lse,
+                 const void* dout, float* dq, float* dk, float* dv, int B, int H, int N, int d,
+                 int causal, float scale, void* workspace, size_t workspace_bytes,
+                 cudaStream_t stream) {
+  // ---- synchronous validation: nothing is launched on failure ----
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !workspace)
+    return FAT_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1) return FAT_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FAT_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return FAT_ERR_INVALID_ARG;
+  const long long BH = static_cast<long long>(B) * H;
+  const long long npad = bwd_npad(N);
+  if (BH > (1ll << 30) || BH * (npad / 128) > 0x7fffffffll) return FAT_ERR_INVALID_ARG;
+  if (workspace_bytes < fat_attn_bwd_workspace_bytes(B, H, N)) return FAT_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) || !aligned16(o) ||
+      !aligned16(dq) || !aligned16(dk) || !aligned16(dv) ||
+      (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return FAT_ERR_ALIGNMENT;
+
+  int dev = 0;
+  const int arch = check_device(&dev);
+  if (arch != FAT_OK) return arch;
+
+  fat::BwdParams bp;
+  const int bh = static_cast<int>(BH);
+  if (!encode_qkv_map(&bp.tm_q, q, d, N, bh, 2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) ||
+      !encode_qkv_map(&bp.tm_k, k, d, N, bh, 2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) ||
+      !encode_qkv_map(&bp.tm_v, v, d, N, bh, 2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) ||
+      !encode_qkv_map(&bp.tm_do, dout, d, N, bh, 2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
+    return FAT_ERR_LAUNCH;
+  const uintptr_t base = (reinterpret_cast<uintptr_t>(workspace) + 255) & ~uintptr_t(255);
+  bp.lse2 = reinterpret_cast<const float*>(base);
+  bp.dvec = reinterpret_cast<const float*>(base) + BH * npad;
+  bp.dq = dq;
+  bp.dk = dk;
+  bp.dv = dv;
+  bp.BH = bh;
+  bp.N = N;
+  bp.Npad = static_cast<int>(npad);
+  bp.causal = causal ? 1 : 0;
+  bp.n_blocks = static_cast<int>(npad / 128);
+  bp.c = scale * fat::kLog2e;
+  bp.scale = scale;
+  bp.poll_limit = 0;
+  bp.timeout_ns = 4000000000ull;
+  bp.error_word = g_dev[dev].error_word;
+  if (cudaMemsetAsync(dq, 0, static_cast<size_t>(BH) * N * d * sizeof(float), stream) !=
+      cudaSuccess)
+    return FAT_ERR_LAUNCH;
+  const int st = fat::launch_bwd(bp, d, o, dout, lse, dev, stream);
+  if (st != 0) return st == -1 ? FAT_ERR_UNSUPPORTED : FAT_ERR_LAUNCH;
   return FAT_OK;
 }
 

@@ -1,0 +1,42 @@
+// Backward-pass launchers: the D / LSE preparation and the fused kernel for
+// d = 64 and d = 128 (see fat_bwd_kernel.cuh).
+#include <cuda_runtime.h>
+
+#include "fat_bwd_kernel.cuh"
+#include "fat_launch.cuh"
+
+namespace fat {
+
+namespace {
+template <int D>
+int launch_bwd_d(const BwdParams& bp, const float* o, const void* dout, const float* lse, int dev,
+                 cudaStream_t stream) {
+  static int ready[kMaxDevices];
+  auto kern = fat_bwd_kernel<D>;
+  const int smem = BwdSmem<D>::kAlloc;
+  if (!ready[dev]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+        cudaSuccess)
+      return -4;
+    ready[dev] = 1;
+  }
+  const long long rows = static_cast<long long>(bp.BH) * bp.Npad;
+  const int warps = 8;
+  fat_bwd_prep_kernel<D><<<static_cast<unsigned>((rows + warps - 1) / warps), warps * 32, 0,
+                           stream>>>(o, static_cast<const __nv_bfloat16*>(dout), lse,
+                                     const_cast<float*>(bp.lse2), const_cast<float*>(bp.dvec),
+                                     bp.N, bp.Npad, rows);
+  if (cudaGetLastError() != cudaSuccess) return -4;
+  kern<<<bp.BH * bp.n_blocks, kBwdThreads, smem, stream>>>(bp);
+  return cudaGetLastError() == cudaSuccess ? 0 : -4;
+}
+}  // namespace
+
+int launch_bwd(const BwdParams& bp, int d, const float* o, const void* dout, const float* lse,
+               int dev, cudaStream_t stream) {
+  if (d == 128) return launch_bwd_d<128>(bp, o, dout, lse, dev, stream);
+  if (d == 64) return launch_bwd_d<64>(bp, o, dout, lse, dev, stream);
+  return -1;
+}
+
+}  // namespace fat

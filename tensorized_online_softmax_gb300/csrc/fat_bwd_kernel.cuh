@@ -1,0 +1,357 @@
+// Fused attention backward pass for sm_103a: recomputes the attention
+// weights from Q, K and the forward's LSE (the backward pass by
+// recomputation that the v1 recap of "FlashAttention-T 完全张量化内核与内存布局
+// 优化深度剖析" describes: only O and the softmax statistics are kept) and
+// forms dQ, dK, dV with five tcgen05 MMAs per 128 x 128 tile:
+//
+//   S^T  = K Q^T           (TMEM)       P^T  = exp2(c S^T - log2(e) LSE)
+//   dP^T = V dO^T          (TMEM)       dS^T = scale P^T * (dP^T - D)
+//   dV  += P^T dO          (A = P^T from TMEM, bf16)
+//   dK  += dS^T Q          (A = dS^T from shared memory, K-major)
+//   dQ   = dS K            (A = the same tile read MN-major), added to
+//                           global dQ with vector atomics
+//
+// with D_i = sum_d dO_id O_id formed beforehand (fat_bwd_prep_kernel).
+// One CTA per 128-key block of one (b, h); it walks the query blocks that
+// see those keys (all of them, or those at or after the diagonal when
+// causal).  Warps: 0-3 form P^T and dS^T (one key row per thread), 4-7 move
+// each dQ partial from TMEM to global memory, 8 issues the MMAs, 9 loads
+// K and V once and Q, dO per query block with TMA.
+#pragma once
+
+#include "fat_fwd_kernel.cuh"
+
+namespace fat {
+
+struct BwdParams {
+  CUtensorMap tm_q;   // bf16 [B*H, N, d], boxes of 64 columns x 128 rows, 128-byte swizzle
+  CUtensorMap tm_k;
+  CUtensorMap tm_v;
+  CUtensorMap tm_do;
+  const float* lse2;  // [B*H][Npad] log2(e) * LSE; +inf for rows >= N
+  const float* dvec;  // [B*H][Npad] D; 0 for rows >= N
+  float* dq;          // fp32 [B*H, N, d], zero on entry, accumulated atomically
+  float* dk;          // fp32 [B*H, N, d]
+  float* dv;          // fp32 [B*H, N, d]
+  int BH, N, Npad, causal, n_blocks;
+  float c;            // log2(e) * scale
+  float scale;
+  unsigned long long poll_limit;
+  unsigned long long timeout_ns;
+  unsigned int* error_word;
+};
+
+constexpr int kBwdThreads = 320;
+constexpr int kBwdMmaWarp = 8;
+constexpr int kBwdLoadWarp = 9;
+// TMEM columns: S^T / P^T and then the dQ partial; dP^T; dV; dK
+constexpr int kBwdColS = 0;
+constexpr int kBwdColDP = 128;
+constexpr int kBwdColDV = 256;
+
+template <int D>
+struct BwdSmem {
+  static constexpr int kTile = 128 * D * 2;  // one 128 x D bf16 tile
+  static constexpr int kK = 0;
+  static constexpr int kV = kTile;
+  static constexpr int kQ = 2 * kTile;
+  static constexpr int kDO = 3 * kTile;
+  static constexpr int kDS = 4 * kTile;      // dS^T: 128 keys x 128 queries bf16 (32 KB)
+  static constexpr int kBars = kDS + 32768;
+  static constexpr int bKV = 0, bQFull = 1, bQFree = 2, bSFull = 3, bPReady = 4, bDQFull = 5,
+                       bDQFree = 6, bFinal = 7, bDrain = 8, kNumBars = 9;
+  static constexpr int kMisc = kBars + 8 * kNumBars;  // u32: tmem base, abort
+  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kAlloc = kBytes + 1024;
+  static_assert(kAlloc <= 227 * 1024, "shared memory budget");
+};
+
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_constant__ BwdParams p) {
+  using L = BwdSmem<D>;
+  constexpr int kAtoms = D / 64;  // 128-byte column slabs of a tile
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + L::kMisc);
+  volatile uint32_t* abort_flag = misc + 1;
+  auto bar = [&](int i) -> uint32_t { return sb + L::kBars + 8 * i; };
+
+  // work item: key block jb of head bh (causal: the first key blocks see the
+  // most query blocks, so they come first)
+  const int jb = static_cast<int>(blockIdx.x) / p.BH;
+  const int bh = static_cast<int>(blockIdx.x) % p.BH;
+  const int ib0 = p.causal ? jb : 0;
+  const int n_q = p.n_blocks - ib0;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar(L::bKV), 1);
+    mbar_init(bar(L::bQFull), 1);
+    mbar_init(bar(L::bQFree), 1);
+    mbar_init(bar(L::bSFull), 1);
+    mbar_init(bar(L::bPReady), 4);
+    mbar_init(bar(L::bDQFull), 1);
+    mbar_init(bar(L::bDQFree), 4);
+    mbar_init(bar(L::bFinal), 1);
+    mbar_init(bar(L::bDrain), 1);
+    misc[1] = 0;
+    fence_mbar_init();
+  }
+  if (warp == kBwdMmaWarp) {
+    tmem_alloc(sb + L::kMisc, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+
+  if (warp == kBwdLoadWarp) {
+    // =================== TMA producer ===================
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_do);
+      mbar_arrive_expect_tx(bar(L::bKV), 2 * L::kTile);
+      for (int a = 0; a < kAtoms; ++a) {
+        tma_load_3d(sb + L::kK + a * 16384, &p.tm_k, bar(L::bKV), a * 64, jb * 128, bh);
+        tma_load_3d(sb + L::kV + a * 16384, &p.tm_v, bar(L::bKV), a * 64, jb * 128, bh);
+      }
+      int issued = 0;
+      for (int t = 0; t < n_q; ++t) {
+        if (t > 0 && !wait_bounded(bar(L::bQFree), (t - 1) & 1, p, abort_flag)) break;
+        const int ib = ib0 + t;
+        mbar_arrive_expect_tx(bar(L::bQFull), 2 * L::kTile);
+        for (int a = 0; a < kAtoms; ++a) {
+          tma_load_3d(sb + L::kQ + a * 16384, &p.tm_q, bar(L::bQFull), a * 64, ib * 128, bh);
+          tma_load_3d(sb + L::kDO + a * 16384, &p.tm_do, bar(L::bQFull), a * 64, ib * 128, bh);
+        }
+        issued = t + 1;
+      }
+      if (*abort_flag) {
+        // let the copies already issued land before the CTA can exit
+        wait_drain(bar(L::bKV), 0);
+        if (issued > 0) wait_drain(bar(L::bQFull), (issued - 1) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == kBwdMmaWarp) {
+    // =================== MMA issuer (whole warp, elected lane) ===================
+    constexpr uint32_t idesc_sq = idesc_f32acc<1u>(128, 128, false);       // K-major A, B
+    constexpr uint32_t idesc_b_mn = idesc_f32acc<1u>(128, D, true);        // B MN-major
+    constexpr uint32_t idesc_ab_mn = idesc_f32acc<1u>(128, D, true, true); // A, B MN-major
+    const uint64_t k_kmaj = sdesc_sw128(sb + L::kK, 16, 1024);
+    const uint64_t v_kmaj = sdesc_sw128(sb + L::kV, 16, 1024);
+    const uint64_t q_kmaj = sdesc_sw128(sb + L::kQ, 16, 1024);
+    const uint64_t do_kmaj = sdesc_sw128(sb + L::kDO, 16, 1024);
+    const uint64_t ds_kmaj = sdesc_sw128(sb + L::kDS, 16, 1024);
+    const uint64_t q_mn = sdesc_sw128(sb + L::kQ, 16384, 1024);
+    const uint64_t do_mn = sdesc_sw128(sb + L::kDO, 16384, 1024);
+    const uint64_t k_mn = sdesc_sw128(sb + L::kK, 16384, 1024);
+    const uint64_t ds_mn = sdesc_sw128(sb + L::kDS, 16384, 1024);
+    // K step kk (16 elements) of a K-major operand: 128-byte slab kk / 4,
+    // 32-byte step kk % 4 within its rows; of an MN-major one: 16 rows
+    auto kstep = [](int kk) -> uint32_t { return ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4; };
+    auto mnstep = [](int kk) -> uint32_t { return (kk * 2048) >> 4; };
+    bool ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bKV), 0, p, abort_flag));
+    for (int t = 0; ok && t < n_q; ++t) {
+      if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bQFull), t & 1, p, abort_flag))))
+        break;
+      tc_fence_after();
+      // dP^T = V dO^T (its TMEM columns were last read by the softmax warps
+      // of the previous block, before they signalled P ready)
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss<false>(tmem + kBwdColDP, v_kmaj + kstep(kk), do_kmaj + kstep(kk), idesc_sq, kk > 0);
+      // S^T = K Q^T, once the previous dQ partial has left those columns
+      if (t > 0 &&
+          !(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bDQFree), (t - 1) & 1, p, abort_flag))))
+        break;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss<false>(tmem + kBwdColS, k_kmaj + kstep(kk), q_kmaj + kstep(kk), idesc_sq, kk > 0);
+      mma_commit(bar(L::bSFull));
+      if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bPReady), t & 1, p, abort_flag))))
+        break;
+      tc_fence_after();
+      // dV += P^T dO: P^T (bf16, two per column) from TMEM, 8 columns per K step
+#pragma unroll
+      for (int g = 0; g < 8; ++g)
+        mma_ts<false>(tmem + kBwdColDV, tmem + kBwdColS + g * 8, do_mn + mnstep(g), idesc_b_mn,
+                      t > 0 || g > 0);
+      // dK += dS^T Q
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ss<false>(tmem + kBwdColDV + D, ds_kmaj + kstep(kk), q_mn + mnstep(kk), idesc_b_mn,
+                      t > 0 || kk > 0);
+      mma_commit(bar(L::bQFree));  // Q and dO are free once these have read them
+      // dQ partial = dS K into the S columns (P^T was read by the dV MMAs above)
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ss<false>(tmem + kBwdColS, ds_mn + mnstep(kk), k_mn + mnstep(kk), idesc_ab_mn, kk > 0);
+      mma_commit(bar(L::bDQFull));
+    }
+    if (ok) {
+      mma_commit(bar(L::bFinal));
+    } else {
+      mma_commit(bar(L::bDrain));
+      wait_drain(bar(L::bDrain), 0);
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // =================== P^T and dS^T (one key row per thread) ===================
+    const int r = warp * 32 + lane;
+    const int key = jb * 128 + r;
+    const bool row_ok = key < p.N;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const float c = p.c;
+    bool ok = true;
+    for (int t = 0; t < n_q; ++t) {
+      const int ib = ib0 + t;
+      if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bSFull), t & 1, p, abort_flag))))
+        break;
+      tc_fence_after();
+      const float* lse2 = p.lse2 + static_cast<size_t>(bh) * p.Npad + ib * 128;
+      const float* dvec = p.dvec + static_cast<size_t>(bh) * p.Npad + ib * 128;
+      // causal: query ib * 128 + col sees this key iff col >= lim
+      const int lim = p.causal ? key - ib * 128 : -1;
+#pragma unroll 1
+      for (int k = 0; k < 4; ++k) {
+        uint32_t s[32], dp[32];
+        tmem_ld32(tmem + lane_base + kBwdColS + 32 * k, s);
+        tmem_ld32(tmem + lane_base + kBwdColDP + 32 * k, dp);
+        float l2[32], dd[32];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 a = __ldg(reinterpret_cast<const float4*>(lse2 + 32 * k) + i);
+          const float4 b = __ldg(reinterpret_cast<const float4*>(dvec + 32 * k) + i);
+          l2[4 * i] = a.x; l2[4 * i + 1] = a.y; l2[4 * i + 2] = a.z; l2[4 * i + 3] = a.w;
+          dd[4 * i] = b.x; dd[4 * i + 1] = b.y; dd[4 * i + 2] = b.z; dd[4 * i + 3] = b.w;
+        }
+        tmem_wait_ld(s);
+        tmem_wait_ld(dp);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float pv[2], dsv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = 32 * k + i + e;
+            const bool keep = row_ok && col >= lim;
+            const float pf = keep ? ex2_approx(fmaf(__uint_as_float(s[i + e]), c, -l2[i + e])) : 0.f;
+            pv[e] = pf;
+            dsv[e] = pf * (__uint_as_float(dp[i + e]) - dd[i + e]) * p.scale;
+          }
+          pk[i / 2] = pack_bf16x2(pv[0], pv[1]);
+          dk[i / 2] = pack_bf16x2(dsv[0], dsv[1]);
+        }
+        // P^T over its own scores (bf16, columns 16 k ..), dS^T into row r of
+        // the swizzled tile: queries 32 k .. 32 k + 31 are four 16-byte chunks
+        tmem_st16(tmem + lane_base + kBwdColS + 16 * k, pk);
+        const uint32_t row = sb + L::kDS + (k >> 1) * 16384 + r * 128;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const int chunk = (k & 1) * 4 + cc;
+          st_shared_v4u(row + ((chunk ^ (r & 7)) << 4), dk[4 * cc], dk[4 * cc + 1],
+                        dk[4 * cc + 2], dk[4 * cc + 3]);
+        }
+      }
+      tmem_wait_st();
+      fence_async_shared();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::bPReady));
+    }
+    // epilogue: dV and dK rows of this block's keys
+    if (ok) ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bFinal), 0, p, abort_flag));
+    if (ok) {
+      tc_fence_after();
+      const size_t base = (static_cast<size_t>(bh) * p.N + key) * D;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        float* out = which == 0 ? p.dv : p.dk;
+#pragma unroll 1
+        for (int k = 0; k < D / 32; ++k) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + kBwdColDV + which * D + 32 * k, v);
+          tmem_wait_ld(v);
+          if (row_ok) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              st_global_v4(out + base + 32 * k + 4 * i, __uint_as_float(v[4 * i]),
+                           __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
+                           __uint_as_float(v[4 * i + 3]));
+          }
+        }
+      }
+    }
+    tc_fence_before();
+  } else {
+    // =================== dQ partials: TMEM -> global atomics ===================
+    const int qw = warp & 3;  // TMEM lanes 32 qw .. (query rows of the block)
+    const uint32_t lane_base = static_cast<uint32_t>(qw * 32) << 16;
+    for (int t = 0; t < n_q; ++t) {
+      const int ib = ib0 + t;
+      if (!__all_sync(0xffffffffu, wait_bounded(bar(L::bDQFull), t & 1, p, abort_flag))) break;
+      tc_fence_after();
+      const int row = ib * 128 + qw * 32 + lane;
+      float* dst = p.dq + (static_cast<size_t>(bh) * p.N + row) * D;
+#pragma unroll 1
+      for (int k = 0; k < D / 32; ++k) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + kBwdColS + 32 * k, v);
+        tmem_wait_ld(v);
+        if (row < p.N) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            red_add_v4(dst + 32 * k + 4 * i, __uint_as_float(v[4 * i]),
+                       __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
+                       __uint_as_float(v[4 * i + 3]));
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::bDQFree));
+    }
+  }
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kBwdMmaWarp) tmem_dealloc(tmem, kTmemCols);
+}
+
+// D_i = sum_d dO_id O_id and log2(e) LSE_i for every row, padded to whole
+// 128-row blocks (D = 0, log2(e) LSE = +inf past N, so those queries weigh
+// nothing); one warp per row.
+template <int D>
+__global__ void fat_bwd_prep_kernel(const float* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                                    const float* __restrict__ lse, float* __restrict__ lse2,
+                                    float* __restrict__ dvec, int N, int Npad, long long rows) {
+  const long long row = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const long long bh = row / Npad;
+  const int n = static_cast<int>(row - bh * Npad);
+  float acc = 0.f;
+  if (n < N) {
+    const size_t base = (static_cast<size_t>(bh) * N + n) * D;
+#pragma unroll
+    for (int i = lane * 4; i < D; i += 128) {
+      const float4 ov = *reinterpret_cast<const float4*>(o + base + i);
+      const __nv_bfloat162 d01 = *reinterpret_cast<const __nv_bfloat162*>(dout + base + i);
+      const __nv_bfloat162 d23 = *reinterpret_cast<const __nv_bfloat162*>(dout + base + i + 2);
+      acc += ov.x * __low2float(d01) + ov.y * __high2float(d01) + ov.z * __low2float(d23) +
+             ov.w * __high2float(d23);
+    }
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) {
+    dvec[row] = n < N ? acc : 0.f;
+    lse2[row] = n < N ? lse[bh * N + n] * kLog2e : INFINITY;
+  }
+}
+
+}  // namespace fat

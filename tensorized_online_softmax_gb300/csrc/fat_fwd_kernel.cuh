@@ -159,7 +159,9 @@ struct Smem {
 // ---------------------------------------------------------------------------
 // bounded waits
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const FwdParams& p,
+// (P: any parameter block with poll_limit, timeout_ns and error_word)
+template <class P>
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const P& p,
                                              volatile uint32_t* abort_flag) {
   if (mbar_test_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();

@@ -32,6 +32,12 @@ int launch_fwd(const FwdParams& fp, int dev, int grid, int splits, cudaStream_t 
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }
 
+// Backward pass (fat_bwd.cu): D / LSE preparation, then the fused kernel.
+// Returns 0, -1 for a d without an instance, -4 on a CUDA error.
+struct BwdParams;
+int launch_bwd(const BwdParams& bp, int d, const float* o, const void* dout, const float* lse,
+               int dev, cudaStream_t stream);
+
 // LSE-weighted merge of split-KV partial results (fat_splitkv_combine.cu).
 int launch_splitkv_combine(const float* o_part, const float* lse_part, float* o, float* lse,
                            long long rows, int splits, int d, cudaStream_t stream);

@@ -105,6 +105,17 @@ __device__ __forceinline__ void bulk_wait_read() {
 __device__ __forceinline__ void fence_async_shared() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Vector atomic add of four floats to global memory (16-byte aligned).
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+__device__ __forceinline__ void st_global_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("st.global.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
 __device__ __forceinline__ void st_shared_v4u(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                               uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
@@ -172,12 +183,13 @@ __device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr, uint32_t lbo_byt
 
 // Instruction descriptor for kind::f16 (bf16 or fp16 inputs -> f32) and
 // kind::f8f6f4 (e4m3 -> f32): D format F32 at bit 4, A/B format codes at
-// bits 7 and 10 (kind::f16: 0 fp16, 1 bf16; kind::f8f6f4: 0 e4m3), B
-// major-ness at bit 16 (0 = K-major, 1 = MN-major), N >> 3 at bit 17, M >> 4
-// at bit 24.
+// bits 7 and 10 (kind::f16: 0 fp16, 1 bf16; kind::f8f6f4: 0 e4m3), A and B
+// major-ness at bits 15 and 16 (0 = K-major, 1 = MN-major), N >> 3 at bit 17,
+// M >> 4 at bit 24.
 template <uint32_t kFmt>
-__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool b_mn_major) {
-  return (1u << 4) | (kFmt << 7) | (kFmt << 10) |
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool b_mn_major,
+                                                     bool a_mn_major = false) {
+  return (1u << 4) | (kFmt << 7) | (kFmt << 10) | ((a_mn_major ? 1u : 0u) << 15) |
          ((b_mn_major ? 1u : 0u) << 16) | ((static_cast<uint32_t>(N) >> 3) << 17) |
          ((static_cast<uint32_t>(M) >> 4) << 24);
 }
