@@ -374,6 +374,27 @@ def run_all(args):
                           "ms": ms, "tflops": 4.0 * B * H * Nq * Nk * d / ms / 1e9,
                           "hbm_gbs": kv_bytes / ms / 1e6, "hbm_peak_gbs": peaks["hbm_gbs"],
                           "frac_hbm": kv_bytes / ms / 1e6 / peaks["hbm_gbs"]}), flush=True)
+    # backward pass on the bf16 workloads' shapes (dout ~ N(0, 1)): five
+    # GEMMs of 2 N^2 d FLOPs per head (S, dP, dV, dK, dQ; halved causal); the
+    # time includes the D / LSE preparation and the clearing of dq
+    for name in ("b4h16n2048d128", "b4h16n2048d128_causal", "b2h16n8192d128_causal",
+                 "stress_b1h32n16384d64"):
+        w = gen.WORKLOADS[name]
+        inp = gen.make_inputs(w)
+        q, k, v = (inp[n].to(device) for n in ("q", "k", "v"))
+        g = torch.Generator().manual_seed(77)
+        do = torch.randn(q.shape, generator=g).to(torch.bfloat16).to(device)
+        o, lse = fat.attn_fwd(q, k, v, w.causal, w.scale, w.X)
+        ws = torch.empty(fat.load_library().fat_attn_bwd_workspace_bytes(w.B, w.H, w.N),
+                         dtype=torch.uint8, device=device)
+        grads = tuple(torch.empty(q.shape, dtype=torch.float32, device=device) for _ in range(3))
+        ms = timeit(lambda: fat.attn_bwd(q, k, v, o, lse, do, w.causal, w.scale, workspace=ws,
+                                         out=grads), steps)
+        flops = 2.5 * w.flops
+        print(json.dumps({"workload": name + "_bwd", "ms": ms, "tflops": flops / ms / 1e9,
+                          "peak_tflops": peaks["bf16_tflops"],
+                          "frac_tensor": flops / ms / 1e9 / peaks["bf16_tflops"]}),
+              flush=True)
 
 
 def run_sweep(args):

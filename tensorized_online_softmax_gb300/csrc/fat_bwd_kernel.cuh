@@ -14,9 +14,10 @@
 // with D_i = sum_d dO_id O_id formed beforehand (fat_bwd_prep_kernel).
 // One CTA per 128-key block of one (b, h); it walks the query blocks that
 // see those keys (all of them, or those at or after the diagonal when
-// causal).  Warps: 0-3 form P^T and dS^T (one key row per thread), 4-7 move
-// each dQ partial from TMEM to global memory, 8 issues the MMAs, 9 loads
-// K and V once and Q, dO per query block with TMA.
+// causal).  Warps: 0-7 form P^T and dS^T (warp w: key rows 32 (w % 4) ..,
+// query columns 64 (w / 4) ..) and then move the block's dQ partial from
+// TMEM to global memory; 8 issues the MMAs; 9 loads K and V once and Q, dO,
+// log2(e) LSE and D per query block with TMA.
 #pragma once
 
 #include "fat_fwd_kernel.cuh"
@@ -44,10 +45,15 @@ struct BwdParams {
 constexpr int kBwdThreads = 320;
 constexpr int kBwdMmaWarp = 8;
 constexpr int kBwdLoadWarp = 9;
-// TMEM columns: S^T / P^T and then the dQ partial; dP^T; dV; dK
+// TMEM columns: S^T / P^T; dP^T; dV; dK; the dQ partial in columns of its
+// own when they fit (d = 64), else over S^T / P^T once the dV MMA has read P^T
 constexpr int kBwdColS = 0;
 constexpr int kBwdColDP = 128;
 constexpr int kBwdColDV = 256;
+template <int D>
+struct BwdColDQ {
+  static constexpr int value = 256 + 3 * D <= 512 ? 256 + 2 * D : kBwdColS;
+};
 
 template <int D>
 struct BwdSmem {
@@ -57,9 +63,12 @@ struct BwdSmem {
   static constexpr int kQ = 2 * kTile;
   static constexpr int kDO = 3 * kTile;
   static constexpr int kDS = 4 * kTile;      // dS^T: 128 keys x 128 queries bf16 (32 KB)
-  static constexpr int kBars = kDS + 32768;
+  static constexpr int kLse = kDS + 32768;   // log2(e) LSE of the query block (128 fp32)
+  static constexpr int kDvec = kLse + 512;   // D of the query block (128 fp32)
+  static constexpr int kBars = kDvec + 512;
+  // bSHeld + w % 4: both warps of those key rows hold their scores (2 arrivals)
   static constexpr int bKV = 0, bQFull = 1, bQFree = 2, bSFull = 3, bPReady = 4, bDQFull = 5,
-                       bDQFree = 6, bFinal = 7, bDrain = 8, kNumBars = 9;
+                       bDQFree = 6, bFinal = 7, bDrain = 8, bSHeld = 9, kNumBars = 13;
   static constexpr int kMisc = kBars + 8 * kNumBars;  // u32: tmem base, abort
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -70,6 +79,7 @@ template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_constant__ BwdParams p) {
   using L = BwdSmem<D>;
   constexpr int kAtoms = D / 64;  // 128-byte column slabs of a tile
+  constexpr int kColDQ = BwdColDQ<D>::value;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -92,11 +102,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
     mbar_init(bar(L::bQFull), 1);
     mbar_init(bar(L::bQFree), 1);
     mbar_init(bar(L::bSFull), 1);
-    mbar_init(bar(L::bPReady), 4);
+    mbar_init(bar(L::bPReady), 8);
     mbar_init(bar(L::bDQFull), 1);
-    mbar_init(bar(L::bDQFree), 4);
+    mbar_init(bar(L::bDQFree), 8);
     mbar_init(bar(L::bFinal), 1);
     mbar_init(bar(L::bDrain), 1);
+    for (int i = 0; i < 4; ++i) mbar_init(bar(L::bSHeld + i), 2);
     misc[1] = 0;
     fence_mbar_init();
   }
@@ -123,11 +134,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
       for (int t = 0; t < n_q; ++t) {
         if (t > 0 && !wait_bounded(bar(L::bQFree), (t - 1) & 1, p, abort_flag)) break;
         const int ib = ib0 + t;
-        mbar_arrive_expect_tx(bar(L::bQFull), 2 * L::kTile);
+        mbar_arrive_expect_tx(bar(L::bQFull), 2 * L::kTile + 1024);
         for (int a = 0; a < kAtoms; ++a) {
           tma_load_3d(sb + L::kQ + a * 16384, &p.tm_q, bar(L::bQFull), a * 64, ib * 128, bh);
           tma_load_3d(sb + L::kDO + a * 16384, &p.tm_do, bar(L::bQFull), a * 64, ib * 128, bh);
         }
+        const size_t row0 = static_cast<size_t>(bh) * p.Npad + ib * 128;
+        bulk_load(sb + L::kLse, p.lse2 + row0, 512, bar(L::bQFull));
+        bulk_load(sb + L::kDvec, p.dvec + row0, 512, bar(L::bQFull));
         issued = t + 1;
       }
       if (*abort_flag) {
@@ -165,8 +179,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         mma_ss<false>(tmem + kBwdColDP, v_kmaj + kstep(kk), do_kmaj + kstep(kk), idesc_sq, kk > 0);
-      // S^T = K Q^T, once the previous dQ partial has left those columns
-      if (t > 0 &&
+      // S^T = K Q^T (when the dQ partial shares its columns, once the
+      // previous one has left them)
+      if (kColDQ == kBwdColS && t > 0 &&
           !(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bDQFree), (t - 1) & 1, p, abort_flag))))
         break;
       tc_fence_after();
@@ -188,10 +203,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
         mma_ss<false>(tmem + kBwdColDV + D, ds_kmaj + kstep(kk), q_mn + mnstep(kk), idesc_b_mn,
                       t > 0 || kk > 0);
       mma_commit(bar(L::bQFree));  // Q and dO are free once these have read them
-      // dQ partial = dS K into the S columns (P^T was read by the dV MMAs above)
+      // dQ partial = dS K (over the S columns, P^T having been read by the dV
+      // MMAs above, or in its own columns once the previous one has left)
+      if (kColDQ != kBwdColS && t > 0 &&
+          !(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bDQFree), (t - 1) & 1, p, abort_flag))))
+        break;
+      tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
-        mma_ss<false>(tmem + kBwdColS, ds_mn + mnstep(kk), k_mn + mnstep(kk), idesc_ab_mn, kk > 0);
+        mma_ss<false>(tmem + kColDQ, ds_mn + mnstep(kk), k_mn + mnstep(kk), idesc_ab_mn, kk > 0);
       mma_commit(bar(L::bDQFull));
     }
     if (ok) {
@@ -201,12 +221,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
       wait_drain(bar(L::bDrain), 0);
     }
     __syncwarp();
-  } else if (warp < 4) {
-    // =================== P^T and dS^T (one key row per thread) ===================
-    const int r = warp * 32 + lane;
+  } else {
+    // ============ P^T, dS^T and the dQ partials (warps 0-7) ============
+    const int qw = warp & 3;   // TMEM lanes 32 qw ..: key rows (S^T, dP^T), query rows (dQ)
+    const int hf = warp >> 2;  // query columns 64 hf .. of S^T and dP^T
+    const int r = qw * 32 + lane;
     const int key = jb * 128 + r;
     const bool row_ok = key < p.N;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t lane_base = static_cast<uint32_t>(qw * 32) << 16;
     const float c = p.c;
     bool ok = true;
     for (int t = 0; t < n_q; ++t) {
@@ -214,41 +236,50 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
       if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bSFull), t & 1, p, abort_flag))))
         break;
       tc_fence_after();
-      const float* lse2 = p.lse2 + static_cast<size_t>(bh) * p.Npad + ib * 128;
-      const float* dvec = p.dvec + static_cast<size_t>(bh) * p.Npad + ib * 128;
+      uint32_t s[2][32];
+      tmem_ld32(tmem + lane_base + kBwdColS + 64 * hf, s[0]);
+      tmem_ld32(tmem + lane_base + kBwdColS + 64 * hf + 32, s[1]);
+      tmem_wait_ld(s[0]);
+      tmem_wait_ld(s[1]);
+      // P^T goes over the scores in place (columns 0-63): both warps of these
+      // rows must hold their scores first
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::bSHeld + qw));
+      if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bSHeld + qw), t & 1, p, abort_flag))))
+        break;
+      tc_fence_after();
       // causal: query ib * 128 + col sees this key iff col >= lim
       const int lim = p.causal ? key - ib * 128 : -1;
-#pragma unroll 1
-      for (int k = 0; k < 4; ++k) {
-        uint32_t s[32], dp[32];
-        tmem_ld32(tmem + lane_base + kBwdColS + 32 * k, s);
-        tmem_ld32(tmem + lane_base + kBwdColDP + 32 * k, dp);
-        float l2[32], dd[32];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 a = __ldg(reinterpret_cast<const float4*>(lse2 + 32 * k) + i);
-          const float4 b = __ldg(reinterpret_cast<const float4*>(dvec + 32 * k) + i);
-          l2[4 * i] = a.x; l2[4 * i + 1] = a.y; l2[4 * i + 2] = a.z; l2[4 * i + 3] = a.w;
-          dd[4 * i] = b.x; dd[4 * i + 1] = b.y; dd[4 * i + 2] = b.z; dd[4 * i + 3] = b.w;
-        }
-        tmem_wait_ld(s);
+      for (int kk = 0; kk < 2; ++kk) {
+        const int k = 2 * hf + kk;  // 32-column chunk of the block's queries
+        uint32_t dp[32];
+        tmem_ld32(tmem + lane_base + kBwdColDP + 32 * k, dp);
         tmem_wait_ld(dp);
         uint32_t pk[16], dk[16];
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float pv[2], dsv[2];
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const float4 l4 = ld_shared_v4(sb + L::kLse + (32 * k + 4 * i4) * 4);
+          const float4 d4 = ld_shared_v4(sb + L::kDvec + (32 * k + 4 * i4) * 4);
+          const float l2[4] = {l4.x, l4.y, l4.z, l4.w};
+          const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
+          float pv[4], dsv[4];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int col = 32 * k + i + e;
-            const bool keep = row_ok && col >= lim;
-            const float pf = keep ? ex2_approx(fmaf(__uint_as_float(s[i + e]), c, -l2[i + e])) : 0.f;
+          for (int e = 0; e < 4; ++e) {
+            const int i = 4 * i4 + e;
+            const bool keep = row_ok && 32 * k + i >= lim;
+            const float pf =
+                keep ? ex2_approx(fmaf(__uint_as_float(s[kk][i]), c, -l2[e])) : 0.f;
             pv[e] = pf;
-            dsv[e] = pf * (__uint_as_float(dp[i + e]) - dd[i + e]) * p.scale;
+            dsv[e] = pf * (__uint_as_float(dp[i]) - dd[e]) * p.scale;
           }
-          pk[i / 2] = pack_bf16x2(pv[0], pv[1]);
-          dk[i / 2] = pack_bf16x2(dsv[0], dsv[1]);
+          pk[2 * i4] = pack_bf16x2(pv[0], pv[1]);
+          pk[2 * i4 + 1] = pack_bf16x2(pv[2], pv[3]);
+          dk[2 * i4] = pack_bf16x2(dsv[0], dsv[1]);
+          dk[2 * i4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
         }
-        // P^T over its own scores (bf16, columns 16 k ..), dS^T into row r of
+        // P^T (bf16, two per column) at columns 16 k ..; dS^T into row r of
         // the swizzled tile: queries 32 k .. 32 k + 31 are four 16-byte chunks
         tmem_st16(tmem + lane_base + kBwdColS + 16 * k, pk);
         const uint32_t row = sb + L::kDS + (k >> 1) * 16384 + r * 128;
@@ -264,50 +295,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::bPReady));
-    }
-    // epilogue: dV and dK rows of this block's keys
-    if (ok) ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bFinal), 0, p, abort_flag));
-    if (ok) {
+
+      // this block's dQ partial (query rows 32 qw .., columns D/2 hf ..)
+      if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bDQFull), t & 1, p, abort_flag))))
+        break;
       tc_fence_after();
-      const size_t base = (static_cast<size_t>(bh) * p.N + key) * D;
-#pragma unroll 1
-      for (int which = 0; which < 2; ++which) {
-        float* out = which == 0 ? p.dv : p.dk;
-#pragma unroll 1
-        for (int k = 0; k < D / 32; ++k) {
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_base + kBwdColDV + which * D + 32 * k, v);
-          tmem_wait_ld(v);
-          if (row_ok) {
+      const int qrow = ib * 128 + r;
+      float* dst = p.dq + (static_cast<size_t>(bh) * p.N + qrow) * D + hf * (D / 2);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              st_global_v4(out + base + 32 * k + 4 * i, __uint_as_float(v[4 * i]),
-                           __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
-                           __uint_as_float(v[4 * i + 3]));
-          }
-        }
-      }
-    }
-    tc_fence_before();
-  } else {
-    // =================== dQ partials: TMEM -> global atomics ===================
-    const int qw = warp & 3;  // TMEM lanes 32 qw .. (query rows of the block)
-    const uint32_t lane_base = static_cast<uint32_t>(qw * 32) << 16;
-    for (int t = 0; t < n_q; ++t) {
-      const int ib = ib0 + t;
-      if (!__all_sync(0xffffffffu, wait_bounded(bar(L::bDQFull), t & 1, p, abort_flag))) break;
-      tc_fence_after();
-      const int row = ib * 128 + qw * 32 + lane;
-      float* dst = p.dq + (static_cast<size_t>(bh) * p.N + row) * D;
-#pragma unroll 1
-      for (int k = 0; k < D / 32; ++k) {
+      for (int cg = 0; cg < D / 64; ++cg) {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_base + kBwdColS + 32 * k, v);
+        tmem_ld32(tmem + lane_base + kColDQ + hf * (D / 2) + 32 * cg, v);
         tmem_wait_ld(v);
-        if (row < p.N) {
+        if (qrow < p.N) {
 #pragma unroll
           for (int i = 0; i < 8; ++i)
-            red_add_v4(dst + 32 * k + 4 * i, __uint_as_float(v[4 * i]),
+            red_add_v4(dst + 32 * cg + 4 * i, __uint_as_float(v[4 * i]),
                        __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
                        __uint_as_float(v[4 * i + 3]));
         }
@@ -316,6 +319,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::bDQFree));
     }
+    // epilogue: dV and dK rows of this block's keys (columns D/2 hf ..)
+    if (ok) ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bFinal), 0, p, abort_flag));
+    if (ok) {
+      tc_fence_after();
+      const size_t base = (static_cast<size_t>(bh) * p.N + key) * D + hf * (D / 2);
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        float* out = which == 0 ? p.dv : p.dk;
+#pragma unroll
+        for (int cg = 0; cg < D / 64; ++cg) {
+          uint32_t v[32];
+          tmem_ld32(tmem + lane_base + kBwdColDV + which * D + hf * (D / 2) + 32 * cg, v);
+          tmem_wait_ld(v);
+          if (row_ok) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              st_global_v4(out + base + 32 * cg + 4 * i, __uint_as_float(v[4 * i]),
+                           __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
+                           __uint_as_float(v[4 * i + 3]));
+          }
+        }
+      }
+    }
+    tc_fence_before();
   }
   __syncthreads();
   tc_fence_after();
