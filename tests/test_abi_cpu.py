@@ -138,3 +138,29 @@ def test_splitkv_workspace_and_validation(lib):
     assert call(splits=65) == fat.FAT_ERR_INVALID_ARG
     assert call(causal=1, Nq=2048, Nk=1024) == fat.FAT_ERR_INVALID_ARG  # Nk < Nq, causal
     assert call(Nk=0) == fat.FAT_ERR_INVALID_ARG
+
+
+def test_bwd_validation(lib):
+    """fat_attn_bwd refuses bad arguments before any device call."""
+    ws_bytes = lib.fat_attn_bwd_workspace_bytes(2, 3, 300)
+    # D and log2(e) LSE per row, rows padded to whole 128-row blocks
+    assert ws_bytes == 2 * 2 * 3 * 384 * 4 + 256
+    assert lib.fat_attn_bwd_workspace_bytes(0, 3, 300) == 0
+    assert lib.fat_attn_bwd_workspace_bytes(1, 1, 0) == 0
+    args = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000, do=0x6000, dq=0x7000,
+                dk=0x8000, dv=0x9000, B=2, H=3, N=300, d=64, causal=1, scale=0.125, ws=0xA000,
+                wsb=ws_bytes)
+
+    def call(**kw):
+        a = dict(args, **kw)
+        return lib.fat_attn_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["do"], a["dq"],
+                                a["dk"], a["dv"], a["B"], a["H"], a["N"], a["d"], a["causal"],
+                                a["scale"], a["ws"], a["wsb"], None)
+
+    for kw in (dict(q=None), dict(do=None), dict(dq=None), dict(ws=None), dict(d=96),
+               dict(d=256), dict(N=0), dict(B=0), dict(H=-2), dict(scale=0.0),
+               dict(scale=float("inf")), dict(wsb=ws_bytes - 1)):
+        assert call(**kw) == fat.FAT_ERR_INVALID_ARG, kw
+    for kw in (dict(q=0x1008), dict(do=0x6004), dict(dq=0x7004), dict(o=0x4008),
+               dict(lse=0x5002)):
+        assert call(**kw) == fat.FAT_ERR_ALIGNMENT, kw
