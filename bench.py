@@ -318,23 +318,7 @@ def run_all(args):
 
     device = torch.device("cuda", 0)
     peaks = load_peaks()
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
-
-    def timeit(fn, steps):
-        for _ in range(3):
-            flush.zero_()
-            fn()
-        tot = 0.0
-        for _ in range(steps):
-            flush.zero_()
-            s0, s1 = torch.cuda.Event(True), torch.cuda.Event(True)
-            s0.record()
-            fn()
-            s1.record()
-            s1.synchronize()
-            tot += s0.elapsed_time(s1)
-        return tot / steps
-
+    timeit = event_timer(torch, device)
     steps = max(10, min(args.steps, 100))
     for name, w in gen.WORKLOADS.items():
         if name == "tiny":
@@ -374,11 +358,50 @@ def run_all(args):
                           "ms": ms, "tflops": 4.0 * B * H * Nq * Nk * d / ms / 1e9,
                           "hbm_gbs": kv_bytes / ms / 1e6, "hbm_peak_gbs": peaks["hbm_gbs"],
                           "frac_hbm": kv_bytes / ms / 1e6 / peaks["hbm_gbs"]}), flush=True)
-    # backward pass on the bf16 workloads' shapes (dout ~ N(0, 1)): five
-    # GEMMs of 2 N^2 d FLOPs per head (S, dP, dV, dK, dQ; halved causal); the
-    # time includes the D / LSE preparation and the clearing of dq
-    for name in ("b4h16n2048d128", "b4h16n2048d128_causal", "b2h16n8192d128_causal",
-                 "stress_b1h32n16384d64"):
+    run_bwd(args, BWD_WORKLOADS, steps)
+
+
+def event_timer(torch, device):
+    """fn, steps -> mean device time (ms) of fn over `steps` calls, each
+    preceded by an L2 flush, after 3 untimed calls."""
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    def timeit(fn, steps):
+        for _ in range(3):
+            flush.zero_()
+            fn()
+        tot = 0.0
+        for _ in range(steps):
+            flush.zero_()
+            s0, s1 = torch.cuda.Event(True), torch.cuda.Event(True)
+            s0.record()
+            fn()
+            s1.record()
+            s1.synchronize()
+            tot += s0.elapsed_time(s1)
+        return tot / steps
+
+    return timeit
+
+
+BWD_WORKLOADS = ("b4h16n2048d128", "b4h16n2048d128_causal", "b2h16n8192d128_causal",
+                 "stress_b1h32n16384d64")
+
+
+def run_bwd(args, names, steps):
+    """Backward pass on the shapes of bf16 workloads (dout ~ N(0, 1)), one
+    JSON line each: five GEMMs of 2 N^2 d FLOPs per head (S, dP, dV, dK, dQ;
+    halved causal), i.e. 2.5x the forward's; the time includes the D / LSE
+    preparation and the clearing of dq."""
+    import torch
+
+    import tensorized_online_softmax_gb300 as fat
+    from tensorized_online_softmax_gb300 import inputs as gen
+
+    device = torch.device("cuda", 0)
+    peaks = load_peaks()
+    timeit = event_timer(torch, device)
+    for name in names:
         w = gen.WORKLOADS[name]
         inp = gen.make_inputs(w)
         q, k, v = (inp[n].to(device) for n in ("q", "k", "v"))
@@ -390,6 +413,8 @@ def run_all(args):
         grads = tuple(torch.empty(q.shape, dtype=torch.float32, device=device) for _ in range(3))
         ms = timeit(lambda: fat.attn_bwd(q, k, v, o, lse, do, w.causal, w.scale, workspace=ws,
                                          out=grads), steps)
+        if fat.check_device_error() != fat.FAT_OK:
+            raise SystemExit("device error word set during the backward run")
         flops = 2.5 * w.flops
         print(json.dumps({"workload": name + "_bwd", "ms": ms, "tflops": flops / ms / 1e9,
                           "peak_tflops": peaks["bf16_tflops"],
@@ -470,8 +495,13 @@ def main():
                     help="one line per workload (results tables) instead of the benchmark line")
     ap.add_argument("--sweep", action="store_true",
                     help="the pages' fp16 / fp8 sweep, one line per shape")
+    ap.add_argument("--bwd", action="store_true",
+                    help="time the backward pass on --workload (bf16) only, one line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.bwd:
+        run_bwd(args, [args.workload], max(1, args.steps))
+        return
     if args.sweep:
         run_sweep(args)
         return

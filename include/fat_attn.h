@@ -236,8 +236,8 @@ int fat_attn_fwd_ex(const fat_params* p);
  * q, k, v, dout: bf16 [B, H, N, d]; o, lse: the fp32 outputs of a forward
  * call on the same q, k, v (any variant: they are exact up to rounding);
  * dq, dk, dv: fp32 [B, H, N, d], overwritten (dq is cleared on `stream`
- * first and accumulated across key blocks with atomic adds, so its low-order
- * bits may differ from run to run).  d is 64 or 128.  P and dS enter their
+ * first and accumulated across key blocks with TMA reduce-adds in no fixed
+ * order, so its low-order bits may differ from run to run).  d is 64 or 128.  P and dS enter their
  * MMAs as bf16, with fp32 accumulation.  workspace: device memory owned by
  * the caller, at least fat_attn_bwd_workspace_bytes(B, H, N) bytes (D and
  * log2(e) LSE per row); calls sharing it must not overlap on the device.

@@ -461,7 +461,8 @@ int fat_attn_bwd(const void* q, const void* k, const void* v, const float* o, co
   if (!encode_qkv_map(&bp.tm_q, q, d, N, bh, 2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) ||
       !encode_qkv_map(&bp.tm_k, k, d, N, bh, 2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) ||
       !encode_qkv_map(&bp.tm_v, v, d, N, bh, 2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) ||
-      !encode_qkv_map(&bp.tm_do, dout, d, N, bh, 2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
+      !encode_qkv_map(&bp.tm_do, dout, d, N, bh, 2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) ||
+      !encode_o_map(&bp.tm_dq, dq, d, N, BH))
     return FAT_ERR_LAUNCH;
   const uintptr_t base = (reinterpret_cast<uintptr_t>(workspace) + 255) & ~uintptr_t(255);
   bp.lse2 = reinterpret_cast<const float*>(base);

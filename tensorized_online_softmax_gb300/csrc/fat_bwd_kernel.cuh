@@ -8,16 +8,18 @@
 //   dP^T = V dO^T          (TMEM)       dS^T = scale P^T * (dP^T - D)
 //   dV  += P^T dO          (A = P^T from TMEM, bf16)
 //   dK  += dS^T Q          (A = dS^T from shared memory, K-major)
-//   dQ   = dS K            (A = the same tile read MN-major), added to
-//                           global dQ with vector atomics
+//   dQ   = dS K            (A = the same tile read MN-major), staged in
+//                           shared memory and added to global dQ with TMA
+//                           tensor reduce-adds
 //
 // with D_i = sum_d dO_id O_id formed beforehand (fat_bwd_prep_kernel).
 // One CTA per 128-key block of one (b, h); it walks the query blocks that
 // see those keys (all of them, or those at or after the diagonal when
 // causal).  Warps: 0-7 form P^T and dS^T (warp w: key rows 32 (w % 4) ..,
-// query columns 64 (w / 4) ..) and then move the block's dQ partial from
-// TMEM to global memory; 8 issues the MMAs; 9 loads K and V once and Q, dO,
-// log2(e) LSE and D per query block with TMA.
+// query columns 64 (w / 4) ..) and then stage the block's dQ partial from
+// TMEM in shared memory; 8 issues the MMAs; 9 loads K and V once and Q, dO,
+// log2(e) LSE and D per query block with TMA; 10 adds each staged dQ
+// partial into global dQ with TMA reduce-adds.
 #pragma once
 
 #include "fat_fwd_kernel.cuh"
@@ -29,9 +31,10 @@ struct BwdParams {
   CUtensorMap tm_k;
   CUtensorMap tm_v;
   CUtensorMap tm_do;
+  CUtensorMap tm_dq;  // fp32 [B*H, N, d], boxes of 32 columns x 128 rows, 128-byte swizzle
   const float* lse2;  // [B*H][Npad] log2(e) * LSE; +inf for rows >= N
   const float* dvec;  // [B*H][Npad] D; 0 for rows >= N
-  float* dq;          // fp32 [B*H, N, d], zero on entry, accumulated atomically
+  float* dq;          // fp32 [B*H, N, d], zero on entry, accumulated by TMA reduce-adds
   float* dk;          // fp32 [B*H, N, d]
   float* dv;          // fp32 [B*H, N, d]
   int BH, N, Npad, causal, n_blocks;
@@ -42,9 +45,10 @@ struct BwdParams {
   unsigned int* error_word;
 };
 
-constexpr int kBwdThreads = 320;
+constexpr int kBwdThreads = 352;
 constexpr int kBwdMmaWarp = 8;
 constexpr int kBwdLoadWarp = 9;
+constexpr int kBwdReduceWarp = 10;
 // TMEM columns: S^T / P^T; dP^T; dV; dK; the dQ partial in columns of its
 // own when they fit (d = 64), else over S^T / P^T once the dV MMA has read P^T
 constexpr int kBwdColS = 0;
@@ -63,12 +67,18 @@ struct BwdSmem {
   static constexpr int kQ = 2 * kTile;
   static constexpr int kDO = 3 * kTile;
   static constexpr int kDS = 4 * kTile;      // dS^T: 128 keys x 128 queries bf16 (32 KB)
-  static constexpr int kLse = kDS + 32768;   // log2(e) LSE of the query block (128 fp32)
+  // the dQ partial of a query block: fp32, 128-byte-swizzled boxes of 32
+  // columns x 128 rows (16 KB each), the layout of the dQ tensor map
+  static constexpr int kDQ = kDS + 32768;
+  static constexpr int kLse = kDQ + 128 * D * 4;  // log2(e) LSE of the query block (128 fp32)
   static constexpr int kDvec = kLse + 512;   // D of the query block (128 fp32)
   static constexpr int kBars = kDvec + 512;
-  // bSHeld + w % 4: both warps of those key rows hold their scores (2 arrivals)
+  // bSHeld + w % 4: both warps of those key rows hold their scores (2 arrivals);
+  // bStaged: the dQ partial is in shared memory (8 arrivals); bStageFree: its
+  // reduce-adds have read it (1 arrival)
   static constexpr int bKV = 0, bQFull = 1, bQFree = 2, bSFull = 3, bPReady = 4, bDQFull = 5,
-                       bDQFree = 6, bFinal = 7, bDrain = 8, bSHeld = 9, kNumBars = 13;
+                       bDQFree = 6, bFinal = 7, bDrain = 8, bSHeld = 9, bStaged = 13,
+                       bStageFree = 14, kNumBars = 15;
   static constexpr int kMisc = kBars + 8 * kNumBars;  // u32: tmem base, abort
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -96,6 +106,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
   const int bh = static_cast<int>(blockIdx.x) % p.BH;
   const int ib0 = p.causal ? jb : 0;
   const int n_q = p.n_blocks - ib0;
+  // query block of step t: causal blocks start at their diagonal; the others
+  // start at their own index and wrap, so that the key blocks of a head add
+  // into different dQ rows at any one time
+  auto q_block = [&](int t) -> int {
+    return p.causal ? ib0 + t : (jb + t < p.n_blocks ? jb + t : jb + t - p.n_blocks);
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(L::bKV), 1);
@@ -108,6 +124,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
     mbar_init(bar(L::bFinal), 1);
     mbar_init(bar(L::bDrain), 1);
     for (int i = 0; i < 4; ++i) mbar_init(bar(L::bSHeld + i), 2);
+    mbar_init(bar(L::bStaged), 8);
+    mbar_init(bar(L::bStageFree), 1);
     misc[1] = 0;
     fence_mbar_init();
   }
@@ -133,7 +151,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
       int issued = 0;
       for (int t = 0; t < n_q; ++t) {
         if (t > 0 && !wait_bounded(bar(L::bQFree), (t - 1) & 1, p, abort_flag)) break;
-        const int ib = ib0 + t;
+        const int ib = q_block(t);
         mbar_arrive_expect_tx(bar(L::bQFull), 2 * L::kTile + 1024);
         for (int a = 0; a < kAtoms; ++a) {
           tma_load_3d(sb + L::kQ + a * 16384, &p.tm_q, bar(L::bQFull), a * 64, ib * 128, bh);
@@ -221,6 +239,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
       wait_drain(bar(L::bDrain), 0);
     }
     __syncwarp();
+  } else if (warp == kBwdReduceWarp) {
+    // =================== dQ reduce-adds ===================
+    for (int t = 0; t < n_q; ++t) {
+      if (!__all_sync(0xffffffffu, wait_bounded(bar(L::bStaged), t & 1, p, abort_flag))) break;
+      if (lane == 0) {
+        // rows past N are clipped by the tensor map
+        for (int b = 0; b < D / 32; ++b)
+          tma_reduce_add_3d(&p.tm_dq, sb + L::kDQ + b * 16384, b * 32, q_block(t) * 128, bh);
+        bulk_commit();
+        bulk_wait_read();
+        mbar_arrive(bar(L::bStageFree));
+      }
+      __syncwarp();
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   } else {
     // ============ P^T, dS^T and the dQ partials (warps 0-7) ============
     const int qw = warp & 3;   // TMEM lanes 32 qw ..: key rows (S^T, dP^T), query rows (dQ)
@@ -232,7 +266,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
     const float c = p.c;
     bool ok = true;
     for (int t = 0; t < n_q; ++t) {
-      const int ib = ib0 + t;
+      const int ib = q_block(t);
       if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bSFull), t & 1, p, abort_flag))))
         break;
       tc_fence_after();
@@ -296,28 +330,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(L::bPReady));
 
-      // this block's dQ partial (query rows 32 qw .., columns D/2 hf ..)
+      // this block's dQ partial (query rows 32 qw .., columns D/2 hf ..) into
+      // the staging boxes, once the previous partial's reduce-adds read them
       if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bDQFull), t & 1, p, abort_flag))))
         break;
+      if (t > 0 &&
+          !(ok = __all_sync(0xffffffffu,
+                            wait_bounded(bar(L::bStageFree), (t - 1) & 1, p, abort_flag))))
+        break;
       tc_fence_after();
-      const int qrow = ib * 128 + r;
-      float* dst = p.dq + (static_cast<size_t>(bh) * p.N + qrow) * D + hf * (D / 2);
 #pragma unroll
       for (int cg = 0; cg < D / 64; ++cg) {
         uint32_t v[32];
         tmem_ld32(tmem + lane_base + kColDQ + hf * (D / 2) + 32 * cg, v);
         tmem_wait_ld(v);
-        if (qrow < p.N) {
+        const uint32_t box = sb + L::kDQ + (hf * (D / 64) + cg) * 16384 + r * 128;
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            red_add_v4(dst + 32 * cg + 4 * i, __uint_as_float(v[4 * i]),
-                       __uint_as_float(v[4 * i + 1]), __uint_as_float(v[4 * i + 2]),
-                       __uint_as_float(v[4 * i + 3]));
-        }
+        for (int c4 = 0; c4 < 8; ++c4)
+          st_shared_v4u(box + ((c4 ^ (r & 7)) << 4), v[4 * c4], v[4 * c4 + 1], v[4 * c4 + 2],
+                        v[4 * c4 + 3]);
       }
+      fence_async_shared();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::bDQFree));
+      if (lane == 0) {
+        mbar_arrive(bar(L::bDQFree));
+        mbar_arrive(bar(L::bStaged));
+      }
     }
     // epilogue: dV and dK rows of this block's keys (columns D/2 hf ..)
     if (ok) ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bFinal), 0, p, abort_flag));
