@@ -50,13 +50,13 @@ constexpr int kBwdMmaWarp = 8;
 constexpr int kBwdLoadWarp = 9;
 constexpr int kBwdReduceWarp = 10;
 // TMEM columns: S^T / P^T; dP^T; dV; dK; the dQ partial in columns of its
-// own when they fit (d = 64), else over S^T / P^T once the dV MMA has read P^T
+// own when they fit (d = 64), else over dP^T once dS^T has been formed
 constexpr int kBwdColS = 0;
 constexpr int kBwdColDP = 128;
 constexpr int kBwdColDV = 256;
 template <int D>
 struct BwdColDQ {
-  static constexpr int value = 256 + 3 * D <= 512 ? 256 + 2 * D : kBwdColS;
+  static constexpr int value = 256 + 3 * D <= 512 ? 256 + 2 * D : kBwdColDP;
 };
 
 template <int D>
@@ -73,12 +73,15 @@ struct BwdSmem {
   static constexpr int kLse = kDQ + 128 * D * 4;  // log2(e) LSE of the query block (128 fp32)
   static constexpr int kDvec = kLse + 512;   // D of the query block (128 fp32)
   static constexpr int kBars = kDvec + 512;
-  // bSHeld + w % 4: both warps of those key rows hold their scores (2 arrivals);
-  // bStaged: the dQ partial is in shared memory (8 arrivals); bStageFree: its
-  // reduce-adds have read it (1 arrival)
+  // bQFull / bQFree: Q with log2(e) LSE and D; bOFull / bOFree: dO;
+  // bSFull, bDPFull: S^T, dP^T in TMEM; bPReady: P^T in TMEM, bDSReady: dS^T
+  // in shared memory (8 arrivals each); bSHeld + w % 4: both warps of those
+  // key rows hold their scores (2 arrivals); bStaged: the dQ partial is in
+  // shared memory (8 arrivals); bStageFree: its reduce-adds have read it
   static constexpr int bKV = 0, bQFull = 1, bQFree = 2, bSFull = 3, bPReady = 4, bDQFull = 5,
                        bDQFree = 6, bFinal = 7, bDrain = 8, bSHeld = 9, bStaged = 13,
-                       bStageFree = 14, kNumBars = 15;
+                       bStageFree = 14, bOFull = 15, bOFree = 16, bDPFull = 17, bDSReady = 18,
+                       kNumBars = 19;
   static constexpr int kMisc = kBars + 8 * kNumBars;  // u32: tmem base, abort
   static constexpr int kBytes = kMisc + 16;
   static constexpr int kAlloc = kBytes + 1024;
@@ -126,6 +129,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
     for (int i = 0; i < 4; ++i) mbar_init(bar(L::bSHeld + i), 2);
     mbar_init(bar(L::bStaged), 8);
     mbar_init(bar(L::bStageFree), 1);
+    mbar_init(bar(L::bOFull), 1);
+    mbar_init(bar(L::bOFree), 1);
+    mbar_init(bar(L::bDPFull), 1);
+    mbar_init(bar(L::bDSReady), 8);
     misc[1] = 0;
     fence_mbar_init();
   }
@@ -148,24 +155,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
         tma_load_3d(sb + L::kK + a * 16384, &p.tm_k, bar(L::bKV), a * 64, jb * 128, bh);
         tma_load_3d(sb + L::kV + a * 16384, &p.tm_v, bar(L::bKV), a * 64, jb * 128, bh);
       }
-      int issued = 0;
+      // dO of block t once dV of block t - 1 has read the previous one; Q,
+      // log2(e) LSE and D once dK of block t - 1 has (D is read while dS is
+      // formed, which dK waits for, so it travels with Q)
+      int issued_o = 0, issued_q = 0;
       for (int t = 0; t < n_q; ++t) {
-        if (t > 0 && !wait_bounded(bar(L::bQFree), (t - 1) & 1, p, abort_flag)) break;
         const int ib = q_block(t);
-        mbar_arrive_expect_tx(bar(L::bQFull), 2 * L::kTile + 1024);
-        for (int a = 0; a < kAtoms; ++a) {
+        if (t > 0 && !wait_bounded(bar(L::bOFree), (t - 1) & 1, p, abort_flag)) break;
+        mbar_arrive_expect_tx(bar(L::bOFull), L::kTile);
+        for (int a = 0; a < kAtoms; ++a)
+          tma_load_3d(sb + L::kDO + a * 16384, &p.tm_do, bar(L::bOFull), a * 64, ib * 128, bh);
+        issued_o = t + 1;
+        if (t > 0 && !wait_bounded(bar(L::bQFree), (t - 1) & 1, p, abort_flag)) break;
+        mbar_arrive_expect_tx(bar(L::bQFull), L::kTile + 1024);
+        for (int a = 0; a < kAtoms; ++a)
           tma_load_3d(sb + L::kQ + a * 16384, &p.tm_q, bar(L::bQFull), a * 64, ib * 128, bh);
-          tma_load_3d(sb + L::kDO + a * 16384, &p.tm_do, bar(L::bQFull), a * 64, ib * 128, bh);
-        }
         const size_t row0 = static_cast<size_t>(bh) * p.Npad + ib * 128;
         bulk_load(sb + L::kLse, p.lse2 + row0, 512, bar(L::bQFull));
         bulk_load(sb + L::kDvec, p.dvec + row0, 512, bar(L::bQFull));
-        issued = t + 1;
+        issued_q = t + 1;
       }
       if (*abort_flag) {
         // let the copies already issued land before the CTA can exit
         wait_drain(bar(L::bKV), 0);
-        if (issued > 0) wait_drain(bar(L::bQFull), (issued - 1) & 1);
+        if (issued_o > 0) wait_drain(bar(L::bOFull), (issued_o - 1) & 1);
+        if (issued_q > 0) wait_drain(bar(L::bQFull), (issued_q - 1) & 1);
       }
     }
     __syncwarp();
@@ -188,44 +202,47 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
     auto kstep = [](int kk) -> uint32_t { return ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4; };
     auto mnstep = [](int kk) -> uint32_t { return (kk * 2048) >> 4; };
     bool ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bKV), 0, p, abort_flag));
+    auto wait_all = [&](int b, int phase) -> bool {
+      return __all_sync(0xffffffffu, wait_bounded(bar(b), phase & 1, p, abort_flag));
+    };
     for (int t = 0; ok && t < n_q; ++t) {
-      if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bQFull), t & 1, p, abort_flag))))
-        break;
-      tc_fence_after();
-      // dP^T = V dO^T (its TMEM columns were last read by the softmax warps
-      // of the previous block, before they signalled P ready)
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        mma_ss<false>(tmem + kBwdColDP, v_kmaj + kstep(kk), do_kmaj + kstep(kk), idesc_sq, kk > 0);
-      // S^T = K Q^T (when the dQ partial shares its columns, once the
-      // previous one has left them)
-      if (kColDQ == kBwdColS && t > 0 &&
-          !(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bDQFree), (t - 1) & 1, p, abort_flag))))
-        break;
+      // S^T = K Q^T (its columns last held P^T of block t - 1, which the dV
+      // MMAs issued before this one read)
+      if (!(ok = wait_all(L::bQFull, t))) break;
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
         mma_ss<false>(tmem + kBwdColS, k_kmaj + kstep(kk), q_kmaj + kstep(kk), idesc_sq, kk > 0);
       mma_commit(bar(L::bSFull));
-      if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bPReady), t & 1, p, abort_flag))))
-        break;
+      // dP^T = V dO^T (when the dQ partial shares its columns, once the
+      // previous one has left them)
+      if (!(ok = wait_all(L::bOFull, t))) break;
+      if (kColDQ == kBwdColDP && t > 0 && !(ok = wait_all(L::bDQFree, t - 1))) break;
       tc_fence_after();
-      // dV += P^T dO: P^T (bf16, two per column) from TMEM, 8 columns per K step
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ss<false>(tmem + kBwdColDP, v_kmaj + kstep(kk), do_kmaj + kstep(kk), idesc_sq, kk > 0);
+      mma_commit(bar(L::bDPFull));
+      // dV += P^T dO: P^T (bf16, two per column) from TMEM, 8 columns per K
+      // step, while the softmax warps still form dS^T
+      if (!(ok = wait_all(L::bPReady, t))) break;
+      tc_fence_after();
 #pragma unroll
       for (int g = 0; g < 8; ++g)
         mma_ts<false>(tmem + kBwdColDV, tmem + kBwdColS + g * 8, do_mn + mnstep(g), idesc_b_mn,
                       t > 0 || g > 0);
+      mma_commit(bar(L::bOFree));
       // dK += dS^T Q
+      if (!(ok = wait_all(L::bDSReady, t))) break;
+      tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
         mma_ss<false>(tmem + kBwdColDV + D, ds_kmaj + kstep(kk), q_mn + mnstep(kk), idesc_b_mn,
                       t > 0 || kk > 0);
-      mma_commit(bar(L::bQFree));  // Q and dO are free once these have read them
-      // dQ partial = dS K (over the S columns, P^T having been read by the dV
-      // MMAs above, or in its own columns once the previous one has left)
-      if (kColDQ != kBwdColS && t > 0 &&
-          !(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bDQFree), (t - 1) & 1, p, abort_flag))))
-        break;
+      mma_commit(bar(L::bQFree));
+      // dQ partial = dS K (over dP^T, which the softmax warps have read, or in
+      // its own columns once the previous partial has left them)
+      if (kColDQ != kBwdColDP && t > 0 && !(ok = wait_all(L::bDQFree, t - 1))) break;
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
@@ -285,37 +302,62 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
       tc_fence_after();
       // causal: query ib * 128 + col sees this key iff col >= lim
       const int lim = p.causal ? key - ib * 128 : -1;
+      // P^T = exp2(c S^T - log2(e) LSE), kept in fp32 (over the scores'
+      // registers) for dS^T and stored as bf16 over the scores' columns
+      // (columns 16 k .. for the 32-column chunk k)
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
         const int k = 2 * hf + kk;  // 32-column chunk of the block's queries
-        uint32_t dp[32];
-        tmem_ld32(tmem + lane_base + kBwdColDP + 32 * k, dp);
-        tmem_wait_ld(dp);
-        uint32_t pk[16], dk[16];
+        uint32_t pk[16];
 #pragma unroll
         for (int i4 = 0; i4 < 8; ++i4) {
           const float4 l4 = ld_shared_v4(sb + L::kLse + (32 * k + 4 * i4) * 4);
-          const float4 d4 = ld_shared_v4(sb + L::kDvec + (32 * k + 4 * i4) * 4);
           const float l2[4] = {l4.x, l4.y, l4.z, l4.w};
-          const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
-          float pv[4], dsv[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int i = 4 * i4 + e;
             const bool keep = row_ok && 32 * k + i >= lim;
             const float pf =
                 keep ? ex2_approx(fmaf(__uint_as_float(s[kk][i]), c, -l2[e])) : 0.f;
-            pv[e] = pf;
-            dsv[e] = pf * (__uint_as_float(dp[i]) - dd[e]) * p.scale;
+            s[kk][i] = __float_as_uint(pf);
           }
-          pk[2 * i4] = pack_bf16x2(pv[0], pv[1]);
-          pk[2 * i4 + 1] = pack_bf16x2(pv[2], pv[3]);
+          pk[2 * i4] = pack_bf16x2(__uint_as_float(s[kk][4 * i4]),
+                                   __uint_as_float(s[kk][4 * i4 + 1]));
+          pk[2 * i4 + 1] = pack_bf16x2(__uint_as_float(s[kk][4 * i4 + 2]),
+                                       __uint_as_float(s[kk][4 * i4 + 3]));
+        }
+        tmem_st16(tmem + lane_base + kBwdColS + 16 * k, pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(L::bPReady));
+
+      // dS^T = scale P^T (dP^T - D) into row r of the swizzled tile (queries
+      // 32 k .. 32 k + 31 are four 16-byte chunks), while the dV MMAs run
+      if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bDPFull), t & 1, p, abort_flag))))
+        break;
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        const int k = 2 * hf + kk;
+        uint32_t dp[32];
+        tmem_ld32(tmem + lane_base + kBwdColDP + 32 * k, dp);
+        tmem_wait_ld(dp);
+        uint32_t dk[16];
+#pragma unroll
+        for (int i4 = 0; i4 < 8; ++i4) {
+          const float4 d4 = ld_shared_v4(sb + L::kDvec + (32 * k + 4 * i4) * 4);
+          const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
+          float dsv[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = 4 * i4 + e;
+            dsv[e] = __uint_as_float(s[kk][i]) * (__uint_as_float(dp[i]) - dd[e]) * p.scale;
+          }
           dk[2 * i4] = pack_bf16x2(dsv[0], dsv[1]);
           dk[2 * i4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
         }
-        // P^T (bf16, two per column) at columns 16 k ..; dS^T into row r of
-        // the swizzled tile: queries 32 k .. 32 k + 31 are four 16-byte chunks
-        tmem_st16(tmem + lane_base + kBwdColS + 16 * k, pk);
         const uint32_t row = sb + L::kDS + (k >> 1) * 16384 + r * 128;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
@@ -324,11 +366,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
                         dk[4 * cc + 2], dk[4 * cc + 3]);
         }
       }
-      tmem_wait_st();
       fence_async_shared();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(L::bPReady));
+      if (lane == 0) mbar_arrive(bar(L::bDSReady));
 
       // this block's dQ partial (query rows 32 qw .., columns D/2 hf ..) into
       // the staging boxes, once the previous partial's reduce-adds read them
