@@ -475,6 +475,15 @@ int fat_attn_bwd(const void* q, const void* k, const void* v, const float* o, co
   bp.Npad = static_cast<int>(npad);
   bp.causal = causal ? 1 : 0;
   bp.n_blocks = static_cast<int>(npad / 128);
+  // causal block order: groups of heads whose Q, dO (bf16) and dQ (fp32),
+  // 8 N d bytes each, fill about 48 MiB of L2
+  {
+    const long long per_head = 8ll * N * d;
+    long long g = (48ll << 20) / per_head;
+    if (g < 1) g = 1;
+    if (g > BH) g = BH;
+    bp.group_heads = static_cast<int>(g);
+  }
   bp.c = scale * fat::kLog2e;
   bp.scale = scale;
   bp.poll_limit = 0;
