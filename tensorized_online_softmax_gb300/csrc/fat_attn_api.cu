@@ -203,6 +203,14 @@ int run_fwd(const fat_params* p, int Nq, int Nk, int splits, void* workspace,
   fp.causal = p->causal ? 1 : 0;
   fp.X = p->X;
   fp.n_mblocks = static_cast<int>(n_mblocks);
+  // block order: groups of heads whose K and V (2 Nk d input bytes each)
+  // fill about 48 MiB of L2
+  {
+    long long g = (48ll << 20) / (2ll * Nk * p->d * elt);
+    if (g < 1) g = 1;
+    if (g > BH) g = BH;
+    fp.group_heads = static_cast<int>(g);
+  }
   fp.kv_split_len = kv_split_len;
   fp.o_part = o_part;
   fp.lse_part = lse_part;

@@ -76,6 +76,7 @@ struct FwdParams {
   int causal;              // key j allowed for query i iff j <= i + Nk - Nq
   int X;
   int n_mblocks;           // ceil(Nq / 128)
+  int group_heads;         // heads whose query blocks are ordered together
   int kv_split_len;        // keys per split (a multiple of 128): blockIdx.y = split
   float* o_part;           // nullable: per-split partial O [splits][B*H][Nq][d] ...
   float* lse_part;         // ... and LSE [splits][B*H][Nq] instead of o / lse
@@ -668,10 +669,21 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
   volatile uint32_t* abort_flag = misc + 1;
   auto bar = [&](int i) -> uint32_t { return sb + L::kBars + 8 * i; };
 
-  // work item: heaviest query blocks first (causal), then (b, h)
+  // work item: query block mblock of head bh
   const int BH = p.B * p.H;
-  const int mblock = p.n_mblocks - 1 - static_cast<int>(blockIdx.x) / BH;
-  const int bh = static_cast<int>(blockIdx.x) % BH;
+  // (heads run a few at a time, as many as keep their K and V in L2 while
+  // the query blocks re-read them; within a group, the heaviest causal
+  // blocks first)
+  int mblock, bh;
+  {
+    const int idx = static_cast<int>(blockIdx.x);
+    const int per = p.group_heads * p.n_mblocks;
+    const int g = idx / per;
+    const int rem = idx - g * per;
+    const int gh = min(p.group_heads, BH - g * p.group_heads);
+    mblock = p.n_mblocks - 1 - rem / gh;
+    bh = g * p.group_heads + rem % gh;
+  }
   const int m0 = mblock * kRowsPerCta;
   // this block's key range: the split's range, cut at the causal limit of
   // its last row
