@@ -211,6 +211,11 @@ int run_fwd(const fat_params* p, int Nq, int Nk, int splits, void* workspace,
     if (g > BH) g = BH;
     fp.group_heads = static_cast<int>(g);
   }
+  {
+    int sms = 0;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    fp.prefetch_stride = sms > 0 ? sms : 0;
+  }
   fp.kv_split_len = kv_split_len;
   fp.o_part = o_part;
   fp.lse_part = lse_part;

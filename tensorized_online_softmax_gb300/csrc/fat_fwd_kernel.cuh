@@ -77,6 +77,7 @@ struct FwdParams {
   int X;
   int n_mblocks;           // ceil(Nq / 128)
   int group_heads;         // heads whose query blocks are ordered together
+  int prefetch_stride;     // > 0: prefetch into L2 the first tiles of block + this
   int kv_split_len;        // keys per split (a multiple of 128): blockIdx.y = split
   float* o_part;           // nullable: per-split partial O [splits][B*H][Nq][d] ...
   float* lse_part;         // ... and LSE [splits][B*H][Nq] instead of o / lse
@@ -103,6 +104,19 @@ constexpr int kTraceWords = 5 * 2 * kTraceIters + 2;
 __device__ __forceinline__ void trace_mark(const FwdParams& p, int e, int t, int j, int pass) {
   if (p.trace != nullptr && blockIdx.x == 0 && pass == 0 && j < kTraceIters)
     p.trace[(e * 2 + t) * kTraceIters + j] = static_cast<unsigned long long>(clock64());
+}
+
+// Block idx -> (query block, head).  Heads run a few at a time, as many as
+// keep their K and V in L2 while the query blocks re-read them; within a
+// group, the heaviest causal blocks first.
+__device__ __forceinline__ void fwd_work_item(const FwdParams& p, int idx, int& mblock, int& bh) {
+  const int BH = p.B * p.H;
+  const int per = p.group_heads * p.n_mblocks;
+  const int g = idx / per;
+  const int rem = idx - g * per;
+  const int gh = min(p.group_heads, BH - g * p.group_heads);
+  mblock = p.n_mblocks - 1 - rem / gh;
+  bh = g * p.group_heads + rem % gh;
 }
 
 template <int D, bool kE4M3 = false, bool kZT = false>
@@ -671,19 +685,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
 
   // work item: query block mblock of head bh
   const int BH = p.B * p.H;
-  // (heads run a few at a time, as many as keep their K and V in L2 while
-  // the query blocks re-read them; within a group, the heaviest causal
-  // blocks first)
   int mblock, bh;
-  {
-    const int idx = static_cast<int>(blockIdx.x);
-    const int per = p.group_heads * p.n_mblocks;
-    const int g = idx / per;
-    const int rem = idx - g * per;
-    const int gh = min(p.group_heads, BH - g * p.group_heads);
-    mblock = p.n_mblocks - 1 - rem / gh;
-    bh = g * p.group_heads + rem % gh;
-  }
+  fwd_work_item(p, static_cast<int>(blockIdx.x), mblock, bh);
   const int m0 = mblock * kRowsPerCta;
   // this block's key range: the split's range, cut at the causal limit of
   // its last row
@@ -787,7 +790,20 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
             for (int a = 0; a < L::kAtoms; ++a)
               tma_load_3d(sb + L::kQ + a * 16384, &p.tm_q, bar(L::bQFull), a * L::kAtomCols, m0, bh);
           }
-          if (pass == 0 && !is_k) tma_prefetch_desc(&p.tm_v);
+          if (pass == 0 && !is_k) {
+            tma_prefetch_desc(&p.tm_v);
+            // the block about one wave ahead finds its Q tile and first K
+            // tile in L2 when it starts
+            const int next = static_cast<int>(blockIdx.x) + p.prefetch_stride;
+            if (p.prefetch_stride > 0 && next < static_cast<int>(gridDim.x)) {
+              int mb_n, bh_n;
+              fwd_work_item(p, next, mb_n, bh_n);
+              for (int a = 0; a < L::kAtoms; ++a) {
+                tma_prefetch_l2_3d(&p.tm_q, a * L::kAtomCols, mb_n * kRowsPerCta, bh_n);
+                tma_prefetch_l2_3d(&p.tm_k, a * L::kAtomCols, kv_begin, bh_n);
+              }
+            }
+          }
           for (int jj = 0; jj < n_kv; ++jj) {
             const int it = it0 + jj, st = it % S;
             if (!wait_bounded(bar(empty + st), ((it / S) & 1) ^ 1, p, abort_flag)) break;
