@@ -711,7 +711,12 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
   }
 
   // ---- set-up --------------------------------------------------------------
-  if (threadIdx.x == 0) {
+  // The Q/K producer's first thread initialises the barriers and at once
+  // issues the loads of Q and of the first K tiles, which then overlap the
+  // TMEM allocation and the block-wide sync.
+  const bool init_thread = threadIdx.x == kLoadWarp * 32;
+  int k_pre = 0;  // K tiles of pass 0 issued here (by init_thread)
+  if (init_thread) {
     mbar_init(bar(L::bQFull), 1);
     for (int s = 0; s < SK; ++s) {
       mbar_init(bar(L::bKFull + s), 1);
@@ -735,6 +740,18 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
     misc[1] = 0;
     misc[2] = 0;
     fence_mbar_init();
+    tma_prefetch_desc(&p.tm_q);
+    tma_prefetch_desc(&p.tm_k);
+    mbar_arrive_expect_tx(bar(L::bQFull), L::kTile);
+    for (int a = 0; a < L::kAtoms; ++a)
+      tma_load_3d(sb + L::kQ + a * 16384, &p.tm_q, bar(L::bQFull), a * L::kAtomCols, m0, bh);
+    k_pre = min(SK, n_kv);
+    for (int jj = 0; jj < k_pre; ++jj) {
+      mbar_arrive_expect_tx(bar(L::bKFull + jj), L::kTile);
+      for (int a = 0; a < L::kAtoms; ++a)
+        tma_load_3d(sb + L::kK + jj * L::kTile + a * 16384, &p.tm_k, bar(L::bKFull + jj),
+                    a * L::kAtomCols, kv_begin + jj * kBlockN, bh);
+    }
   }
   if constexpr (kZT) {
     // zero bias tiles (12 KB, a bias of 0 for the first three S tiles) and the
@@ -782,14 +799,9 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
           const int empty = is_k ? L::bKEmpty : (SV == kSBufs ? L::bOReady : L::bVEmpty);
           const int ring = is_k ? L::kK : L::kV;
           const CUtensorMap* tm = is_k ? &p.tm_k : &p.tm_v;
-          int issued = 0;
-          if (pass == 0 && is_k) {
-            tma_prefetch_desc(&p.tm_q);
-            tma_prefetch_desc(&p.tm_k);
-            mbar_arrive_expect_tx(bar(L::bQFull), L::kTile);
-            for (int a = 0; a < L::kAtoms; ++a)
-              tma_load_3d(sb + L::kQ + a * 16384, &p.tm_q, bar(L::bQFull), a * L::kAtomCols, m0, bh);
-          }
+          // (pass 0: Q and the first K tiles were issued during set-up)
+          const int jj0 = (pass == 0 && is_k) ? k_pre : 0;
+          int issued = jj0;
           if (pass == 0 && !is_k) {
             tma_prefetch_desc(&p.tm_v);
             // the block about one wave ahead finds its Q tile and first K
@@ -804,7 +816,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
               }
             }
           }
-          for (int jj = 0; jj < n_kv; ++jj) {
+          for (int jj = jj0; jj < n_kv; ++jj) {
             const int it = it0 + jj, st = it % S;
             if (!wait_bounded(bar(empty + st), ((it / S) & 1) ^ 1, p, abort_flag)) break;
             mbar_arrive_expect_tx(bar(full + st), L::kTile);
