@@ -8,14 +8,17 @@
   identical keys make the weights independent of the query, so dq = 0;
 * the row-sampled form agrees with the full matrices, and the forward
   quantities it returns agree with the C oracle.
-A dropped D term, a wrong sign, a transposed operand or a missing scale each
-breaks the finite-difference check; a dropped D also breaks the key-sum one.
+A mutation test plants mistakes (a dropped D term, a wrong sign of D, a
+missing scale, a transposed operand, P instead of P^T) into a copy of the
+oracle and checks that each fails at least one pin.
 """
+import importlib.util
+
 import numpy as np
 import pytest
 
 import oracle
-from oracle.backward import attn_bwd, attn_bwd_sampled
+import oracle.backward as backward
 
 pytestmark = pytest.mark.filterwarnings("ignore::RuntimeWarning")
 
@@ -29,12 +32,11 @@ def _f(q, k, v, do, causal, scale):
     return float((o * do).sum())
 
 
-@pytest.mark.parametrize("causal", [False, True])
-def test_finite_differences(causal):
+def _check_finite_differences(mod, causal):
     B, H, N, d = 1, 2, 5, 3
     q, k, v, do = (_rand((B, H, N, d), s) for s in (1, 2, 3, 4))
     scale = 0.7
-    dq, dk, dv, _, _ = attn_bwd(q, k, v, do, causal, scale)
+    dq, dk, dv, _, _ = mod.attn_bwd(q, k, v, do, causal, scale)
     h = 1e-6
     for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
         num = np.zeros_like(x)
@@ -50,15 +52,14 @@ def test_finite_differences(causal):
         assert np.abs(num - g).max() <= 1e-7 * max(1.0, np.abs(g).max()), name
 
 
-@pytest.mark.parametrize("causal", [False, True])
-def test_invariants(causal):
+def _check_invariants(mod, causal):
     B, H, N, d = 2, 2, 37, 8
     q, k, v, do = (_rand((B, H, N, d), s) for s in (5, 6, 7, 8))
-    dq, dk, dv, _, _ = attn_bwd(q, k, v, do, causal, 0.35)
+    dq, dk, dv, _, _ = mod.attn_bwd(q, k, v, do, causal, 0.35)
     assert np.abs(dk.sum(axis=2)).max() <= 1e-11 * np.abs(dk).sum(axis=2).max()
     assert np.abs(dv.sum(axis=2) - do.sum(axis=2)).max() <= 1e-11 * np.abs(do).sum()
     k_same = np.broadcast_to(k[:, :, :1], k.shape).copy()
-    dq0, _, _, o, _ = attn_bwd(q, k_same, v, do, causal, 0.35)
+    dq0, _, _, o, _ = mod.attn_bwd(q, k_same, v, do, causal, 0.35)
     assert np.abs(dq0).max() <= 1e-12
     # identical keys: uniform weights over the allowed keys
     counts = np.arange(1, N + 1)[:, None] if causal else np.full((N, 1), N)
@@ -67,17 +68,56 @@ def test_invariants(causal):
     assert np.abs(o - want).max() <= 1e-12
 
 
-@pytest.mark.parametrize("causal", [False, True])
-def test_sampled_matches_full_and_forward_matches_c_oracle(causal):
+def _check_sampled_and_forward(mod, causal):
     B, H, N, d = 1, 1, 300, 16
     q, k, v, do = (_rand((B, H, N, d), s) for s in (9, 10, 11, 12))
     scale = d ** -0.5
-    dq, dk, dv, o, lse = attn_bwd(q, k, v, do, causal, scale)
+    dq, dk, dv, o, lse = mod.attn_bwd(q, k, v, do, causal, scale)
     o_c, lse_c = oracle.attn_fwd(q, k, v, causal, scale)
     assert np.abs(o - o_c).max() <= 1e-12 and np.abs(lse - lse_c).max() <= 1e-12
     rows = [0, 1, 127, 128, 299]
-    sq, sk, sv = attn_bwd_sampled(q[0, 0], k[0, 0], v[0, 0], do[0, 0], causal, scale, rows, rows)
+    sq, sk, sv = mod.attn_bwd_sampled(q[0, 0], k[0, 0], v[0, 0], do[0, 0], causal, scale, rows,
+                                      rows)
     for r in rows:
         assert np.abs(sq[r] - dq[0, 0, r]).max() <= 1e-12
         assert np.abs(sk[r] - dk[0, 0, r]).max() <= 1e-12
         assert np.abs(sv[r] - dv[0, 0, r]).max() <= 1e-12
+
+
+CHECKS = (_check_finite_differences, _check_invariants, _check_sampled_and_forward)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("check", CHECKS, ids=lambda f: f.__name__[len("_check_"):])
+def test_pins(check, causal):
+    check(backward, causal)
+
+
+# planted mistakes: each must fail at least one pin
+MUTANTS = {
+    "dropped_D": ("ds = p * (dp - D[:, None])", "ds = p * dp"),
+    "D_sign": ("ds = p * (dp - D[:, None])", "ds = p * (dp + D[:, None])"),
+    "dq_scale": ("dq[b, h] = scale * (ds @ k[b, h])", "dq[b, h] = (ds @ k[b, h])"),
+    "dk_transposed": ("dk[b, h] = scale * (ds.T @ q[b, h])", "dk[b, h] = scale * (ds @ q[b, h])"),
+    "dv_not_transposed": ("dv[b, h] = p.T @ do[b, h]", "dv[b, h] = p @ do[b, h]"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(backward.__file__).read()
+    assert src.count(old) == 1, f"mutation site for {name} not found"
+    path = tmp_path / "backward_mut.py"
+    path.write_text(src.replace(old, new))
+    spec = importlib.util.spec_from_file_location("backward_mut", str(path))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    failures = 0
+    for check in CHECKS:
+        for causal in (False, True):
+            try:
+                check(mod, causal)
+            except AssertionError:
+                failures += 1
+    assert failures >= 1, f"no pin caught the planted mistake {name}"
