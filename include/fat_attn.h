@@ -183,6 +183,28 @@ int fat_attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, fl
                                  float* lse, int B, int H, int Nq, int Nk, int d, int causal,
                                  float scale, int X, int num_splits, cudaStream_t stream);
 
+/*
+ * fat_attn_fwd on host-resident tensors: q, k, v bf16 [B, H, N, d] and o, lse
+ * fp32 ([B, H, N, d], [B, H, N]) in page-locked host memory.  The problem is
+ * streamed through the device in chunks of heads_per_chunk heads (heads are
+ * independent and contiguous): the copy to the device of one chunk, the
+ * kernel of the previous one and the copy back of the one before overlap on
+ * three internal streams, through two chunk slots in `workspace` (device
+ * memory owned by the caller, at least fat_attn_fwd_host_workspace_bytes(...)
+ * bytes).  Every copy is one cudaMemcpyAsync.  The work starts after what is
+ * already queued on `stream`, and `stream` waits for the last copy back, so
+ * the results are on the host once `stream` has completed.  heads_per_chunk
+ * <= 0 picks about eight chunks.  Calls sharing a workspace, or running on
+ * the same device from several host threads, must not overlap.  No
+ * counterpart on the pages.
+ */
+int fat_attn_fwd_host(const void* q, const void* k, const void* v, float* o, float* lse, int B,
+                      int H, int N, int d, int causal, float scale, int X, int heads_per_chunk,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace size for fat_attn_fwd_host (0 for invalid arguments). */
+size_t fat_attn_fwd_host_workspace_bytes(int B, int H, int N, int d, int heads_per_chunk);
+
 /* Every knob of the entry points above in one struct (tests and ablations). */
 typedef struct fat_params {
   const void* q;

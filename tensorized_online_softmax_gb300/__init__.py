@@ -21,7 +21,7 @@ from . import _build
 
 __all__ = [
     "FatError", "load_library", "attn_fwd", "attn_fwd_vec", "attn_fwd_fp8", "attn_fwd_splitkv",
-    "attn_bwd",
+    "attn_bwd", "attn_fwd_host",
     "check_device_error", "status_string", "ABI_SYMBOLS", "FAT_OK",
     "FAT_ERR_INVALID_ARG", "FAT_ERR_UNSUPPORTED", "FAT_ERR_ALIGNMENT", "FAT_ERR_LAUNCH",
     "FAT_ERR_DEVICE_TIMEOUT", "FAT_ERR_ARCH",
@@ -48,6 +48,7 @@ ABI_SYMBOLS = (
     "fat_attn_splitkv_workspace_bytes", "fat_attn_splitkv_default_splits",
     "fat_attn_fwd_splitkv_noalloc", "fat_attn_fwd_ex",
     "fat_attn_bwd", "fat_attn_bwd_workspace_bytes",
+    "fat_attn_fwd_host", "fat_attn_fwd_host_workspace_bytes",
     "fat_status_string", "fat_check_device_error",
 )
 
@@ -123,6 +124,11 @@ def load_library(build_if_missing: bool = True):
         lib.fat_attn_bwd.restype = I
         lib.fat_attn_bwd_workspace_bytes.argtypes = [I, I, I]
         lib.fat_attn_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.fat_attn_fwd_host.argtypes = [P, P, P, P, P, I, I, I, I, I, F, I, I, P,
+                                          ctypes.c_size_t, P]
+        lib.fat_attn_fwd_host.restype = I
+        lib.fat_attn_fwd_host_workspace_bytes.argtypes = [I, I, I, I, I]
+        lib.fat_attn_fwd_host_workspace_bytes.restype = ctypes.c_size_t
         lib.fat_status_string.argtypes = [I]
         lib.fat_status_string.restype = ctypes.c_char_p
         lib.fat_check_device_error.argtypes = [P]
@@ -313,6 +319,51 @@ def attn_bwd(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = 
     if st != FAT_OK:
         raise FatError(st, "fat_attn_bwd")
     return dq, dk, dv
+
+
+def attn_fwd_host(q, k, v, causal: bool = False, scale: float | None = None, X: int = 64, *,
+                  out=None, workspace=None, heads_per_chunk: int = 0, stream=None, device=None):
+    """Forward pass on host-resident tensors (``fat_attn_fwd_host``).
+
+    ``q, k, v``: contiguous bf16 CPU tensors [B, H, N, d] in page-locked memory
+    (``tensor.pin_memory()``); ``out``: optional page-locked fp32 ``(o, lse)``.
+    The problem is streamed through the device in chunks of heads, the copies
+    overlapping the kernels.  ``workspace`` (a CUDA uint8 tensor) is
+    allocated here if not given.  The call is asynchronous on ``stream``;
+    synchronise it before reading ``o`` and ``lse``.  Returns ``(o, lse)``.
+    """
+    import torch
+
+    lib = load_library()
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if (not isinstance(t, torch.Tensor) or t.is_cuda or t.dtype != torch.bfloat16 or
+                not t.is_pinned()):
+            raise ValueError(f"{name} must be a page-locked bf16 host tensor")
+        if t.dim() != 4 or not t.is_contiguous() or t.shape != q.shape:
+            raise ValueError(f"{name} must be a contiguous [B, H, N, d] tensor")
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = d ** -0.5
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    if out is None:
+        o = torch.empty((B, H, N, d), dtype=torch.float32).pin_memory()
+        lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    else:
+        o, lse = out
+    for name, t, shape in (("o", o, (B, H, N, d)), ("lse", lse, (B, H, N))):
+        if t.is_cuda or t.dtype != torch.float32 or tuple(t.shape) != shape or not t.is_pinned():
+            raise ValueError(f"{name} must be a page-locked fp32 host tensor of shape {shape}")
+    with torch.cuda.device(dev):
+        nbytes = lib.fat_attn_fwd_host_workspace_bytes(B, H, N, d, int(heads_per_chunk))
+        if workspace is None:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        st = lib.fat_attn_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                   lse.data_ptr(), B, H, N, d, int(bool(causal)), float(scale),
+                                   int(X), int(heads_per_chunk), workspace.data_ptr(),
+                                   workspace.numel(), _stream_handle(stream))
+    if st != FAT_OK:
+        raise FatError(st, "fat_attn_fwd_host")
+    return o, lse
 
 
 def check_device_error(stream=None) -> int:

@@ -511,3 +511,147 @@ int fat_attn_bwd(const void* q, const void* k, const void* v, const float* o, co
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Host-resident tensors: chunks of heads through two device slots, the copies
+// in, the kernel and the copies out on three streams of their own
+// ---------------------------------------------------------------------------
+namespace {
+
+struct HostPipe {
+  std::once_flag once;
+  bool ok = false;
+  cudaStream_t s_in = nullptr, s_run = nullptr, s_out = nullptr;
+  cudaEvent_t start = nullptr, end = nullptr;
+  cudaEvent_t in_ready[2] = {}, run_done[2] = {}, slot_free[2] = {};
+  std::mutex mu;
+};
+HostPipe g_pipe[kMaxDevices];
+
+long long host_chunk_heads(long long BH, int heads_per_chunk) {
+  long long c = heads_per_chunk > 0 ? heads_per_chunk : (BH + 7) / 8;
+  if (c < 1) c = 1;
+  return c < BH ? c : BH;
+}
+
+long long align256(long long x) { return (x + 255) / 256 * 256; }
+
+// one slot: q, k, v (bf16), o (fp32), lse (fp32) of `hc` heads, each 256-byte aligned
+long long host_slot_bytes(long long hc, int N, int d) {
+  const long long rows = hc * N;
+  return 3 * align256(rows * d * 2) + align256(rows * d * 4) + align256(rows * 4);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t fat_attn_fwd_host_workspace_bytes(int B, int H, int N, int d, int heads_per_chunk) {
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
+  const long long hc = host_chunk_heads(static_cast<long long>(B) * H, heads_per_chunk);
+  return static_cast<size_t>(2 * host_slot_bytes(hc, N, d) + 256);
+}
+
+int fat_attn_fwd_host(const void* q, const void* k, const void* v, float* o, float* lse, int B,
+                      int H, int N, int d, int causal, float scale, int X, int heads_per_chunk,
+                      void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  // ---- synchronous validation: nothing is queued on failure ----
+  if (!q || !k || !v || !o || !lse || !workspace) return FAT_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || N < 1) return FAT_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return FAT_ERR_INVALID_ARG;
+  if (X != 16 && X != 32 && X != 64 && X != 128) return FAT_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return FAT_ERR_INVALID_ARG;
+  if (workspace_bytes < fat_attn_fwd_host_workspace_bytes(B, H, N, d, heads_per_chunk))
+    return FAT_ERR_INVALID_ARG;
+  int dev = 0;
+  const int arch = check_device(&dev);
+  if (arch != FAT_OK) return arch;
+  HostPipe& hp = g_pipe[dev];
+  std::call_once(hp.once, [&] {
+    bool ok = true;
+    for (cudaStream_t* s : {&hp.s_in, &hp.s_run, &hp.s_out})
+      ok = ok && cudaStreamCreateWithFlags(s, cudaStreamNonBlocking) == cudaSuccess;
+    for (cudaEvent_t* e : {&hp.start, &hp.end, &hp.in_ready[0], &hp.in_ready[1], &hp.run_done[0],
+                           &hp.run_done[1], &hp.slot_free[0], &hp.slot_free[1]})
+      ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
+    hp.ok = ok;
+  });
+  if (!hp.ok) return FAT_ERR_LAUNCH;
+  std::lock_guard<std::mutex> lock(hp.mu);
+
+  const long long BH = static_cast<long long>(B) * H;
+  const long long hc = host_chunk_heads(BH, heads_per_chunk);
+  const long long slot = host_slot_bytes(hc, N, d);
+  const uintptr_t base = (reinterpret_cast<uintptr_t>(workspace) + 255) & ~uintptr_t(255);
+  struct Slot { void *q, *k, *v; float *o, *lse; } sl[2];
+  for (int s = 0; s < 2; ++s) {
+    uint8_t* p = reinterpret_cast<uint8_t*>(base + s * slot);
+    const long long in = align256(hc * N * d * 2);
+    sl[s].q = p;
+    sl[s].k = p + in;
+    sl[s].v = p + 2 * in;
+    sl[s].o = reinterpret_cast<float*>(p + 3 * in);
+    sl[s].lse = reinterpret_cast<float*>(p + 3 * in + align256(hc * N * d * 4));
+  }
+  bool ok = cudaEventRecord(hp.start, stream) == cudaSuccess;
+  for (cudaStream_t s : {hp.s_in, hp.s_run, hp.s_out})
+    ok = ok && cudaStreamWaitEvent(s, hp.start, 0) == cudaSuccess;
+  int st = FAT_OK;
+  const auto* qh = static_cast<const uint8_t*>(q);
+  const auto* kh = static_cast<const uint8_t*>(k);
+  const auto* vh = static_cast<const uint8_t*>(v);
+  for (long long h0 = 0, c = 0; ok && st == FAT_OK && h0 < BH; h0 += hc, ++c) {
+    const int s = static_cast<int>(c & 1);
+    const long long n = hc < BH - h0 ? hc : BH - h0;
+    const size_t in_off = static_cast<size_t>(h0) * N * d * 2, in_bytes = n * N * d * 2;
+    // the slot's previous chunk has been copied out
+    if (c >= 2) ok = ok && cudaStreamWaitEvent(hp.s_in, hp.slot_free[s], 0) == cudaSuccess;
+    ok = ok && cudaMemcpyAsync(sl[s].q, qh + in_off, in_bytes, cudaMemcpyHostToDevice, hp.s_in) ==
+                   cudaSuccess;
+    ok = ok && cudaMemcpyAsync(sl[s].k, kh + in_off, in_bytes, cudaMemcpyHostToDevice, hp.s_in) ==
+                   cudaSuccess;
+    ok = ok && cudaMemcpyAsync(sl[s].v, vh + in_off, in_bytes, cudaMemcpyHostToDevice, hp.s_in) ==
+                   cudaSuccess;
+    ok = ok && cudaEventRecord(hp.in_ready[s], hp.s_in) == cudaSuccess;
+    ok = ok && cudaStreamWaitEvent(hp.s_run, hp.in_ready[s], 0) == cudaSuccess;
+    if (!ok) break;
+    fat_params p = {};
+    p.q = sl[s].q;
+    p.k = sl[s].k;
+    p.v = sl[s].v;
+    p.o = sl[s].o;
+    p.lse = sl[s].lse;
+    p.B = 1;
+    p.H = static_cast<int>(n);
+    p.N = N;
+    p.d = d;
+    p.causal = causal;
+    p.scale = scale;
+    p.X = X;
+    p.variant = FAT_VARIANT_TENSOR;
+    p.dtype = FAT_DTYPE_BF16;
+    p.stream = hp.s_run;
+    st = fat_attn_fwd_ex(&p);
+    ok = ok && cudaEventRecord(hp.run_done[s], hp.s_run) == cudaSuccess;
+    ok = ok && cudaStreamWaitEvent(hp.s_out, hp.run_done[s], 0) == cudaSuccess;
+    if (st != FAT_OK || !ok) break;
+    ok = ok && cudaMemcpyAsync(o + static_cast<size_t>(h0) * N * d, sl[s].o, n * N * d * 4,
+                               cudaMemcpyDeviceToHost, hp.s_out) == cudaSuccess;
+    ok = ok && cudaMemcpyAsync(lse + static_cast<size_t>(h0) * N, sl[s].lse, n * N * 4,
+                               cudaMemcpyDeviceToHost, hp.s_out) == cudaSuccess;
+    ok = ok && cudaEventRecord(hp.slot_free[s], hp.s_out) == cudaSuccess;
+  }
+  // `stream` continues after everything queued above (the copies out wait for
+  // the kernels, which wait for the copies in)
+  for (cudaStream_t s : {hp.s_in, hp.s_run}) {
+    if (cudaEventRecord(hp.end, s) != cudaSuccess || cudaStreamWaitEvent(hp.s_out, hp.end, 0) != cudaSuccess)
+      ok = false;
+  }
+  if (cudaEventRecord(hp.end, hp.s_out) != cudaSuccess ||
+      cudaStreamWaitEvent(stream, hp.end, 0) != cudaSuccess)
+    ok = false;
+  if (st != FAT_OK) return st;
+  return ok ? FAT_OK : FAT_ERR_LAUNCH;
+}
+
+}  // extern "C"
