@@ -189,7 +189,7 @@ int fat_attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, fl
  * streamed through the device in chunks of heads_per_chunk heads (heads are
  * independent and contiguous): the copy to the device of one chunk, the
  * kernel of the previous one and the copy back of the one before overlap on
- * three internal streams, through two chunk slots in `workspace` (device
+ * three internal streams, through three chunk slots in `workspace` (device
  * memory owned by the caller, at least fat_attn_fwd_host_workspace_bytes(...)
  * bytes).  Every copy is one cudaMemcpyAsync.  The work starts after what is
  * already queued on `stream`, and `stream` waits for the last copy back, so

@@ -513,17 +513,21 @@ int fat_attn_bwd(const void* q, const void* k, const void* v, const float* o, co
 }  // extern "C"
 
 // ---------------------------------------------------------------------------
-// Host-resident tensors: chunks of heads through two device slots, the copies
-// in, the kernel and the copies out on three streams of their own
+// Host-resident tensors: chunks of heads through kHostSlots device slots, the
+// copies in, the kernel and the copies out on three streams of their own
 // ---------------------------------------------------------------------------
 namespace {
+
+// (three slots: the copy in of a chunk need not wait for the copy out of the
+// chunk two before it, which the shared link slows while both directions run)
+constexpr int kHostSlots = 3;
 
 struct HostPipe {
   std::once_flag once;
   bool ok = false;
   cudaStream_t s_in = nullptr, s_run = nullptr, s_out = nullptr;
   cudaEvent_t start = nullptr, end = nullptr;
-  cudaEvent_t in_ready[2] = {}, run_done[2] = {}, slot_free[2] = {};
+  cudaEvent_t in_ready[kHostSlots] = {}, run_done[kHostSlots] = {}, slot_free[kHostSlots] = {};
   std::mutex mu;
 };
 HostPipe g_pipe[kMaxDevices];
@@ -549,7 +553,7 @@ extern "C" {
 size_t fat_attn_fwd_host_workspace_bytes(int B, int H, int N, int d, int heads_per_chunk) {
   if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return 0;
   const long long hc = host_chunk_heads(static_cast<long long>(B) * H, heads_per_chunk);
-  return static_cast<size_t>(2 * host_slot_bytes(hc, N, d) + 256);
+  return static_cast<size_t>(kHostSlots * host_slot_bytes(hc, N, d) + 256);
 }
 
 int fat_attn_fwd_host(const void* q, const void* k, const void* v, float* o, float* lse, int B,
@@ -571,9 +575,11 @@ int fat_attn_fwd_host(const void* q, const void* k, const void* v, float* o, flo
     bool ok = true;
     for (cudaStream_t* s : {&hp.s_in, &hp.s_run, &hp.s_out})
       ok = ok && cudaStreamCreateWithFlags(s, cudaStreamNonBlocking) == cudaSuccess;
-    for (cudaEvent_t* e : {&hp.start, &hp.end, &hp.in_ready[0], &hp.in_ready[1], &hp.run_done[0],
-                           &hp.run_done[1], &hp.slot_free[0], &hp.slot_free[1]})
-      ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
+    ok = ok && cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming) == cudaSuccess;
+    ok = ok && cudaEventCreateWithFlags(&hp.end, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; i < kHostSlots; ++i)
+      for (cudaEvent_t* e : {&hp.in_ready[i], &hp.run_done[i], &hp.slot_free[i]})
+        ok = ok && cudaEventCreateWithFlags(e, cudaEventDisableTiming) == cudaSuccess;
     hp.ok = ok;
   });
   if (!hp.ok) return FAT_ERR_LAUNCH;
@@ -583,8 +589,8 @@ int fat_attn_fwd_host(const void* q, const void* k, const void* v, float* o, flo
   const long long hc = host_chunk_heads(BH, heads_per_chunk);
   const long long slot = host_slot_bytes(hc, N, d);
   const uintptr_t base = (reinterpret_cast<uintptr_t>(workspace) + 255) & ~uintptr_t(255);
-  struct Slot { void *q, *k, *v; float *o, *lse; } sl[2];
-  for (int s = 0; s < 2; ++s) {
+  struct Slot { void *q, *k, *v; float *o, *lse; } sl[kHostSlots];
+  for (int s = 0; s < kHostSlots; ++s) {
     uint8_t* p = reinterpret_cast<uint8_t*>(base + s * slot);
     const long long in = align256(hc * N * d * 2);
     sl[s].q = p;
@@ -601,11 +607,12 @@ int fat_attn_fwd_host(const void* q, const void* k, const void* v, float* o, flo
   const auto* kh = static_cast<const uint8_t*>(k);
   const auto* vh = static_cast<const uint8_t*>(v);
   for (long long h0 = 0, c = 0; ok && st == FAT_OK && h0 < BH; h0 += hc, ++c) {
-    const int s = static_cast<int>(c & 1);
+    const int s = static_cast<int>(c % kHostSlots);
     const long long n = hc < BH - h0 ? hc : BH - h0;
     const size_t in_off = static_cast<size_t>(h0) * N * d * 2, in_bytes = n * N * d * 2;
     // the slot's previous chunk has been copied out
-    if (c >= 2) ok = ok && cudaStreamWaitEvent(hp.s_in, hp.slot_free[s], 0) == cudaSuccess;
+    if (c >= kHostSlots)
+      ok = ok && cudaStreamWaitEvent(hp.s_in, hp.slot_free[s], 0) == cudaSuccess;
     ok = ok && cudaMemcpyAsync(sl[s].q, qh + in_off, in_bytes, cudaMemcpyHostToDevice, hp.s_in) ==
                    cudaSuccess;
     ok = ok && cudaMemcpyAsync(sl[s].k, kh + in_off, in_bytes, cudaMemcpyHostToDevice, hp.s_in) ==

@@ -169,10 +169,10 @@ def test_bwd_validation(lib):
 def test_host_entry_validation(lib):
     """fat_attn_fwd_host refuses bad arguments before any device call."""
     ws = lib.fat_attn_fwd_host_workspace_bytes(2, 3, 300, 64, 2)
-    # two slots of 2 heads: q, k, v bf16 + o fp32 + lse fp32, each 256-aligned
+    # three slots of 2 heads: q, k, v bf16 + o fp32 + lse fp32, each 256-aligned
     rows = 2 * 300
     a = lambda x: (x + 255) // 256 * 256
-    assert ws == 2 * (3 * a(rows * 64 * 2) + a(rows * 64 * 4) + a(rows * 4)) + 256
+    assert ws == 3 * (3 * a(rows * 64 * 2) + a(rows * 64 * 4) + a(rows * 4)) + 256
     assert lib.fat_attn_fwd_host_workspace_bytes(2, 3, 300, 96, 2) == 0
     args = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000, B=2, H=3, N=300, d=64,
                 causal=0, scale=0.125, X=64, hc=2, ws=0x6000, wsb=ws)
