@@ -88,6 +88,17 @@ typedef enum { FAT_LMODE_VECTOR = 0, FAT_LMODE_TENSOR = 1 } fat_lmode;
 typedef enum { FAT_ZMODE_VECTOR = 0, FAT_ZMODE_TENSOR = 1 } fat_zmode;
 
 /*
+ * How query tiles (128 rows of one (b, h): the row blocks of the page's
+ * section A3, one per worker) map to thread blocks.  FAT_BLOCKS_AUTO
+ * (default): one thread block per SM takes tiles in turn, so the next tile's
+ * Q and first K tiles load, and its first S tiles run on the tensor pipe,
+ * while the last tile's output is normalised and stored; split-KV calls use
+ * one block per tile.  FAT_BLOCKS_PER_TILE: one thread block per tile, in the
+ * same order (for comparison).  The results are the same either way.
+ */
+typedef enum { FAT_BLOCKS_AUTO = 0, FAT_BLOCKS_PER_TILE = 1 } fat_block_mode;
+
+/*
  * Tensorized online softmax (section A2 of the page above).
  *   - m_hat: per X-row tile, the maximum of the row maxima seen so far
  *     (Algorithm 1 step 1), kept as an integer number of binades so that the
@@ -231,6 +242,7 @@ typedef struct fat_params {
    * long the tensor pipe waits for the softmax (see fat_trace_layout below) */
   unsigned long long* trace;
   int z_mode;                         /* fat_zmode (tensorized variant only) */
+  int block_mode;                     /* fat_block_mode */
 } fat_params;
 
 /*

@@ -38,6 +38,7 @@ FAT_ERR_ARCH = -6
 VARIANTS = {"tensor": 0, "vec": 1}
 DTYPES = {"bf16": 0, "e4m3": 1, "fp16": 2}
 LMODES = {"vector": 0, "tensor": 1}
+BLOCK_MODES = {"auto": 0, "per_tile": 1}
 ZMODES = {"vector": 0, "tensor": 1}
 TRACE_ITERS = 128
 TRACE_WORDS = 5 * 2 * TRACE_ITERS + 2
@@ -77,6 +78,7 @@ class FatParams(ctypes.Structure):
         ("stream", ctypes.c_void_p),
         ("trace", ctypes.c_void_p),
         ("z_mode", ctypes.c_int),
+        ("block_mode", ctypes.c_int),
     ]
 
 
@@ -172,7 +174,8 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, X: int =
              variant: str = "tensor", *, out=None, stream=None, fallback_rows=None,
              underflow_log2_threshold: float = 0.0, wait_poll_limit: int = 0,
              wait_timeout_ns: int = 0, dtype: str = "bf16", descales=(1.0, 1.0, 1.0),
-             l_mode: str = "vector", trace=None, z_mode: str = "vector"):
+             l_mode: str = "vector", trace=None, z_mode: str = "vector",
+             block_mode: str = "auto"):
     """Fused attention forward.  Returns ``(o, lse)`` (fp32 [B,H,N,d], fp32 [B,H,N]).
 
     ``q, k, v``: contiguous CUDA tensors [B, H, N, d] (bf16; fp16 with
@@ -183,6 +186,8 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, X: int =
     ``l_mode="tensor"`` forms the row sum on the tensor pipe (see fat_lmode in
     include/fat_attn.h for its accuracy); ``z_mode="tensor"`` has the S MMA
     subtract a reference offset (fat_zmode: bf16, X = 128, tensorized only).
+    ``block_mode="per_tile"`` launches one thread block per 128-row query tile
+    instead of one per SM taking tiles in turn (fat_block_mode).
     The call is asynchronous on ``stream`` (default: torch's current stream).
     """
     import torch
@@ -210,6 +215,7 @@ def attn_fwd(q, k, v, causal: bool = False, scale: float | None = None, X: int =
     p.dtype = DTYPES[dtype]
     p.l_mode = LMODES[l_mode]
     p.z_mode = ZMODES[z_mode]
+    p.block_mode = BLOCK_MODES[block_mode]
     p.q_descale, p.k_descale, p.v_descale = (float(x) for x in descales)
     p.underflow_log2_threshold = float(underflow_log2_threshold)
     p.fallback_rows = fallback_rows.data_ptr() if fallback_rows is not None else None

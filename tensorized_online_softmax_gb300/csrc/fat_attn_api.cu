@@ -143,6 +143,8 @@ int run_fwd(const fat_params* p, int Nq, int Nk, int splits, void* workspace,
   if (p->l_mode != FAT_LMODE_VECTOR && p->l_mode != FAT_LMODE_TENSOR) return FAT_ERR_INVALID_ARG;
   if (p->z_mode != FAT_ZMODE_VECTOR && p->z_mode != FAT_ZMODE_TENSOR) return FAT_ERR_INVALID_ARG;
   const bool z_tensor = p->z_mode == FAT_ZMODE_TENSOR;
+  if (p->block_mode != FAT_BLOCKS_AUTO && p->block_mode != FAT_BLOCKS_PER_TILE)
+    return FAT_ERR_INVALID_ARG;
   if (z_tensor &&
       (p->variant != FAT_VARIANT_TENSOR || p->X != 128 || p->dtype != FAT_DTYPE_BF16))
     return FAT_ERR_UNSUPPORTED;
@@ -203,6 +205,7 @@ int run_fwd(const fat_params* p, int Nq, int Nk, int splits, void* workspace,
   fp.causal = p->causal ? 1 : 0;
   fp.X = p->X;
   fp.n_mblocks = static_cast<int>(n_mblocks);
+  fp.n_items = static_cast<int>(BH * n_mblocks);
   // block order: groups of heads whose K and V (2 Nk d input bytes each)
   // fill about 48 MiB of L2
   {
@@ -211,11 +214,14 @@ int run_fwd(const fat_params* p, int Nq, int Nk, int splits, void* workspace,
     if (g > BH) g = BH;
     fp.group_heads = static_cast<int>(g);
   }
-  {
-    int sms = 0;
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    fp.prefetch_stride = sms > 0 ? sms : 0;
-  }
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  // One block per SM taking items in turn, or one block per item (split-KV
+  // launches, and on request); the latter prefetches for the block one wave
+  // ahead, the former for its own next item.
+  int grid = fp.n_items;
+  if (p->block_mode == FAT_BLOCKS_AUTO && n_splits == 1 && sms > 0 && sms < grid) grid = sms;
+  fp.prefetch_stride = (grid == fp.n_items && sms > 0) ? sms : 0;
   fp.kv_split_len = kv_split_len;
   fp.o_part = o_part;
   fp.lse_part = lse_part;
@@ -234,7 +240,6 @@ int run_fwd(const fat_params* p, int Nq, int Nk, int splits, void* workspace,
   fp.trace = p->trace;
   fp.error_word = g_dev[dev].error_word;
 
-  const int grid = static_cast<int>(BH * n_mblocks);
   const bool tensor = p->variant == FAT_VARIANT_TENSOR;
   const bool l_tensor = tensor && p->l_mode == FAT_LMODE_TENSOR;
   const int X = tensor ? p->X : 0;  // X = 0: the vector-softmax kernel

@@ -42,6 +42,9 @@ constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;    // Q and K
 constexpr int kLoadVWarp = 10;  // V; warp 11 completes the third warpgroup
 constexpr int kNumThreads = 384;
+// A block takes at most this many items (the host sizes the grid so), which
+// bounds its list of items deferred to the fallback pass.
+constexpr int kMaxDeferred = 64;
 // Register budget: 384 threads launch with kLaunchRegs each; the MMA/TMA
 // warpgroup drops to kCtrlRegs and the two softmax warpgroups rise to
 // kSoftmaxRegs.  256 * kSoftmaxRegs + 128 * kCtrlRegs <= 384 * kLaunchRegs.
@@ -76,6 +79,7 @@ struct FwdParams {
   int causal;              // key j allowed for query i iff j <= i + Nk - Nq
   int X;
   int n_mblocks;           // ceil(Nq / 128)
+  int n_items;             // work items (query tiles) per split: B H n_mblocks
   int group_heads;         // heads whose query blocks are ordered together
   int prefetch_stride;     // > 0: prefetch into L2 the first tiles of block + this
   int kv_split_len;        // keys per split (a multiple of 128): blockIdx.y = split
@@ -91,7 +95,8 @@ struct FwdParams {
   unsigned int* error_word;   // device error word: bit 0 = a bounded wait ran out
 };
 
-// Phase trace of CTA 0, SM clock (clock64) stamps, pass 0 only:
+// Phase trace of CTA 0, SM clock (clock64) stamps, its first item's first
+// pass only:
 //   word (e * 2 + t) * kTraceIters + j for event e, K/V tile j, and t = the
 //   softmax set that takes tile j (softmax events, written by warps 0 and
 //   4) or 0 (MMA):
@@ -101,12 +106,12 @@ struct FwdParams {
 constexpr int kTraceIters = 128;
 constexpr int kTraceWords = 5 * 2 * kTraceIters + 2;
 
-__device__ __forceinline__ void trace_mark(const FwdParams& p, int e, int t, int j, int pass) {
-  if (p.trace != nullptr && blockIdx.x == 0 && pass == 0 && j < kTraceIters)
+__device__ __forceinline__ void trace_mark(const FwdParams& p, int e, int t, int j, bool on) {
+  if (on && p.trace != nullptr && blockIdx.x == 0 && j < kTraceIters)
     p.trace[(e * 2 + t) * kTraceIters + j] = static_cast<unsigned long long>(clock64());
 }
 
-// Block idx -> (query block, head).  Heads run a few at a time, as many as
+// Item idx -> (query block, head).  Heads run a few at a time, as many as
 // keep their K and V in L2 while the query blocks re-read them; within a
 // group, the heaviest causal blocks first.
 __device__ __forceinline__ void fwd_work_item(const FwdParams& p, int idx, int& mblock, int& bh) {
@@ -117,6 +122,17 @@ __device__ __forceinline__ void fwd_work_item(const FwdParams& p, int idx, int& 
   const int gh = min(p.group_heads, BH - g * p.group_heads);
   mblock = p.n_mblocks - 1 - rem / gh;
   bh = g * p.group_heads + rem % gh;
+}
+
+// The k-th item of this block, or -1 past the end.  Blocks take items in
+// strides of gridDim.x, in alternating direction (0 1 2 .. G-1, then 2G-1
+// .. G), so that within an L2 group (costs falling along the list) a block
+// with a heavy item in one stride gets a light one in the next.  With one
+// block per item (gridDim.x == n_items) this is just blockIdx.x.
+__device__ __forceinline__ int fwd_item_at(const FwdParams& p, int k) {
+  const int G = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
+  const int idx = k * G + ((k & 1) ? G - 1 - b : b);
+  return idx < p.n_items ? idx : -1;
 }
 
 template <int D, bool kE4M3 = false, bool kZT = false>
@@ -158,15 +174,29 @@ struct Smem {
   static constexpr int bOFinal = bOReady + kSBufs;
   static constexpr int bDrain = bOFinal + 1;
   static constexpr int bMReady = bDrain + 1;         // [2 sets], 4 arrivals: offset published
-  static constexpr int kNumBars = bMReady + 2;
+  // a block runs several work items (query tiles) in turn:
+  static constexpr int bQFree = bMReady + 2;         // every S MMA of an item has read Q
+  static constexpr int bOFree = bQFree + 1;          // 8 arrivals: the epilogue has read O
+  static constexpr int bDecided = bOFree + 1;        // 4 arrivals: set 0's detector done
+  static constexpr int bStageFree = bDecided + 1;    // 2 arrivals: O staging read by TMA
+  static constexpr int bListReady = bStageFree + 1;  // once: every first pass detected
+  static constexpr int kNumBars = bListReady + 1;
   static constexpr int kRed = (kBars + 8 * kNumBars + 15) & ~15;  // float [2 sets][2 parity][4 warps]
   static constexpr int kMRow = kRed + 64;            // float [2 sets][128 rows]: offsets
-  static constexpr int kFin = kMRow + 1024;          // float [4][2 sets][128 rows]
-  // u32: tmem base, abort, redo, -, then (kZT) as floats the bias held by
-  // each score buffer's bias tile [3]
-  static constexpr int kMisc = kFin + 4096;
-  static constexpr int kBytes = kMisc + 64;
+  static constexpr int kFin = kMRow + 1024;          // float [2 epilogues][4][2 sets][128 rows]
+  // u32: tmem base, abort, deferred count, last flagged item + 1, then (kZT)
+  // as floats the bias held by each score buffer's bias tile [3]
+  static constexpr int kMisc = kFin + 8192;
+  static constexpr int kDefer = kMisc + 64;          // int [kMaxDeferred]: flagged items
+  static constexpr int kBytes = kDefer + 4 * kMaxDeferred;
   static constexpr int kAlloc = kBytes + 1024;       // slack for 1024-byte alignment
+  // The epilogue stages O (fp32, 128 x D) in the V ring when it fits there,
+  // so that the next item's Q and K tiles can load meanwhile; otherwise from
+  // the start of the K ring (which then waits for the staging as well).
+  static constexpr int kStageBytes = kBlockM * D * 4;
+  static constexpr bool kStageInK = kVStages * kTile < kStageBytes;
+  static constexpr int kStage = kStageInK ? kK : kV;
+  static_assert(kStage + kStageBytes <= kOnes, "O staging overlaps the ones tile");
   static_assert(kK % 1024 == 0 && kV % 1024 == 0 && kOnes % 1024 == 0, "tiles 1 KB aligned");
   static_assert(kAlloc <= 227 * 1024, "shared memory budget");
 };
@@ -217,16 +247,28 @@ __device__ __forceinline__ float f16_round(float x) { return __half2float(__floa
 // and one mbarrier per set.
 //   kX > 0   tensorized online softmax with the surrogate maximum over kX-row
 //            tiles (X is a compile-time constant so no runtime branching sits
-//            in the hot loop); `exact` (the fallback pass) uses each row's own
+//            in the hot loop); kExact (the fallback pass) uses each row's own
 //            maximum instead, rounded up to a whole binade.
 //   kX == 0  the vector-softmax ablation: exact per-row maximum.
+//
+// One call covers one pass over one item (item idx, the seq-th of the
+// block).  it0: the block's K/V tiles before this pass (all ring and buffer
+// phases count from the block's start); epi: the block's passes before this
+// one (phases of the once-per-pass barriers); mr_other: the other set's
+// tiles before this pass (phases of its offset barrier); tr: stamp the phase
+// trace.  In a first pass (not kExact) set 0 runs the detector and appends a
+// flagged item to the block's deferred list, which gets its fallback pass
+// after the block's last item.  Returns true when the block must stop (a
+// bounded wait ran out somewhere); all eight warps return the same value.
 // ---------------------------------------------------------------------------
-template <int D, int kX, bool kLTensor, int kDt, bool kZT>
-__device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, uint32_t sb,
+constexpr uint32_t kBarSoftmax = 11;  // all eight softmax warps
+
+template <int D, int kX, bool kLTensor, int kDt, bool kZT, bool kExact>
+__device__ __forceinline__ bool softmax_role(const FwdParams& p, uint8_t* smem, uint32_t sb,
                                              uint32_t tmem, volatile uint32_t* misc, int warp,
-                                             int lane, int m0, int bh, int n_kv, int it0,
-                                             int pass, bool exact, int split, int kv_begin,
-                                             int kv_end, int kv_off) {
+                                             int lane, int idx, int seq, int m0, int bh, int n_kv,
+                                             int it0, int split, int kv_begin, int kv_end,
+                                             int kv_off, int epi, int mr_other, bool tr) {
   constexpr bool kE4M3 = kDt == kDtE4M3;
   using L = Smem<D, kE4M3, kZT>;
   constexpr bool kTensor = kX > 0;
@@ -247,17 +289,17 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
   const float c = p.c;
   float* red = reinterpret_cast<float*>(smem + L::kRed);    // [2 sets][2 parity][4 warps]
   float* mrow = reinterpret_cast<float*>(smem + L::kMRow);  // [2 sets][128 rows]
-  float* fin = reinterpret_cast<float*>(smem + L::kFin);    // [4][2 sets][128 rows]
+  // [4][2 sets][128 rows], one copy per parity of epi (the other set may
+  // still read the previous pass's values)
+  float* fin = reinterpret_cast<float*>(smem + L::kFin) + (epi & 1) * (4 * 2 * kBlockM);
   // (kZT) the bias b held by each score buffer's bias tile, in raw score units
   volatile float* zvals = reinterpret_cast<volatile float*>(misc + 4);
   // Warps of the set that share a surrogate maximum: none besides this one
   // for X <= 32, the fallback pass and the vector variant; two for X = 64,
   // the set's four for X = 128.
-  const bool solo = kX <= 32 || exact;
+  constexpr bool solo = kX <= 32 || kExact;
   const uint32_t gbar_id = kX == 64 ? kBarGroup + set * 2 + (q >> 1) : kBarSet + set;
   const uint32_t gbar_n = kX == 64 ? 64 : 128;
-  // the other set's tiles in one pass (completions of its offset barrier)
-  const int n_other = other == 0 ? (n_kv + 1) / 2 : n_kv / 2;
 
   float M = -INFINITY;    // offset of this set's latest tile (per row; uniform over
                           // the X-row group in the surrogate modes), binades
@@ -289,7 +331,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     if (jj == 0) return -INFINITY;
     const int kk = (jj - 1) / 2;  // the other set's tile count
     if (!__all_sync(0xffffffffu, wait_bounded(bar(L::bMReady + other),
-                                              (pass * n_other + kk) & 1, p, abort_flag))) {
+                                              (mr_other + kk) & 1, p, abort_flag))) {
       dead = true;
       return -INFINITY;
     }
@@ -308,7 +350,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     const uint32_t s_taddr = tmem + lane_base + buf * kBlockN;
     dead = !__all_sync(0xffffffffu,
                        wait_bounded(bar(L::bSFull + buf), (it / kSBufs) & 1, p, abort_flag));
-    if (q == 0 && lane == 0) trace_mark(p, 0, set, j, pass);
+    if (q == 0 && lane == 0) trace_mark(p, 0, set, j, tr);
     uint32_t s[4][32];
     float rowmax = -INFINITY;
     int limit = kBlockN;  // keys of this K/V tile the row may see
@@ -413,7 +455,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
         tmax -= zb;
         m_row = fmaxf(m_row, rowmax);
       }
-      const float gm = (exact || !kTensor) ? rowmax : tmax;
+      const float gm = (kExact || !kTensor) ? rowmax : tmax;
       if constexpr (kTensor) {
         M_new = fmaxf(M_prev, (gm == -INFINITY) ? -INFINITY : ceilf(gm * c));
       } else {
@@ -439,7 +481,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
         if (q == 0 && lane == 0) zvals[buf] = bz;
       }
     }
-    if (q == 0 && lane == 0) trace_mark(p, 1, set, j, pass);
+    if (q == 0 && lane == 0) trace_mark(p, 1, set, j, tr);
     const float neg_E = (M_new == -INFINITY) ? 0.f : -M_new;
     // step 7 on the tensor pipe: the row sum of this set's previous tile
     // (relative to that tile's offset M), taken before the exponentials and
@@ -542,7 +584,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     tmem_wait_st();
     tc_fence_before();
     __syncwarp();
-    if (q == 0 && lane == 0) trace_mark(p, 2, set, j, pass);
+    if (q == 0 && lane == 0) trace_mark(p, 2, set, j, tr);
     // a warp that gave up still signals; the MMA issuer sees the abort flag
     if (lane == 0) mbar_arrive(bar(L::bPFull + buf));
     if (dead) break;
@@ -561,7 +603,7 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
   }
 
   bool ok = !dead;
-  if (ok) ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bOFinal), pass & 1, p, abort_flag));
+  if (ok) ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bOFinal), epi & 1, p, abort_flag));
   if (ok && kLTensor && rs_pending >= 0) ok = take_row_sum(rs_pending);
   // combine the two sets' parts of every row (both warps of a pair get here)
   fin[(0 * 2 + set) * kBlockM + r] = m_row;
@@ -579,30 +621,53 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
   const float f_o = (M_o == -INFINITY) ? 0.f : ex2_approx(M_o - M_fin);
   const float l_full = l * f_me + l_o * f_o;
   const float delta_full = delta * f_me + d_o * f_o;
-  if (ok) {
-    tc_fence_after();
-    // detector for the all-underflow case: surrogate far above the exact
-    // maximum, or nothing left of the row sum (counted once per row)
-    if (kTensor && pass == 0 && set == 0) {
+  if (set == 0) {
+    // Detector for the all-underflow case (first pass of the tensorized
+    // softmax): surrogate far above the exact maximum, or nothing left of
+    // the row sum; flagged rows counted once.  The first warp of set 0 to
+    // flag a row puts the item on the block's deferred list (the atomic
+    // maximum over seq + 1 lets exactly one warp per item through).  Then
+    // each warp of set 0 arrives on the detector barrier, which every role
+    // waits for before it reads the list, and (kZT) the MMA issuer before
+    // the next S tiles -- so that is also where the bias tiles go back to
+    // zero: every S MMA of this pass has completed (O final came after the
+    // last one).
+    bool flagged = false;
+    if (kTensor && !kExact && ok) {
       // (a row with no key in this split's range is empty, not flagged)
-      const bool flagged = row_g < p.Nq && m_full != -INFINITY &&
-                           (!(l_full > 0.f) || (M_fin - m_full * c) > p.underflow_thresh);
-      const uint32_t ball = __ballot_sync(0xffffffffu, flagged);
-      if (ball != 0 && lane == 0) {
-        atomicOr(const_cast<uint32_t*>(misc + 2), 1u);
-        if (p.fallback_rows) atomicAdd(p.fallback_rows, __popc(ball));
+      flagged = row_g < p.Nq && m_full != -INFINITY &&
+                (!(l_full > 0.f) || (M_fin - m_full * c) > p.underflow_thresh);
+    }
+    const uint32_t ball = __ballot_sync(0xffffffffu, flagged);
+    if (ball != 0 && lane == 0) {
+      if (p.fallback_rows) atomicAdd(p.fallback_rows, __popc(ball));
+      uint32_t* m = const_cast<uint32_t*>(misc);
+      if (atomicMax(m + 3, static_cast<uint32_t>(seq + 1)) < static_cast<uint32_t>(seq + 1)) {
+        const uint32_t k = atomicAdd(m + 2, 1u);
+        if (k < kMaxDeferred) reinterpret_cast<volatile int*>(smem + L::kDefer)[k] = idx;
       }
     }
+    if constexpr (kZT) {
+      for (int i = r; i < 3 * 4096 / 16; i += kBlockM)
+        st_shared_v4u(sb + L::kZBias + 16 * i, 0u, 0u, 0u, 0u);
+      if (r < kSBufs) zvals[r] = 0.f;
+      fence_async_shared();
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(L::bDecided));
+  }
+  if (ok) {
+    tc_fence_after();
     // epilogue: O / l, this set's half of the columns, staged in shared
-    // memory (the K ring, idle now) as 128-byte-swizzled boxes of 32 columns
-    // x 128 rows for the TMA store below
+    // memory as 128-byte-swizzled boxes of 32 columns x 128 rows for the TMA
+    // store below
     const float inv_l = l_full > 0.f ? p.v_scale / l_full : 0.f;  // an empty row gets O = 0
 #pragma unroll
     for (int k = 0; k < kHalfD / 32; ++k) {
       uint32_t ov[32];
       tmem_ld32(o_taddr + set * kHalfD + 32 * k, ov);
       tmem_wait_ld(ov);
-      const uint32_t box = sb + L::kK + (set * (kHalfD / 32) + k) * 16384 + r * 128;
+      const uint32_t box = sb + L::kStage + (set * (kHalfD / 32) + k) * 16384 + r * 128;
       if (row_g < p.Nq) {  // (rows past N_q are clipped by the store anyway)
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc)
@@ -612,6 +677,12 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
                        __uint_as_float(ov[4 * cc + 3]) * inv_l);
       }
     }
+  }
+  // O has been read: the next pass's (or item's) first O = P V may overwrite it
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar(L::bOFree));
+  if (ok) {
     fence_async_shared();
     if (row_g < p.Nq && set == 0) {
       const size_t out_row = (static_cast<size_t>(split) * (p.B * p.H) + bh) * p.Nq + row_g;
@@ -621,32 +692,34 @@ __device__ __forceinline__ void softmax_role(const FwdParams& p, uint8_t* smem, 
     }
   }
   // One thread of the set stores its boxes once all four warps have staged
-  // their rows (rows past N_q are clipped by the tensor map) and waits until
-  // the copy has read shared memory, which a second pass would reuse.  Every
-  // warp of the set joins this barrier; a warp that gave up vetoes the store.
+  // their rows (rows past N_q are clipped by the tensor map), waits until the
+  // copy has read shared memory and signals that the staging area is free
+  // (the producer whose ring it overlaps waits for that).  Every warp of the
+  // set joins this barrier; a warp that gave up vetoes the store.
   const bool veto = named_bar_or(kBarSet + set, 128, !ok);
-  if (!veto && q == 0 && lane == 0) {
-    const int row_block = p.o_part ? split * (p.B * p.H) + bh : bh;
+  if (q == 0 && lane == 0) {
+    if (!veto) {
+      const int row_block = p.o_part ? split * (p.B * p.H) + bh : bh;
+      // (fallback pass: the first pass's store of this tile, long since
+      // issued by this thread, must have landed before this one overwrites
+      // it)
+      if constexpr (kExact) bulk_wait_all();
 #pragma unroll
-    for (int k = 0; k < kHalfD / 32; ++k) {
-      const int b = set * (kHalfD / 32) + k;
-      tma_store_3d(&p.tm_o, sb + L::kK + b * 16384, b * 32, m0, row_block);
+      for (int k = 0; k < kHalfD / 32; ++k) {
+        const int b = set * (kHalfD / 32) + k;
+        tma_store_3d(&p.tm_o, sb + L::kStage + b * 16384, b * 32, m0, row_block);
+      }
+      bulk_commit();
+      bulk_wait_read();
     }
-    bulk_commit();
-    bulk_wait_read();
+    mbar_arrive(bar(L::bStageFree));
   }
-  if (kZT && pass == 0) {
-    // the fallback pass (if any) starts from zero bias tiles; every S MMA of
-    // this pass has completed (O final was signalled after the last one)
-    const int t = warp * 32 + lane;
-    for (int i = t; i < 3 * 4096 / 16; i += kSoftmaxWarps * 32)
-      st_shared_v4u(sb + L::kZBias + 16 * i, 0u, 0u, 0u, 0u);
-    if (t < kSBufs) zvals[t] = 0.f;
-    fence_async_shared();
-  }
-  if (r == 0 && set == 0 && pass == 0 && p.trace != nullptr && blockIdx.x == 0)
+  if (tr && r == 0 && set == 0 && p.trace != nullptr && blockIdx.x == 0)
     p.trace[kTraceWords - 1] = static_cast<unsigned long long>(clock64());
   tc_fence_before();
+  // all eight warps take the same way on: stop if any warp (or any wait
+  // anywhere in the block) gave up
+  return named_bar_or(kBarSoftmax, kSoftmaxWarps * 32, !ok || *abort_flag != 0u);
 }
 
 // ---------------------------------------------------------------------------
@@ -683,19 +756,28 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
   volatile uint32_t* abort_flag = misc + 1;
   auto bar = [&](int i) -> uint32_t { return sb + L::kBars + 8 * i; };
 
-  // work item: query block mblock of head bh
+  // This block's key range is the split's; a work item is one query tile
+  // (mblock) of one head (bh), with the split's keys cut at the causal limit
+  // of the tile's last row.
   const int BH = p.B * p.H;
-  int mblock, bh;
-  fwd_work_item(p, static_cast<int>(blockIdx.x), mblock, bh);
-  const int m0 = mblock * kRowsPerCta;
-  // this block's key range: the split's range, cut at the causal limit of
-  // its last row
   const int split = static_cast<int>(blockIdx.y);
   const int kv_begin = split * p.kv_split_len;
   const int kv_end = min(p.Nk, kv_begin + p.kv_split_len);
   const int kv_off = p.Nk - p.Nq;
-  const int kv_hi = p.causal ? min(kv_end, m0 + kRowsPerCta + kv_off) : kv_end;
-  const int n_kv = kv_hi > kv_begin ? (kv_hi - kv_begin + kBlockN - 1) / kBlockN : 0;
+  struct Item {
+    int m0, bh, n_kv;
+  };
+  auto item = [&](int idx) -> Item {
+    int mblock, bh;
+    fwd_work_item(p, idx, mblock, bh);
+    const int m0 = mblock * kRowsPerCta;
+    const int kv_hi = p.causal ? min(kv_end, m0 + kRowsPerCta + kv_off) : kv_end;
+    return {m0, bh, kv_hi > kv_begin ? (kv_hi - kv_begin + kBlockN - 1) / kBlockN : 0};
+  };
+  // (the launch never has more blocks than items; only a split can leave an
+  // item without keys, and a split launch gives each block one item)
+  const Item first = item(fwd_item_at(p, 0));
+  const int m0 = first.m0, bh = first.bh, n_kv = first.n_kv;
   if (n_kv == 0) {
     // no key of this split reaches these rows (split-KV, causal): an empty
     // partial result that the combine step weighs by zero
@@ -712,8 +794,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
 
   // ---- set-up --------------------------------------------------------------
   // The Q/K producer's first thread initialises the barriers and at once
-  // issues the loads of Q and of the first K tiles, which then overlap the
-  // TMEM allocation and the block-wide sync.
+  // issues the loads of the first item's Q and first K tiles, which then
+  // overlap the TMEM allocation and the block-wide sync.
   const bool init_thread = threadIdx.x == kLoadWarp * 32;
   int k_pre = 0;  // K tiles of pass 0 issued here (by init_thread)
   if (init_thread) {
@@ -737,8 +819,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
     mbar_init(bar(L::bDrain), 1);
     mbar_init(bar(L::bMReady + 0), kSoftmaxWarps / 2);
     mbar_init(bar(L::bMReady + 1), kSoftmaxWarps / 2);
+    mbar_init(bar(L::bQFree), 1);
+    mbar_init(bar(L::bOFree), kSoftmaxWarps);
+    mbar_init(bar(L::bDecided), kSoftmaxWarps / 2);
+    mbar_init(bar(L::bStageFree), 2);
+    mbar_init(bar(L::bListReady), 1);
     misc[1] = 0;
     misc[2] = 0;
+    misc[3] = 0;
     fence_mbar_init();
     tma_prefetch_desc(&p.tm_q);
     tma_prefetch_desc(&p.tm_k);
@@ -781,143 +869,219 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
     p.trace[kTraceWords - 2] = static_cast<unsigned long long>(clock64());
 
   // Registers: the control warpgroup (TMA, MMA) gives registers back and the
-  // softmax warpgroups take them.  Each role runs its own loop over the
-  // passes so that no code is shared between the two register budgets.
+  // softmax warpgroups take them.  Each role runs its own loops so that no
+  // code is shared between the two register budgets.  Every role walks the
+  // same sequence: the block's items (first passes), then the items its
+  // detector deferred (fallback passes); they count items (seq), tiles and
+  // passes from the block's start, so ring slots and barrier phases carry on
+  // from one item to the next.  Between items the roles meet only through
+  // mbarriers: "Q read" (the last S MMA of an item has completed) before the
+  // next Q, "O read" before the next first O = P V, "staging read" before the
+  // ring that holds the staged O is refilled -- so the next item's Q, first K
+  // tiles and first S tiles load and run while the softmax warps finish the
+  // last item's epilogue -- and, once, "list ready" before the deferred
+  // items.
+  const volatile int* deferred = reinterpret_cast<const volatile int*>(smem + L::kDefer);
   if (warp >= kMmaWarp) {
     regs_dec<kCtrlRegs>();
-    for (int pass = 0; pass < 2; ++pass) {
-      const int it0 = pass * n_kv;
-      if (warp == kLoadWarp || warp == kLoadVWarp) {
-        // =================== TMA producers ===================
-        // warp 9: Q, then K_0, K_1, ...; warp 10: V_0, V_1, ...
-        if (lane == 0) {
-          const bool is_k = warp == kLoadWarp;
-          const int S = is_k ? SK : SV;
-          const int full = is_k ? L::bKFull : L::bVFull;
-          // with as many V stages as score buffers, "V stage free" and "O +=
-          // P V landed" are the same event: one barrier serves both
-          const int empty = is_k ? L::bKEmpty : (SV == kSBufs ? L::bOReady : L::bVEmpty);
-          const int ring = is_k ? L::kK : L::kV;
-          const CUtensorMap* tm = is_k ? &p.tm_k : &p.tm_v;
-          // (pass 0: Q and the first K tiles were issued during set-up)
-          const int jj0 = (pass == 0 && is_k) ? k_pre : 0;
-          int issued = jj0;
-          if (pass == 0 && !is_k) {
-            tma_prefetch_desc(&p.tm_v);
-            // the block about one wave ahead finds its Q tile and first K
-            // tile in L2 when it starts
-            const int next = static_cast<int>(blockIdx.x) + p.prefetch_stride;
-            if (p.prefetch_stride > 0 && next < static_cast<int>(gridDim.x)) {
-              int mb_n, bh_n;
-              fwd_work_item(p, next, mb_n, bh_n);
-              for (int a = 0; a < L::kAtoms; ++a) {
-                tma_prefetch_l2_3d(&p.tm_q, a * L::kAtomCols, mb_n * kRowsPerCta, bh_n);
-                tma_prefetch_l2_3d(&p.tm_k, a * L::kAtomCols, kv_begin, bh_n);
+    if (warp == kLoadWarp || warp == kLoadVWarp) {
+      // =================== TMA producers ===================
+      // warp 9: Q, then K_0, K_1, ... of each item; warp 10: V_0, V_1, ...
+      if (lane == 0) {
+        const bool is_k = warp == kLoadWarp;
+        const int S = is_k ? SK : SV;
+        const int full = is_k ? L::bKFull : L::bVFull;
+        // with as many V stages as score buffers, "V stage free" and "O +=
+        // P V landed" are the same event: one barrier serves both
+        const int empty = is_k ? L::bKEmpty : (SV == kSBufs ? L::bOReady : L::bVEmpty);
+        const int ring = is_k ? L::kK : L::kV;
+        const CUtensorMap* tm = is_k ? &p.tm_k : &p.tm_v;
+        // the ring that holds the staged O of the last pass refills only once
+        // that has been read
+        const bool waits_stage = !is_k || L::kStageInK;
+        int issued = is_k ? k_pre : 0;  // tiles issued (the first K tiles during set-up)
+        int q_issued = 1;               // Q tiles issued (the first during set-up)
+        int seq = 0, it_base = 0;
+        bool ok = true;
+        if (!is_k) tma_prefetch_desc(&p.tm_v);
+#pragma unroll 1
+        for (int phase = 0; phase < 2 && ok; ++phase) {
+          int count = 0;
+          if (phase == 1) {
+            if (!(ok = wait_bounded(bar(L::bListReady), 0, p, abort_flag))) break;
+            count = min(static_cast<int>(misc[2]), kMaxDeferred);
+          }
+#pragma unroll 1
+          for (int k = 0; ok; ++k, ++seq) {
+            const int idx = phase == 0 ? fwd_item_at(p, k) : (k < count ? deferred[k] : -1);
+            if (idx < 0) break;
+            const Item w = item(idx);
+            if (is_k && seq > 0) {
+              // this item's Q, once every S MMA of the last item has read its Q
+              if (!(ok = wait_bounded(bar(L::bQFree), (seq - 1) & 1, p, abort_flag))) break;
+              mbar_arrive_expect_tx(bar(L::bQFull), L::kTile);
+              for (int a = 0; a < L::kAtoms; ++a)
+                tma_load_3d(sb + L::kQ + a * 16384, &p.tm_q, bar(L::bQFull), a * L::kAtomCols,
+                            w.m0, w.bh);
+              ++q_issued;
+            }
+            if (!is_k && phase == 0) {
+              // into L2 ahead of time: the Q tile and first K tile of this
+              // block's next item, or (one block per item) of the block about
+              // one wave ahead
+              int nxt = fwd_item_at(p, k + 1);
+              if (nxt < 0 && k == 0 && p.prefetch_stride > 0 &&
+                  static_cast<int>(blockIdx.x) + p.prefetch_stride < p.n_items)
+                nxt = static_cast<int>(blockIdx.x) + p.prefetch_stride;
+              if (nxt >= 0) {
+                const Item n = item(nxt);
+                for (int a = 0; a < L::kAtoms; ++a) {
+                  tma_prefetch_l2_3d(&p.tm_q, a * L::kAtomCols, n.m0, n.bh);
+                  tma_prefetch_l2_3d(&p.tm_k, a * L::kAtomCols, kv_begin, n.bh);
+                }
               }
             }
-          }
-          for (int jj = jj0; jj < n_kv; ++jj) {
-            const int it = it0 + jj, st = it % S;
-            if (!wait_bounded(bar(empty + st), ((it / S) & 1) ^ 1, p, abort_flag)) break;
-            mbar_arrive_expect_tx(bar(full + st), L::kTile);
-            for (int a = 0; a < L::kAtoms; ++a)
-              tma_load_3d(sb + ring + st * L::kTile + a * 16384, tm, bar(full + st),
-                          a * L::kAtomCols, kv_begin + jj * kBlockN, bh);
-            issued = jj + 1;
-          }
-          if (*abort_flag) {
-            // let every copy already issued land before the CTA can exit
-            if (pass == 0 && is_k) wait_drain(bar(L::bQFull), 0);
-            for (int jj = max(0, issued - S); jj < issued; ++jj)
-              wait_drain(bar(full + (it0 + jj) % S), ((it0 + jj) / S) & 1);
+            if (waits_stage && seq > 0 &&
+                !(ok = wait_bounded(bar(L::bStageFree), (seq - 1) & 1, p, abort_flag)))
+              break;
+            for (int jj = issued - it_base; jj < w.n_kv; ++jj) {
+              const int it = it_base + jj, st = it % S;
+              if (!(ok = wait_bounded(bar(empty + st), ((it / S) & 1) ^ 1, p, abort_flag))) break;
+              mbar_arrive_expect_tx(bar(full + st), L::kTile);
+              for (int a = 0; a < L::kAtoms; ++a)
+                tma_load_3d(sb + ring + st * L::kTile + a * 16384, tm, bar(full + st),
+                            a * L::kAtomCols, kv_begin + jj * kBlockN, w.bh);
+              issued = it + 1;
+            }
+            if (!ok) break;
+            it_base += w.n_kv;
           }
         }
-        __syncwarp();
-      } else if (warp == kMmaWarp) {
-        // =================== MMA issuer ===================
-        // The whole warp runs this code with warp-uniform values; one elected
-        // lane issues each MMA and commit.
-        {
-          // A/B format codes: bf16 1; fp16 0 (kind::f16); e4m3 0 (kind::f8f6f4)
-          constexpr uint32_t kFmt = kDt == kDtBf16 ? 1u : 0u;
-          constexpr uint32_t idesc_s = idesc_f32acc<kFmt>(kBlockM, kBlockN, false);
-          constexpr uint32_t idesc_pv = idesc_f32acc<kFmt>(kBlockM, D, true);
-          constexpr uint32_t idesc_rs = idesc_f32acc<kFmt>(kBlockM, 16, false);
-          const uint64_t ones_desc = sdesc_sw128(sb + L::kOnes, 16, 1024);
-          bool ok = true;
-          // S_it = Q K^T into score buffer it % 3
-          // Descriptors of the first K step of each operand; a step further
-          // only adds its byte offset >> 4 to the start-address field (shared
-          // memory stays below 256 KB, so the field never overflows).
-          const uint64_t q_desc = sdesc_sw128(sb + L::kQ, 16, 1024);
-          const uint64_t k_desc = sdesc_sw128(sb + L::kK, 16, 1024);
-          const uint64_t v_desc = sdesc_sw128(sb + L::kV, 16384, 1024);
-          // (kZT) bias and ones tiles: 16-byte core matrices 128 B apart along
-          // K, 8-row groups 256 B apart; every entry of a tile is equal, so
-          // only the tile's 4 KB extent matters
-          const uint64_t zbias_desc = sdesc_plain(sb + L::kZBias, 128, 256);
-          const uint64_t zones_desc = sdesc_plain(sb + L::kZOnes, 128, 256);
-          auto issue_s = [&](int it) {
-            const uint64_t kd = k_desc + static_cast<uint32_t>(((it % SK) * L::kTile) >> 4);
-            const uint32_t d_t = tmem + (it % kSBufs) * kBlockN;
-  #pragma unroll
-            for (int kk = 0; kk < D / L::kMmaK; ++kk) {
-              // each 128-byte slab row holds four 32-byte K steps
-              const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-              mma_ss<kE4M3>(d_t, q_desc + off, kd + off, idesc_s, kk > 0);
-            }
-            if constexpr (kZT)
-              mma_ss<false>(d_t, zbias_desc + static_cast<uint32_t>(((it % kSBufs) * 4096) >> 4),
-                            zones_desc, idesc_s, 1u);
-          };
-          // TMEM column of the A operand (P~) of K step g: 8 columns per step
-          auto p_col = [&](int buf, int g) -> uint32_t { return tmem + buf * kBlockN + g * 8; };
-          // O (+)= P V
-          auto issue_pv = [&](int it, bool acc) {
-            const uint64_t vd = v_desc + static_cast<uint32_t>(((it % SV) * L::kTile) >> 4);
-  #pragma unroll
-            for (int g = 0; g < kBlockN / L::kMmaK; ++g) {
-              const uint32_t d_t = tmem + kOCol, a_t = p_col(it % kSBufs, g);
-              const uint64_t bd = vd + static_cast<uint32_t>((g * L::kPvStep) >> 4);
-              mma_ts<kE4M3>(d_t, a_t, bd, idesc_pv, acc || g > 0);
-            }
-          };
-          auto issue_rs = [&](int it) {
-  #pragma unroll
-            for (int g = 0; g < kBlockN / L::kMmaK; ++g)
-              mma_ts<kE4M3>(tmem + (it % kSBufs) * kBlockN + 64, p_col(it % kSBufs, g), ones_desc,
-                            idesc_rs, g > 0);
-          };
-          // a score buffer is written again only once the tensor row sum
-          // that shared it has been read
-          auto buffer_free = [&](int it) -> bool {
-            if (!kLTensor || it < kSBufs) return true;
-            return __all_sync(0xffffffffu, wait_bounded(bar(L::bLFree + it % kSBufs),
-                                                        ((it - kSBufs) / kSBufs) & 1, p, abort_flag));
-          };
-          auto queue_s = [&](int it) -> bool {
-            if (!buffer_free(it)) return false;
-            if (!__all_sync(0xffffffffu,
-                            wait_bounded(bar(L::bKFull + it % SK), (it / SK) & 1, p, abort_flag)))
-              return false;
-            tc_fence_after();
-            issue_s(it);
-            mma_commit(bar(L::bSFull + it % kSBufs));
-            mma_commit(bar(L::bKEmpty + it % SK));
-            return true;
-          };
+        if (*abort_flag) {
+          // let every copy already issued land before the block can exit
+          if (is_k) wait_drain(bar(L::bQFull), (q_issued - 1) & 1);
+          for (int g = max(0, issued - S); g < issued; ++g)
+            wait_drain(bar(full + g % S), (g / S) & 1);
+        }
+      }
+      __syncwarp();
+    } else if (warp == kMmaWarp) {
+      // =================== MMA issuer ===================
+      // The whole warp runs this code with warp-uniform values; one elected
+      // lane issues each MMA and commit.
+      // A/B format codes: bf16 1; fp16 0 (kind::f16); e4m3 0 (kind::f8f6f4)
+      constexpr uint32_t kFmt = kDt == kDtBf16 ? 1u : 0u;
+      constexpr uint32_t idesc_s = idesc_f32acc<kFmt>(kBlockM, kBlockN, false);
+      constexpr uint32_t idesc_pv = idesc_f32acc<kFmt>(kBlockM, D, true);
+      constexpr uint32_t idesc_rs = idesc_f32acc<kFmt>(kBlockM, 16, false);
+      const uint64_t ones_desc = sdesc_sw128(sb + L::kOnes, 16, 1024);
+      // S_it = Q K^T into score buffer it % 3
+      // Descriptors of the first K step of each operand; a step further
+      // only adds its byte offset >> 4 to the start-address field (shared
+      // memory stays below 256 KB, so the field never overflows).
+      const uint64_t q_desc = sdesc_sw128(sb + L::kQ, 16, 1024);
+      const uint64_t k_desc = sdesc_sw128(sb + L::kK, 16, 1024);
+      const uint64_t v_desc = sdesc_sw128(sb + L::kV, 16384, 1024);
+      // (kZT) bias and ones tiles: 16-byte core matrices 128 B apart along
+      // K, 8-row groups 256 B apart; every entry of a tile is equal, so
+      // only the tile's 4 KB extent matters
+      const uint64_t zbias_desc = sdesc_plain(sb + L::kZBias, 128, 256);
+      const uint64_t zones_desc = sdesc_plain(sb + L::kZOnes, 128, 256);
+      auto issue_s = [&](int it) {
+        const uint64_t kd = k_desc + static_cast<uint32_t>(((it % SK) * L::kTile) >> 4);
+        const uint32_t d_t = tmem + (it % kSBufs) * kBlockN;
+#pragma unroll
+        for (int kk = 0; kk < D / L::kMmaK; ++kk) {
+          // each 128-byte slab row holds four 32-byte K steps
+          const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+          mma_ss<kE4M3>(d_t, q_desc + off, kd + off, idesc_s, kk > 0);
+        }
+        if constexpr (kZT)
+          mma_ss<false>(d_t, zbias_desc + static_cast<uint32_t>(((it % kSBufs) * 4096) >> 4),
+                        zones_desc, idesc_s, 1u);
+      };
+      // TMEM column of the A operand (P~) of K step g: 8 columns per step
+      auto p_col = [&](int buf, int g) -> uint32_t { return tmem + buf * kBlockN + g * 8; };
+      // O (+)= P V
+      auto issue_pv = [&](int it, bool acc) {
+        const uint64_t vd = v_desc + static_cast<uint32_t>(((it % SV) * L::kTile) >> 4);
+#pragma unroll
+        for (int g = 0; g < kBlockN / L::kMmaK; ++g) {
+          const uint32_t d_t = tmem + kOCol, a_t = p_col(it % kSBufs, g);
+          const uint64_t bd = vd + static_cast<uint32_t>((g * L::kPvStep) >> 4);
+          mma_ts<kE4M3>(d_t, a_t, bd, idesc_pv, acc || g > 0);
+        }
+      };
+      auto issue_rs = [&](int it) {
+#pragma unroll
+        for (int g = 0; g < kBlockN / L::kMmaK; ++g)
+          mma_ts<kE4M3>(tmem + (it % kSBufs) * kBlockN + 64, p_col(it % kSBufs, g), ones_desc,
+                        idesc_rs, g > 0);
+      };
+      // a score buffer is written again only once the tensor row sum
+      // that shared it has been read
+      auto buffer_free = [&](int it) -> bool {
+        if (!kLTensor || it < kSBufs) return true;
+        return __all_sync(0xffffffffu, wait_bounded(bar(L::bLFree + it % kSBufs),
+                                                    ((it - kSBufs) / kSBufs) & 1, p, abort_flag));
+      };
+      auto queue_s = [&](int it) -> bool {
+        if (!buffer_free(it)) return false;
+        if (!__all_sync(0xffffffffu,
+                        wait_bounded(bar(L::bKFull + it % SK), (it / SK) & 1, p, abort_flag)))
+          return false;
+        tc_fence_after();
+        issue_s(it);
+        mma_commit(bar(L::bSFull + it % kSBufs));
+        mma_commit(bar(L::bKEmpty + it % SK));
+        return true;
+      };
 
-          if (pass == 0) ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bQFull), 0, p, abort_flag));
-          for (int jj = 0; ok && jj < min(kSBufs, n_kv); ++jj) ok = queue_s(it0 + jj);
-          for (int j = 0; ok && j < n_kv; ++j) {
+      bool ok = true;
+      int seq = 0, it_base = 0;
+#pragma unroll 1
+      for (int phase = 0; phase < 2 && ok; ++phase) {
+        int count = 0;
+        if (phase == 1) {
+          if (!(ok = __all_sync(0xffffffffu,
+                                wait_bounded(bar(L::bListReady), 0, p, abort_flag))))
+            break;
+          count = min(static_cast<int>(misc[2]), kMaxDeferred);
+        }
+#pragma unroll 1
+        for (int k = 0; ok; ++k, ++seq) {
+          const int idx = phase == 0 ? fwd_item_at(p, k) : (k < count ? deferred[k] : -1);
+          if (idx < 0) break;
+          const int n_kv_t = item(idx).n_kv;
+          const bool tr = seq == 0;
+          if (!(ok = __all_sync(0xffffffffu,
+                                wait_bounded(bar(L::bQFull), seq & 1, p, abort_flag))))
+            break;
+          // (kZT) the bias tiles are zero again once the last item's detector
+          // has run
+          if (kZT && seq > 0 &&
+              !(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bDecided), (seq - 1) & 1, p,
+                                                          abort_flag))))
+            break;
+          const int it0 = it_base;
+          for (int jj = 0; ok && jj < min(kSBufs, n_kv_t); ++jj) ok = queue_s(it0 + jj);
+          // every S MMA of the item issued: Q is free once they have completed
+          if (ok && n_kv_t <= kSBufs) mma_commit(bar(L::bQFree));
+          for (int j = 0; ok && j < n_kv_t; ++j) {
             const int it = it0 + j, buf = it % kSBufs;
-            if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bVFull + it % SV), (it / SV) & 1,
-                                                            p, abort_flag))))
+            if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bVFull + it % SV),
+                                                            (it / SV) & 1, p, abort_flag))))
               break;
-            if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bPFull + buf), (it / kSBufs) & 1,
-                                                            p, abort_flag))))
+            if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bPFull + buf),
+                                                            (it / kSBufs) & 1, p, abort_flag))))
               break;
-            if (lane == 0) trace_mark(p, 3, 0, j, pass);
+            // the first O = P V of an item overwrites O: the last epilogue
+            // must have read it
+            if (j == 0 && seq > 0 &&
+                !(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bOFree), (seq - 1) & 1, p,
+                                                            abort_flag))))
+              break;
+            if (lane == 0) trace_mark(p, 3, 0, j, tr);
             tc_fence_after();
             if (kLTensor) {
               issue_rs(it);
@@ -926,39 +1090,74 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
             issue_pv(it, j > 0);
             if (SV != kSBufs) mma_commit(bar(L::bVEmpty + it % SV));
             mma_commit(bar(L::bOReady + buf));
-            if (j + kSBufs < n_kv && !(ok = queue_s(it + kSBufs))) break;
-            if (lane == 0) trace_mark(p, 4, 0, j, pass);
+            if (j + kSBufs < n_kv_t) {
+              if (!(ok = queue_s(it + kSBufs))) break;
+              if (j + kSBufs == n_kv_t - 1) mma_commit(bar(L::bQFree));
+            }
+            if (lane == 0) trace_mark(p, 4, 0, j, tr);
           }
-          if (ok) {
-            mma_commit(bar(L::bOFinal));
-          } else {
-            // every MMA issued so far must finish before TMEM can be released
-            mma_commit(bar(L::bDrain));
-            wait_drain(bar(L::bDrain), 0);
-          }
+          if (!ok) break;
+          mma_commit(bar(L::bOFinal));
+          it_base += n_kv_t;
         }
-        __syncwarp();
       }
-      __syncthreads();
-      if (!kTensor || misc[2] == 0u || *abort_flag != 0u) break;
+      if (ok) {
+        // the last item's "Q read" is waited for by no one else
+        if (seq > 0) wait_drain(bar(L::bQFree), (seq - 1) & 1);
+      } else {
+        // every MMA issued so far must finish before TMEM can be released
+        mma_commit(bar(L::bDrain));
+        wait_drain(bar(L::bDrain), 0);
+      }
+      __syncwarp();
     }
+    __syncthreads();
     tc_fence_after();
     if (warp == kMmaWarp) tmem_dealloc(tmem, kTmemCols);
   } else {
     regs_inc<kSoftmaxRegs>();
-    for (int pass = 0; pass < 2; ++pass) {
-      const int it0 = pass * n_kv;
-      // =================== softmax warps ===================
-      // Pass 1 (only after a flagged pass 0) reruns the block with one-row
-      // tiles, X = 1: every row's own maximum rounded up to a whole binade,
-      // so no row can underflow (the vector fallback of the page's
-      // all-underflow discussion, on the same code path).
-      softmax_role<D, kX, kLTensor, kDt, kZT>(p, smem, sb, tmem, misc, warp, lane, m0, bh, n_kv, it0,
-                                           pass, /*exact=*/pass == 1, split, kv_begin, kv_end,
-                                           kv_off);
-      __syncthreads();
-      if (!kTensor || misc[2] == 0u || *abort_flag != 0u) break;
+    // =================== softmax warps ===================
+    int seq = 0, it_base = 0;
+    int mr[2] = {0, 0};  // tiles each set has taken so far
+    const int other = (warp >> 2) ^ 1;
+    bool stop = false;
+#pragma unroll 1
+    for (int k = 0; !stop; ++k, ++seq) {
+      const int idx = fwd_item_at(p, k);
+      if (idx < 0) break;
+      const Item w = item(idx);
+      stop = softmax_role<D, kX, kLTensor, kDt, kZT, false>(
+          p, smem, sb, tmem, misc, warp, lane, idx, seq, w.m0, w.bh, w.n_kv, it_base, split,
+          kv_begin, kv_end, kv_off, /*epi=*/seq, mr[other], /*tr=*/seq == 0);
+      it_base += w.n_kv;
+      mr[0] += (w.n_kv + 1) / 2;
+      mr[1] += w.n_kv / 2;
     }
+    if constexpr (kTensor) {
+      // The fallback pass of each deferred item (one-row tiles, X = 1: every
+      // row's own maximum rounded up to a whole binade, so no row can
+      // underflow -- the vector fallback of the page's all-underflow
+      // discussion, on the same code path).  Set 0 appended to the list
+      // before the last barrier of the loop above.
+      if (!stop) {
+        if (warp == 0 && lane == 0) mbar_arrive(bar(L::bListReady));
+        const int count = min(static_cast<int>(misc[2]), kMaxDeferred);
+#pragma unroll 1
+        for (int k = 0; k < count && !stop; ++k, ++seq) {
+          const int idx = deferred[k];
+          const Item w = item(idx);
+          stop = softmax_role<D, kX, kLTensor, kDt, kZT, true>(
+              p, smem, sb, tmem, misc, warp, lane, idx, seq, w.m0, w.bh, w.n_kv, it_base, split,
+              kv_begin, kv_end, kv_off, /*epi=*/seq, mr[other], /*tr=*/false);
+          it_base += w.n_kv;
+          mr[0] += (w.n_kv + 1) / 2;
+          mr[1] += w.n_kv / 2;
+        }
+      }
+    } else {
+      if (!stop && warp == 0 && lane == 0) mbar_arrive(bar(L::bListReady));
+    }
+    __syncthreads();
   }
 }
 

@@ -97,6 +97,17 @@ def test_z_mode_validation(lib):
         assert lib.fat_attn_fwd_ex(ctypes.byref(p)) == want, kw
 
 
+def test_block_mode_validation(lib):
+    """Only the two block modes exist; anything else is refused before any
+    device call."""
+    base = dict(q=0x1000, k=0x2000, v=0x3000, o=0x4000, lse=0x5000, B=1, H=1, N=128, d=128,
+                causal=0, scale=0.125, X=128, variant=0, dtype=0)
+    for bm in (2, -1, 99):
+        p = fat.FatParams(**dict(base, block_mode=bm))
+        assert lib.fat_attn_fwd_ex(ctypes.byref(p)) == fat.FAT_ERR_INVALID_ARG, bm
+    assert fat.BLOCK_MODES == {"auto": 0, "per_tile": 1}
+
+
 def test_params_struct_layout_matches_header(tmp_path):
     """ctypes mirror of fat_params has the C compiler's size and offsets."""
     cuda_inc = "/usr/local/cuda/include"
