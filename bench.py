@@ -45,7 +45,7 @@ MEASURED_TRAFFIC = {
     "workload": "b2h16n8192d128_causal",
     "variant": "tensor",
     "bytes": 252.452e6 + 104.104e6,
-    "csrc_sha256": "bd9a0356ba8079d16e813f90044664d6427a9811416f5da78da830928e2bf5ba",
+    "csrc_sha256": "49454eabba38be46700c9ea13ebdbd63600cf417c25dae0a029010aee77c5e27",
 }
 
 

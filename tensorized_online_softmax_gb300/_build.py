@@ -26,7 +26,7 @@ def translation_units():
 
 def _sources():
     return (glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cuh"))
-            + glob.glob(os.path.join(ROOT, "include", "*.h")))
+            + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(ROOT, "include", "*.h")))
 
 
 def nvcc_path() -> str | None:

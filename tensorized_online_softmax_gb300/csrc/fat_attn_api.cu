@@ -219,8 +219,8 @@ int run_fwd(const fat_params* p, int Nq, int Nk, int splits, void* workspace,
   // One block per SM taking items in turn, or one block per item (split-KV
   // launches, and on request); the latter prefetches for the block one wave
   // ahead, the former for its own next item.
-  int grid = fp.n_items;
-  if (p->block_mode == FAT_BLOCKS_AUTO && n_splits == 1 && sms > 0 && sms < grid) grid = sms;
+  const int grid =
+      fat::fwd_grid(fp.n_items, sms, p->block_mode == FAT_BLOCKS_PER_TILE || n_splits != 1);
   fp.prefetch_stride = (grid == fp.n_items && sms > 0) ? sms : 0;
   fp.kv_split_len = kv_split_len;
   fp.o_part = o_part;

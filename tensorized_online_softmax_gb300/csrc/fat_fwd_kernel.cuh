@@ -3,14 +3,17 @@
 // Tensor-Vector Parallelism" (papercache.org summary, section A2, Algorithm 1)
 // and its vector-softmax ablation (the FA2 arm of the page's Fig. 10).
 //
-// One CTA computes one 128-row query tile of one (batch, head), the fused
-// flow of the page's section A3 / Fig. 2 (one output row block per worker, S
-// and P on chip).  Tensor-vector parallelism comes from a three-deep ring of
-// score buffers in TMEM: while the softmax warps turn S_j into P_j, the tensor
-// pipe already holds S_{j+1} and S_{j+2} and runs O += P_{j-1} V_{j-1}, so
-// neither side waits for the other in the steady state.
+// A work item is one 128-row query tile of one (batch, head), the fused flow
+// of the page's section A3 / Fig. 2 (one output row block per worker, S and P
+// on chip).  By default one CTA per SM takes items in turn (the next item's
+// loads and first S tiles overlap the last one's epilogue); with one CTA per
+// item the same code runs once.  Tensor-vector parallelism comes from a
+// three-deep ring of score buffers in TMEM: while the softmax warps turn S_j
+// into P_j, the tensor pipe already holds S_{j+1} and S_{j+2} and runs
+// O += P_{j-1} V_{j-1}, so neither side waits for the other in the steady
+// state.
 //
-//   warp 9      TMA producer of Q (once) and K_j, through an mbarrier ring;
+//   warp 9      TMA producer of Q (once per item) and K_j, through an mbarrier ring;
 //   warp 10     TMA producer of V_j, through its own ring, so neither stream
 //               waits for a slot of the other (K runs three tiles ahead).
 //   warp 8      MMA issuer (one thread): S_j = Q K_j^T into buffer j % 3,
@@ -28,11 +31,12 @@
 
 #include <cuda.h>
 
+#include "fat_schedule.h"
 #include "sm103_ptx.cuh"
 
 namespace fat {
 
-constexpr int kBlockM = 128;  // query rows per CTA (= TMEM lanes)
+constexpr int kBlockM = 128;  // query rows per item (= TMEM lanes)
 constexpr int kBlockN = 128;  // keys per K/V tile
 constexpr int kRowsPerCta = kBlockM;
 constexpr int kSBufs = 3;     // score / P buffers in TMEM
@@ -42,9 +46,6 @@ constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;    // Q and K
 constexpr int kLoadVWarp = 10;  // V; warp 11 completes the third warpgroup
 constexpr int kNumThreads = 384;
-// A block takes at most this many items (the host sizes the grid so), which
-// bounds its list of items deferred to the fallback pass.
-constexpr int kMaxDeferred = 64;
 // Register budget: 384 threads launch with kLaunchRegs each; the MMA/TMA
 // warpgroup drops to kCtrlRegs and the two softmax warpgroups rise to
 // kSoftmaxRegs.  256 * kSoftmaxRegs + 128 * kCtrlRegs <= 384 * kLaunchRegs.
@@ -124,15 +125,10 @@ __device__ __forceinline__ void fwd_work_item(const FwdParams& p, int idx, int& 
   bh = g * p.group_heads + rem % gh;
 }
 
-// The k-th item of this block, or -1 past the end.  Blocks take items in
-// strides of gridDim.x, in alternating direction (0 1 2 .. G-1, then 2G-1
-// .. G), so that within an L2 group (costs falling along the list) a block
-// with a heavy item in one stride gets a light one in the next.  With one
-// block per item (gridDim.x == n_items) this is just blockIdx.x.
+// The k-th item of this block, or -1 past the end (fat_schedule.h).
 __device__ __forceinline__ int fwd_item_at(const FwdParams& p, int k) {
-  const int G = static_cast<int>(gridDim.x), b = static_cast<int>(blockIdx.x);
-  const int idx = k * G + ((k & 1) ? G - 1 - b : b);
-  return idx < p.n_items ? idx : -1;
+  return fwd_item_index(k, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x),
+                        p.n_items);
 }
 
 template <int D, bool kE4M3 = false, bool kZT = false>
