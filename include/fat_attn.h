@@ -115,7 +115,8 @@ typedef enum { FAT_BLOCKS_AUTO = 0, FAT_BLOCKS_PER_TILE = 1 } fat_block_mode;
  *     or whose sum is zero, are detected; their 128-row block is recomputed
  *     with one-row tiles (X = 1: each row's own maximum rounded up to a whole
  *     binade, so no row can underflow) -- the optional fallback of the
- *     all-underflow discussion.
+ *     all-underflow discussion -- after the thread block's other tiles,
+ *     overwriting the block's O and LSE.
  * q, k, v: bf16.  Returns a fat_status.
  */
 int fat_attn_fwd(const void* q, const void* k, const void* v, float* o, float* lse, int B, int H,
@@ -238,21 +239,22 @@ typedef struct fat_params {
   unsigned long long wait_timeout_ns; /* 0: default of 4 s per device wait */
   cudaStream_t stream;
   /* nullable device buffer of FAT_TRACE_WORDS u64 (8-byte aligned): SM-clock
-   * stamps of the first thread block's pipeline phases, for measuring how
-   * long the tensor pipe waits for the softmax (see fat_trace_layout below) */
+   * stamps of the first thread block's pipeline phases on its first query
+   * tile, for measuring how long the tensor pipe waits for the softmax (see
+   * the trace layout below) */
   unsigned long long* trace;
   int z_mode;                         /* fat_zmode (tensorized variant only) */
   int block_mode;                     /* fat_block_mode */
 } fat_params;
 
 /*
- * Trace layout (first thread block, first pass): word
+ * Trace layout (first thread block, first query tile, first pass): word
  * (e * 2 + t) * FAT_TRACE_ITERS + j holds the clock of event e at K/V tile j
  * (< FAT_TRACE_ITERS); t = the softmax set that takes tile j (j % 2) for the
  * softmax events, 0 for the MMA issuer's: e = 0 softmax received S_j; 1
  * softmax computed m_hat; 2 softmax published P_j; 3 MMA issuer saw P_j; 4
  * MMA issuer queued O += P_j V and S_{j+3}.  Word FAT_TRACE_WORDS-2: kernel
- * start; FAT_TRACE_WORDS-1: end of the softmax epilogue.  Words of events
+ * start; FAT_TRACE_WORDS-1: end of that tile's softmax epilogue.  Words of events
  * that did not happen are left untouched.
  */
 #define FAT_TRACE_ITERS 128
