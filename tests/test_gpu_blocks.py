@@ -72,5 +72,6 @@ def test_tiles_in_turn_match_oracle(cuda_device, causal, variant):
     inp = gen.make_inputs(w)
     o, lse = run_cuda(w, to_dev(inp), variant)
     o_ref, lse_ref = oracle_full(w, inp)
-    compare(o.cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, tol_key(w, variant),
-            what=f"tiles in turn {variant} causal={causal}")
+    compare(o.cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, tol_key(w),
+            what=f"tiles in turn {variant} causal={causal}",
+            variant=variant)

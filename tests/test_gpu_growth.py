@@ -27,5 +27,6 @@ def test_growing_maximum(cuda_device, binades, causal, variant):
     inp = gen.make_inputs(w)
     o, lse = run_cuda(w, to_dev(inp), variant)
     o_ref, lse_ref = oracle_full(w, inp)
-    compare(o.cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, tol_key(w, variant),
-            what=f"growth {binades} binades/tile {variant} causal={causal}")
+    compare(o.cpu().numpy(), lse.cpu().numpy(), o_ref, lse_ref, tol_key(w),
+            what=f"growth {binades} binades/tile {variant} causal={causal}",
+            variant=variant)

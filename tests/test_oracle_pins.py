@@ -309,3 +309,57 @@ def test_rectangular_non_causal_ignores_key_order_and_rejects_short_causal():
     np.testing.assert_allclose(lsep, lse, atol=1e-12)
     with pytest.raises(RuntimeError):
         oracle.attn_fwd_qk(_rand((1, 1, 12, 4), 93), k, v, True, 0.7)
+
+
+# --------------------------------------------------------------------------
+# negative pin: an update rule that must NOT agree with the oracle
+# --------------------------------------------------------------------------
+
+def _blocked_online(q, k, v, scale, block, factor_on_new):
+    """Blocked online softmax over key blocks, with the per-row rescale
+    factor exp(m_old - m_new) placed on the running output (the correct
+    update) or, when ``factor_on_new`` is set, on the new block's term P V
+    (the update rule of the first PyTorch example in the FA-T post,
+    "FlashAttention-T：张量化注意力机制优化方案", which leaves the old
+    output scaled only by l_old / l_new).  The row sum l is carried the same
+    way in both.  Returns (O, l); LSE = m + ln l for the correct rule."""
+    B, H, N, d = q.shape
+    out = np.zeros_like(v)
+    l_run = np.zeros((B, H, N, 1))
+    m_run = np.full((B, H, N, 1), -np.inf)
+    for j in range(0, N, block):
+        s = scale * np.einsum("bhid,bhjd->bhij", q, k[:, :, j:j + block])
+        m_new = np.maximum(m_run, s.max(axis=-1, keepdims=True))
+        alpha = np.exp(m_run - m_new)  # 0 on the first block (m_run = -inf)
+        p = np.exp(s - m_new)
+        l_new = alpha * l_run + p.sum(axis=-1, keepdims=True)
+        pv = np.einsum("bhij,bhjd->bhid", p, v[:, :, j:j + block])
+        if factor_on_new:
+            out = (l_run / l_new) * out + (alpha / l_new) * pv
+        else:
+            out = (alpha * l_run / l_new) * out + pv / l_new
+        m_run, l_run = m_new, l_new
+    return out, m_run[..., 0] + np.log(l_run[..., 0])
+
+
+def test_misplaced_rescale_rule_disagrees_with_the_oracle():
+    """The FA-T post's first example multiplies the new block's P V by
+    exp(m_old - m_new) instead of the running output.  On random data that
+    rule must disagree with the oracle (so the oracle cannot have adopted
+    it), while the same blocked loop with the factor on the running output
+    agrees with the oracle, and the oracle agrees with brute force."""
+    B, H, N, d, block = 2, 2, 128, 16, 32
+    q, k, v = (_rand((B, H, N, d), 300 + i, std=1.2) for i in range(3))
+    scale = d ** -0.5
+    o, lse = oracle.attn_fwd(q, k, v, False, scale)
+    o_bf, lse_bf = oracle.attn_naive(q, k, v, False, scale)
+    np.testing.assert_allclose(o, o_bf, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_bf, atol=1e-12)
+    o_ok, lse_ok = _blocked_online(q, k, v, scale, block, factor_on_new=False)
+    np.testing.assert_allclose(o_ok, o, atol=1e-12)
+    np.testing.assert_allclose(lse_ok, lse, atol=1e-12)
+    o_bad, _ = _blocked_online(q, k, v, scale, block, factor_on_new=True)
+    # the first block's contribution is lost (its factor is exp(-inf) = 0)
+    # and later ones are mis-weighted: far outside any rounding bar
+    assert np.abs(o_bad - o).max() > 0.1
+    assert np.abs(o_bad - o).mean() > 1e-2
