@@ -102,13 +102,22 @@ struct FwdParams {
 //   softmax set that takes tile j (softmax events, written by warps 0 and
 //   4) or 0 (MMA):
 //   e = 0 softmax got S_j, 1 softmax has m_hat, 2 softmax publishes P_j,
-//       3 MMA issuer sees P_j, 4 MMA issuer has queued O += P_j V, S_{j+3};
+//       3 MMA issuer sees P_j, 4 MMA issuer has queued O += P_j V, S_{j+3},
+//       5 MMA issuer sees V_j, 6 MMA issuer has queued O += P_j V,
+//       7 MMA issuer sees K_{j+3};
 //   word kTraceWords - 2 / - 1: kernel start / softmax epilogue done.
 constexpr int kTraceIters = 128;
-constexpr int kTraceWords = 5 * 2 * kTraceIters + 2;
+constexpr int kTraceEvents = 8;
+constexpr int kTraceWords = kTraceEvents * 2 * kTraceIters + 2;
 
 __device__ __forceinline__ void trace_mark(const FwdParams& p, int e, int t, int j, bool on) {
   if (on && p.trace != nullptr && blockIdx.x == 0 && j < kTraceIters)
+    p.trace[(e * 2 + t) * kTraceIters + j] = static_cast<unsigned long long>(clock64());
+}
+
+// The same once the caller has checked that this block traces this pass.
+__device__ __forceinline__ void trace_at(const FwdParams& p, int e, int t, int j) {
+  if (j < kTraceIters)
     p.trace[(e * 2 + t) * kTraceIters + j] = static_cast<unsigned long long>(clock64());
 }
 
@@ -139,6 +148,11 @@ struct Smem {
   // rows fit two K and three V stages
   static constexpr int kKStages = (D * kElt == 256) ? 2 : 4;
   static constexpr int kVStages = (D * kElt == 256) ? 3 : 4;
+  // With at most as many K stages as score buffers, the completion of S_it
+  // also marks K stage it % kKStages free (K_{it + kKStages} is loaded after
+  // it, and the buffer's next S needs a later K tile, so a waiter is never
+  // two phases behind); deeper K rings keep their own "K free" barrier.
+  static constexpr bool kKFreeOnS = kKStages <= kSBufs;
   static constexpr int kAtoms = D * kElt / 128;       // 128-byte-wide column slabs per tile
   static constexpr int kAtomCols = 128 / kElt;        // elements per slab row
   static constexpr int kMmaK = 32 / kElt;             // K of one MMA (bf16 16, e4m3 32)
@@ -942,7 +956,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
               break;
             for (int jj = issued - it_base; jj < w.n_kv; ++jj) {
               const int it = it_base + jj, st = it % S;
-              if (!(ok = wait_bounded(bar(empty + st), ((it / S) & 1) ^ 1, p, abort_flag))) break;
+              if (is_k && L::kKFreeOnS) {
+                // K stage st is free once S_{it - S} has completed
+                if (it >= S && !(ok = wait_bounded(bar(L::bSFull + (it - S) % kSBufs),
+                                                   ((it - S) / kSBufs) & 1, p, abort_flag)))
+                  break;
+              } else if (!(ok = wait_bounded(bar(empty + st), ((it / S) & 1) ^ 1, p, abort_flag))) {
+                break;
+              }
               mbar_arrive_expect_tx(bar(full + st), L::kTile);
               for (int a = 0; a < L::kAtoms; ++a)
                 tma_load_3d(sb + ring + st * L::kTile + a * 16384, tm, bar(full + st),
@@ -983,58 +1004,74 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
       // only the tile's 4 KB extent matters
       const uint64_t zbias_desc = sdesc_plain(sb + L::kZBias, 128, 256);
       const uint64_t zones_desc = sdesc_plain(sb + L::kZOnes, 128, 256);
-      auto issue_s = [&](int it) {
-        const uint64_t kd = k_desc + static_cast<uint32_t>(((it % SK) * L::kTile) >> 4);
-        const uint32_t d_t = tmem + (it % kSBufs) * kBlockN;
-#pragma unroll
-        for (int kk = 0; kk < D / L::kMmaK; ++kk) {
-          // each 128-byte slab row holds four 32-byte K steps
-          const uint32_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-          mma_ss<kE4M3>(d_t, q_desc + off, kd + off, idesc_s, kk > 0);
+      // The tensor pipe queues only a handful of MMAs, so this warp's own
+      // instruction count between MMA groups decides whether the pipe runs
+      // dry: ring positions advance by counters (no divisions), the MMAs of
+      // a GEMM go out four per elected issue, and the trace test is hoisted
+      // out of the tile loop.
+      struct Ring {  // a slot of an n-deep ring and the parity of its phase
+        int slot = 0;
+        uint32_t phase = 0;
+        __device__ __forceinline__ void next(int n) {
+          if (++slot == n) {
+            slot = 0;
+            phase ^= 1u;
+          }
         }
+      };
+      Ring s_buf, s_k;  // score buffer and K stage of the next S MMA
+      Ring p_buf, p_v;  // score buffer (P~) and V stage of the next P V MMA
+      int s_count = 0;  // S tiles queued so far by this block
+      // S = Q K^T: D / kMmaK K steps, four per 128-byte slab of the rows
+      auto issue_s = [&](int buf, int kst) {
+        const uint64_t kd = k_desc + static_cast<uint32_t>((kst * L::kTile) >> 4);
+        const uint32_t d_t = tmem + buf * kBlockN;
+#pragma unroll
+        for (int g = 0; g < D / L::kMmaK / 4; ++g)
+          mma_ss_x4<kE4M3, 2>(d_t, q_desc + g * 1024, kd + g * 1024, idesc_s, g > 0);
         if constexpr (kZT)
-          mma_ss<false>(d_t, zbias_desc + static_cast<uint32_t>(((it % kSBufs) * 4096) >> 4),
-                        zones_desc, idesc_s, 1u);
+          mma_ss<false>(d_t, zbias_desc + static_cast<uint32_t>((buf * 4096) >> 4), zones_desc,
+                        idesc_s, 1u);
       };
-      // TMEM column of the A operand (P~) of K step g: 8 columns per step
-      auto p_col = [&](int buf, int g) -> uint32_t { return tmem + buf * kBlockN + g * 8; };
-      // O (+)= P V
-      auto issue_pv = [&](int it, bool acc) {
-        const uint64_t vd = v_desc + static_cast<uint32_t>(((it % SV) * L::kTile) >> 4);
+      // O (+)= P V: A = P~ in TMEM (8 columns per K step), B = V (MN-major)
+      auto issue_pv = [&](int buf, int vst, bool acc) {
+        const uint64_t vd = v_desc + static_cast<uint32_t>((vst * L::kTile) >> 4);
 #pragma unroll
-        for (int g = 0; g < kBlockN / L::kMmaK; ++g) {
-          const uint32_t d_t = tmem + kOCol, a_t = p_col(it % kSBufs, g);
-          const uint64_t bd = vd + static_cast<uint32_t>((g * L::kPvStep) >> 4);
-          mma_ts<kE4M3>(d_t, a_t, bd, idesc_pv, acc || g > 0);
-        }
+        for (int g = 0; g < kBlockN / L::kMmaK / 4; ++g)
+          mma_ts_x4<kE4M3, 8, (L::kPvStep >> 4)>(
+              tmem + kOCol, tmem + buf * kBlockN + g * 32,
+              vd + static_cast<uint32_t>(g * 4 * (L::kPvStep >> 4)), idesc_pv, acc || g > 0);
       };
-      auto issue_rs = [&](int it) {
+      auto issue_rs = [&](int buf) {
 #pragma unroll
         for (int g = 0; g < kBlockN / L::kMmaK; ++g)
-          mma_ts<kE4M3>(tmem + (it % kSBufs) * kBlockN + 64, p_col(it % kSBufs, g), ones_desc,
+          mma_ts<kE4M3>(tmem + buf * kBlockN + 64, tmem + buf * kBlockN + g * 8, ones_desc,
                         idesc_rs, g > 0);
       };
-      // a score buffer is written again only once the tensor row sum
-      // that shared it has been read
-      auto buffer_free = [&](int it) -> bool {
-        if (!kLTensor || it < kSBufs) return true;
-        return __all_sync(0xffffffffu, wait_bounded(bar(L::bLFree + it % kSBufs),
-                                                    ((it - kSBufs) / kSBufs) & 1, p, abort_flag));
-      };
-      auto queue_s = [&](int it) -> bool {
-        if (!buffer_free(it)) return false;
-        if (!__all_sync(0xffffffffu,
-                        wait_bounded(bar(L::bKFull + it % SK), (it / SK) & 1, p, abort_flag)))
+      auto queue_s = [&](int jt, bool trc) -> bool {
+        // a score buffer is written again only once the tensor row sum
+        // that shared it has been read
+        if (kLTensor && s_count >= kSBufs &&
+            !__all_sync(0xffffffffu, wait_bounded(bar(L::bLFree + s_buf.slot), s_buf.phase ^ 1u,
+                                                  p, abort_flag)))
           return false;
+        if (!__all_sync(0xffffffffu,
+                        wait_bounded(bar(L::bKFull + s_k.slot), s_k.phase, p, abort_flag)))
+          return false;
+        if (trc && lane == 0) trace_at(p, 7, 0, jt);
         tc_fence_after();
-        issue_s(it);
-        mma_commit(bar(L::bSFull + it % kSBufs));
-        mma_commit(bar(L::bKEmpty + it % SK));
+        issue_s(s_buf.slot, s_k.slot);
+        // (with at most three K stages "S done" also frees the K stage)
+        mma_commit(bar(L::bSFull + s_buf.slot));
+        if constexpr (!L::kKFreeOnS) mma_commit(bar(L::bKEmpty + s_k.slot));
+        s_buf.next(kSBufs);
+        s_k.next(SK);
+        ++s_count;
         return true;
       };
 
       bool ok = true;
-      int seq = 0, it_base = 0;
+      int seq = 0;
 #pragma unroll 1
       for (int phase = 0; phase < 2 && ok; ++phase) {
         int count = 0;
@@ -1049,7 +1086,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
           const int idx = phase == 0 ? fwd_item_at(p, k) : (k < count ? deferred[k] : -1);
           if (idx < 0) break;
           const int n_kv_t = item(idx).n_kv;
-          const bool tr = seq == 0;
+          const bool trc = seq == 0 && p.trace != nullptr && blockIdx.x == 0;
           if (!(ok = __all_sync(0xffffffffu,
                                 wait_bounded(bar(L::bQFull), seq & 1, p, abort_flag))))
             break;
@@ -1059,42 +1096,51 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
               !(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bDecided), (seq - 1) & 1, p,
                                                           abort_flag))))
             break;
-          const int it0 = it_base;
-          for (int jj = 0; ok && jj < min(kSBufs, n_kv_t); ++jj) ok = queue_s(it0 + jj);
+          for (int jj = 0; ok && jj < min(kSBufs, n_kv_t); ++jj) ok = queue_s(-1, false);
           // every S MMA of the item issued: Q is free once they have completed
           if (ok && n_kv_t <= kSBufs) mma_commit(bar(L::bQFree));
+#pragma unroll 1
           for (int j = 0; ok && j < n_kv_t; ++j) {
-            const int it = it0 + j, buf = it % kSBufs;
-            if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bVFull + it % SV),
-                                                            (it / SV) & 1, p, abort_flag))))
-              break;
-            if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bPFull + buf),
-                                                            (it / kSBufs) & 1, p, abort_flag))))
-              break;
+            const int buf = p_buf.slot;
+            // V_j and P~_j: one vote when both are already there (the usual
+            // case), the bounded waits otherwise
+            const bool both = mbar_test_wait(bar(L::bVFull + p_v.slot), p_v.phase) &&
+                              mbar_test_wait(bar(L::bPFull + buf), p_buf.phase);
+            if (!__all_sync(0xffffffffu, both)) {
+              if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bVFull + p_v.slot),
+                                                              p_v.phase, p, abort_flag))))
+                break;
+              if (trc && lane == 0) trace_at(p, 5, 0, j);
+              if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bPFull + buf),
+                                                              p_buf.phase, p, abort_flag))))
+                break;
+            }
             // the first O = P V of an item overwrites O: the last epilogue
             // must have read it
             if (j == 0 && seq > 0 &&
                 !(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bOFree), (seq - 1) & 1, p,
                                                             abort_flag))))
               break;
-            if (lane == 0) trace_mark(p, 3, 0, j, tr);
+            if (trc && lane == 0) trace_at(p, 3, 0, j);
             tc_fence_after();
             if (kLTensor) {
-              issue_rs(it);
+              issue_rs(buf);
               mma_commit(bar(L::bRsFull + buf));
             }
-            issue_pv(it, j > 0);
-            if (SV != kSBufs) mma_commit(bar(L::bVEmpty + it % SV));
+            issue_pv(buf, p_v.slot, j > 0);
+            if (SV != kSBufs) mma_commit(bar(L::bVEmpty + p_v.slot));
             mma_commit(bar(L::bOReady + buf));
+            p_buf.next(kSBufs);
+            p_v.next(SV);
+            if (trc && lane == 0) trace_at(p, 6, 0, j);
             if (j + kSBufs < n_kv_t) {
-              if (!(ok = queue_s(it + kSBufs))) break;
+              if (!(ok = queue_s(j, trc))) break;
               if (j + kSBufs == n_kv_t - 1) mma_commit(bar(L::bQFree));
             }
-            if (lane == 0) trace_mark(p, 4, 0, j, tr);
+            if (trc && lane == 0) trace_at(p, 4, 0, j);
           }
           if (!ok) break;
           mma_commit(bar(L::bOFinal));
-          it_base += n_kv_t;
         }
       }
       if (ok) {

@@ -271,6 +271,65 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
   }
 }
 
+// Four consecutive K steps of one GEMM from one elected lane, one predicate
+// set-up for all four (the issuing warp's instruction count per MMA is what
+// keeps the shallow MMA queue fed).  Step k uses the descriptors advanced by
+// k * kStep (16-byte units) -- the same K-step offset in A and B -- and
+// accumulates per `accumulate` at k = 0, always after that.
+#define FAT_MMA_SS_X4(KIND)                                                                   \
+  asm volatile(                                                                               \
+      "{\n\t.reg .pred p, e, t;\n\t.reg .b64 a1, b1;\n\t"                                    \
+      "elect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"     \
+      "@e tcgen05.mma.cta_group::1.kind::" KIND " [%0], %1, %2, %3, p;\n\t"                  \
+      "add.s64 a1, %1, %5;\n\tadd.s64 b1, %2, %5;\n\t"                                      \
+      "@e tcgen05.mma.cta_group::1.kind::" KIND " [%0], a1, b1, %3, t;\n\t"                  \
+      "add.s64 a1, %1, %6;\n\tadd.s64 b1, %2, %6;\n\t"                                      \
+      "@e tcgen05.mma.cta_group::1.kind::" KIND " [%0], a1, b1, %3, t;\n\t"                  \
+      "add.s64 a1, %1, %7;\n\tadd.s64 b1, %2, %7;\n\t"                                      \
+      "@e tcgen05.mma.cta_group::1.kind::" KIND " [%0], a1, b1, %3, t;\n\t}" ::"r"(d_tmem), \
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "n"(kStep), "n"(2 * kStep),        \
+      "n"(3 * kStep)                                                                          \
+      : "memory")
+
+template <bool kE4M3, uint32_t kStep>
+__device__ __forceinline__ void mma_ss_x4(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  if constexpr (kE4M3) {
+    FAT_MMA_SS_X4("f8f6f4");
+  } else {
+    FAT_MMA_SS_X4("f16");
+  }
+}
+
+// The same with A in TMEM: step k reads A at column a_tmem + k * kColStep and
+// B at bdesc + k * kStep.
+#define FAT_MMA_TS_X4(KIND)                                                                   \
+  asm volatile(                                                                               \
+      "{\n\t.reg .pred p, e, t;\n\t.reg .b32 a1;\n\t.reg .b64 b1;\n\t"                       \
+      "elect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\tsetp.eq.b32 t, 0, 0;\n\t"     \
+      "@e tcgen05.mma.cta_group::1.kind::" KIND " [%0], [%1], %2, %3, p;\n\t"                \
+      "add.u32 a1, %1, %5;\n\tadd.s64 b1, %2, %8;\n\t"                                      \
+      "@e tcgen05.mma.cta_group::1.kind::" KIND " [%0], [a1], b1, %3, t;\n\t"                \
+      "add.u32 a1, %1, %6;\n\tadd.s64 b1, %2, %9;\n\t"                                      \
+      "@e tcgen05.mma.cta_group::1.kind::" KIND " [%0], [a1], b1, %3, t;\n\t"                \
+      "add.u32 a1, %1, %7;\n\tadd.s64 b1, %2, %10;\n\t"                                     \
+      "@e tcgen05.mma.cta_group::1.kind::" KIND " [%0], [a1], b1, %3, t;\n\t}" ::"r"(d_tmem), \
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate), "n"(kColStep), "n"(2 * kColStep), \
+      "n"(3 * kColStep), "n"(kStep), "n"(2 * kStep), "n"(3 * kStep)                           \
+      : "memory")
+
+template <bool kE4M3, uint32_t kColStep, uint32_t kStep>
+__device__ __forceinline__ void mma_ts_x4(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  if constexpr (kE4M3) {
+    FAT_MMA_TS_X4("f8f6f4");
+  } else {
+    FAT_MMA_TS_X4("f16");
+  }
+}
+#undef FAT_MMA_SS_X4
+#undef FAT_MMA_TS_X4
+
 // Arrive (once) on an mbarrier when every tcgen05 operation this thread issued
 // before has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
