@@ -44,7 +44,8 @@ constexpr int kOCol = kSBufs * kBlockN;  // first TMEM column of O
 constexpr int kSoftmaxWarps = 8;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;    // Q and K
-constexpr int kLoadVWarp = 10;  // V; warp 11 completes the third warpgroup
+constexpr int kLoadVWarp = 10;  // V
+constexpr int kObsWarp = 11;    // completes the third warpgroup; traced launches only
 constexpr int kNumThreads = 384;
 // Register budget: 384 threads launch with kLaunchRegs each; the MMA/TMA
 // warpgroup drops to kCtrlRegs and the two softmax warpgroups rise to
@@ -104,10 +105,11 @@ struct FwdParams {
 //   e = 0 softmax got S_j, 1 softmax has m_hat, 2 softmax publishes P_j,
 //       3 MMA issuer sees P_j, 4 MMA issuer has queued O += P_j V, S_{j+3},
 //       5 MMA issuer sees V_j, 6 MMA issuer has queued O += P_j V,
-//       7 MMA issuer sees K_{j+3};
+//       7 MMA issuer sees K_{j+3}, 8 S_j has completed, 9 O += P_j V has
+//       completed (events 8 and 9 seen by warp 11, which has no other role);
 //   word kTraceWords - 2 / - 1: kernel start / softmax epilogue done.
 constexpr int kTraceIters = 128;
-constexpr int kTraceEvents = 8;
+constexpr int kTraceEvents = 10;
 constexpr int kTraceWords = kTraceEvents * 2 * kTraceIters + 2;
 
 __device__ __forceinline__ void trace_mark(const FwdParams& p, int e, int t, int j, bool on) {
@@ -1048,14 +1050,15 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
           mma_ts<kE4M3>(tmem + buf * kBlockN + 64, tmem + buf * kBlockN + g * 8, ones_desc,
                         idesc_rs, g > 0);
       };
-      auto queue_s = [&](int jt, bool trc) -> bool {
+      auto queue_s = [&](int jt, bool trc, bool k_ready = false) -> bool {
         // a score buffer is written again only once the tensor row sum
         // that shared it has been read
         if (kLTensor && s_count >= kSBufs &&
             !__all_sync(0xffffffffu, wait_bounded(bar(L::bLFree + s_buf.slot), s_buf.phase ^ 1u,
                                                   p, abort_flag)))
           return false;
-        if (!__all_sync(0xffffffffu,
+        if (!k_ready &&
+            !__all_sync(0xffffffffu,
                         wait_bounded(bar(L::bKFull + s_k.slot), s_k.phase, p, abort_flag)))
           return false;
         if (trc && lane == 0) trace_at(p, 7, 0, jt);
@@ -1102,11 +1105,17 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
 #pragma unroll 1
           for (int j = 0; ok && j < n_kv_t; ++j) {
             const int buf = p_buf.slot;
-            // V_j and P~_j: one vote when both are already there (the usual
-            // case), the bounded waits otherwise
-            const bool both = mbar_test_wait(bar(L::bVFull + p_v.slot), p_v.phase) &&
-                              mbar_test_wait(bar(L::bPFull + buf), p_buf.phase);
-            if (!__all_sync(0xffffffffu, both)) {
+            const bool more_s = j + kSBufs < n_kv_t;
+            // V_j, P~_j and (when S_{j+3} follows) K_{j+3}: three independent
+            // probes and one vote when all are there, the usual case, so that
+            // nothing but a commit separates O += P_j V from S_{j+3}; the
+            // bounded waits otherwise
+            const bool v_ok = mbar_test_wait(bar(L::bVFull + p_v.slot), p_v.phase);
+            const bool p_ok = mbar_test_wait(bar(L::bPFull + buf), p_buf.phase);
+            const bool k_ok = !more_s || mbar_test_wait(bar(L::bKFull + s_k.slot), s_k.phase);
+            const uint32_t all3 = __ballot_sync(0xffffffffu, v_ok && p_ok && k_ok);
+            const bool k_ready = all3 == 0xffffffffu && more_s;
+            if (all3 != 0xffffffffu) {
               if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bVFull + p_v.slot),
                                                               p_v.phase, p, abort_flag))))
                 break;
@@ -1133,8 +1142,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
             p_buf.next(kSBufs);
             p_v.next(SV);
             if (trc && lane == 0) trace_at(p, 6, 0, j);
-            if (j + kSBufs < n_kv_t) {
-              if (!(ok = queue_s(j, trc))) break;
+            if (more_s) {
+              if (!(ok = queue_s(j, trc, k_ready))) break;
               if (j + kSBufs == n_kv_t - 1) mma_commit(bar(L::bQFree));
             }
             if (trc && lane == 0) trace_at(p, 4, 0, j);
@@ -1150,6 +1159,27 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
         // every MMA issued so far must finish before TMEM can be released
         mma_commit(bar(L::bDrain));
         wait_drain(bar(L::bDrain), 0);
+      }
+      __syncwarp();
+    } else if (warp == kObsWarp && p.trace != nullptr && blockIdx.x == 0) {
+      // Completion times of the first item's MMA groups, in the order the
+      // tensor pipe runs them (S_0, S_1, S_2, then O += P_j V, S_{j+3}):
+      // with the issue stamps they show whether the pipe idles between
+      // groups.  Waits without the abort flag and with a short limit, so
+      // observing never stops the kernel.
+      const int n = min(first.n_kv, kTraceIters);
+      auto seen = [&](int e, int j, int b) -> bool {
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(bar(b + j % kSBufs), (j / kSBufs) & 1))
+          if (*abort_flag || globaltimer_ns() - t0 > 100000000ull) return false;
+        if (lane == 0) trace_at(p, e, 0, j);
+        return true;
+      };
+      bool on = true;
+      for (int j = 0; on && j < min(kSBufs, n); ++j) on = seen(8, j, L::bSFull);
+      for (int j = 0; on && j < n; ++j) {
+        on = seen(9, j, L::bOReady);
+        if (on && j + kSBufs < n) on = seen(8, j + kSBufs, L::bSFull);
       }
       __syncwarp();
     }
