@@ -253,14 +253,12 @@ typedef struct fat_params {
  * (< FAT_TRACE_ITERS); t = the softmax set that takes tile j (j % 2) for the
  * softmax events, 0 for the MMA issuer's: e = 0 softmax received S_j; 1
  * softmax computed m_hat; 2 softmax published P_j; 3 MMA issuer saw P_j; 4
- * MMA issuer queued O += P_j V and S_{j+3}; 5 MMA issuer saw V_j; 6 MMA
- * issuer queued O += P_j V; 7 MMA issuer saw K_{j+3}; 8 S_j completed; 9 O += P_j V
- * completed.  Word FAT_TRACE_WORDS-2: kernel
+ * MMA issuer queued O += P_j V and S_{j+3}.  Word FAT_TRACE_WORDS-2: kernel
  * start; FAT_TRACE_WORDS-1: end of that tile's softmax epilogue.  Words of events
  * that did not happen are left untouched.
  */
 #define FAT_TRACE_ITERS 128
-#define FAT_TRACE_EVENTS 10
+#define FAT_TRACE_EVENTS 5
 #define FAT_TRACE_WORDS (FAT_TRACE_EVENTS * 2 * FAT_TRACE_ITERS + 2)
 
 int fat_attn_fwd_ex(const fat_params* p);

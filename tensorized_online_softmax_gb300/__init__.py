@@ -41,7 +41,7 @@ LMODES = {"vector": 0, "tensor": 1}
 BLOCK_MODES = {"auto": 0, "per_tile": 1}
 ZMODES = {"vector": 0, "tensor": 1}
 TRACE_ITERS = 128
-TRACE_EVENTS = 10
+TRACE_EVENTS = 5
 TRACE_WORDS = TRACE_EVENTS * 2 * TRACE_ITERS + 2
 
 # every extern "C" entry point declared in include/fat_attn.h

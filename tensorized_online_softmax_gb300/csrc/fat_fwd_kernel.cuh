@@ -44,8 +44,7 @@ constexpr int kOCol = kSBufs * kBlockN;  // first TMEM column of O
 constexpr int kSoftmaxWarps = 8;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;    // Q and K
-constexpr int kLoadVWarp = 10;  // V
-constexpr int kObsWarp = 11;    // completes the third warpgroup; traced launches only
+constexpr int kLoadVWarp = 10;  // V; warp 11 completes the third warpgroup
 constexpr int kNumThreads = 384;
 // Register budget: 384 threads launch with kLaunchRegs each; the MMA/TMA
 // warpgroup drops to kCtrlRegs and the two softmax warpgroups rise to
@@ -103,13 +102,10 @@ struct FwdParams {
 //   softmax set that takes tile j (softmax events, written by warps 0 and
 //   4) or 0 (MMA):
 //   e = 0 softmax got S_j, 1 softmax has m_hat, 2 softmax publishes P_j,
-//       3 MMA issuer sees P_j, 4 MMA issuer has queued O += P_j V, S_{j+3},
-//       5 MMA issuer sees V_j, 6 MMA issuer has queued O += P_j V,
-//       7 MMA issuer sees K_{j+3}, 8 S_j has completed, 9 O += P_j V has
-//       completed (events 8 and 9 seen by warp 11, which has no other role);
+//       3 MMA issuer sees P_j, 4 MMA issuer has queued O += P_j V, S_{j+3};
 //   word kTraceWords - 2 / - 1: kernel start / softmax epilogue done.
 constexpr int kTraceIters = 128;
-constexpr int kTraceEvents = 10;
+constexpr int kTraceEvents = 5;
 constexpr int kTraceWords = kTraceEvents * 2 * kTraceIters + 2;
 
 __device__ __forceinline__ void trace_mark(const FwdParams& p, int e, int t, int j, bool on) {
@@ -288,6 +284,14 @@ __device__ __forceinline__ bool softmax_role(const FwdParams& p, uint8_t* smem, 
   // so that its terms use the format's range; the factor cancels in O / l and
   // is taken off LSE.  bf16 has fp32's exponent range and needs none.
   constexpr float kKappa = kE4M3 ? 8.f : (kDt == kDtF16 ? 15.f : 0.f);
+  // Headroom of the surrogate offset (binades): it is raised only when a
+  // tile's maximum exceeds it by more than this, so P~ <= 2^kHeadroom.  Once
+  // an item's first tile has set it, Gaussian-like scores hardly ever climb
+  // 8 binades further, so the uniform O rescale -- and its wait for the last
+  // P V -- all but disappears.  bf16 P~ has fp32's exponent range to spare;
+  // fp16 and e4m3 P~ use their range for kKappa, and the fallback pass keeps
+  // each row's own maximum.
+  constexpr float kHeadroom = (kTensor && !kExact && kDt == kDtBf16) ? 8.f : 0.f;
   constexpr int kHalfD = D / 2;  // O columns this set rescales and writes
   volatile uint32_t* abort_flag = misc + 1;
   auto bar = [&](int i) -> uint32_t { return sb + L::kBars + 8 * i; };
@@ -448,7 +452,7 @@ __device__ __forceinline__ bool softmax_role(const FwdParams& p, uint8_t* smem, 
         m_row = fmaxf(m_row, rowmax);
       }
       const float Mc = (tmax == -INFINITY) ? -INFINITY : ceilf(tmax * c);
-      const bool any = named_bar_or(gbar_id, gbar_n, dead || Mc > M_prev);
+      const bool any = named_bar_or(gbar_id, gbar_n, dead || Mc > M_prev + kHeadroom);
       M_new = M_prev;
       if (any) {
         const float gmc = group_max(Mc);
@@ -469,7 +473,8 @@ __device__ __forceinline__ bool softmax_role(const FwdParams& p, uint8_t* smem, 
       }
       const float gm = (kExact || !kTensor) ? rowmax : tmax;
       if constexpr (kTensor) {
-        M_new = fmaxf(M_prev, (gm == -INFINITY) ? -INFINITY : ceilf(gm * c));
+        const float Mc = (gm == -INFINITY) ? -INFINITY : ceilf(gm * c);
+        M_new = Mc > M_prev + kHeadroom ? Mc : M_prev;
       } else {
         M_new = fmaxf(M_prev, (gm == -INFINITY) ? -INFINITY : gm * c);
       }
@@ -1050,7 +1055,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
           mma_ts<kE4M3>(tmem + buf * kBlockN + 64, tmem + buf * kBlockN + g * 8, ones_desc,
                         idesc_rs, g > 0);
       };
-      auto queue_s = [&](int jt, bool trc, bool k_ready = false) -> bool {
+      auto queue_s = [&](bool k_ready) -> bool {
         // a score buffer is written again only once the tensor row sum
         // that shared it has been read
         if (kLTensor && s_count >= kSBufs &&
@@ -1061,7 +1066,6 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
             !__all_sync(0xffffffffu,
                         wait_bounded(bar(L::bKFull + s_k.slot), s_k.phase, p, abort_flag)))
           return false;
-        if (trc && lane == 0) trace_at(p, 7, 0, jt);
         tc_fence_after();
         issue_s(s_buf.slot, s_k.slot);
         // (with at most three K stages "S done" also frees the K stage)
@@ -1099,7 +1103,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
               !(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bDecided), (seq - 1) & 1, p,
                                                           abort_flag))))
             break;
-          for (int jj = 0; ok && jj < min(kSBufs, n_kv_t); ++jj) ok = queue_s(-1, false);
+          for (int jj = 0; ok && jj < min(kSBufs, n_kv_t); ++jj) ok = queue_s(false);
           // every S MMA of the item issued: Q is free once they have completed
           if (ok && n_kv_t <= kSBufs) mma_commit(bar(L::bQFree));
 #pragma unroll 1
@@ -1119,7 +1123,6 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
               if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bVFull + p_v.slot),
                                                               p_v.phase, p, abort_flag))))
                 break;
-              if (trc && lane == 0) trace_at(p, 5, 0, j);
               if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bPFull + buf),
                                                               p_buf.phase, p, abort_flag))))
                 break;
@@ -1141,9 +1144,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
             mma_commit(bar(L::bOReady + buf));
             p_buf.next(kSBufs);
             p_v.next(SV);
-            if (trc && lane == 0) trace_at(p, 6, 0, j);
             if (more_s) {
-              if (!(ok = queue_s(j, trc, k_ready))) break;
+              if (!(ok = queue_s(k_ready))) break;
               if (j + kSBufs == n_kv_t - 1) mma_commit(bar(L::bQFree));
             }
             if (trc && lane == 0) trace_at(p, 4, 0, j);
@@ -1159,27 +1161,6 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
         // every MMA issued so far must finish before TMEM can be released
         mma_commit(bar(L::bDrain));
         wait_drain(bar(L::bDrain), 0);
-      }
-      __syncwarp();
-    } else if (warp == kObsWarp && p.trace != nullptr && blockIdx.x == 0) {
-      // Completion times of the first item's MMA groups, in the order the
-      // tensor pipe runs them (S_0, S_1, S_2, then O += P_j V, S_{j+3}):
-      // with the issue stamps they show whether the pipe idles between
-      // groups.  Waits without the abort flag and with a short limit, so
-      // observing never stops the kernel.
-      const int n = min(first.n_kv, kTraceIters);
-      auto seen = [&](int e, int j, int b) -> bool {
-        const uint64_t t0 = globaltimer_ns();
-        while (!mbar_try_wait(bar(b + j % kSBufs), (j / kSBufs) & 1))
-          if (*abort_flag || globaltimer_ns() - t0 > 100000000ull) return false;
-        if (lane == 0) trace_at(p, e, 0, j);
-        return true;
-      };
-      bool on = true;
-      for (int j = 0; on && j < min(kSBufs, n); ++j) on = seen(8, j, L::bSFull);
-      for (int j = 0; on && j < n; ++j) {
-        on = seen(9, j, L::bOReady);
-        if (on && j + kSBufs < n) on = seen(8, j + kSBufs, L::bSFull);
       }
       __syncwarp();
     }
