@@ -37,10 +37,10 @@ DEFAULT_WORKLOAD = "b2h16n8192d128_causal"
 METRIC = "attn fwd TFLOPS on 1 GB300 (bf16/fp8, causal+full) and % of dense tensor peak"
 L2_FLUSH_BYTES = 256 << 20
 
-# DRAM bytes (read + write) of one launch of the headline kernel from an ncu
-# capture, valid only for the kernel sources it was taken on (their hash);
-# the capture and its command are summarised in
-# profiles/fat_fwd_kernel_b2h16n8192d128_causal.md.
+# DRAM bytes (read + write) of one launch of the headline kernel from one
+# ncu capture (dram__bytes_read.sum + dram__bytes_write.sum).  The hash guards
+# it: the number is reported only while the CUDA sources hash to the value
+# they had when the capture was taken, and as null once they change.
 MEASURED_TRAFFIC = {
     "workload": "b2h16n8192d128_causal",
     "variant": "tensor",

@@ -185,7 +185,9 @@ int fat_attn_splitkv_default_splits(int B, int H, int Nq, int Nk);
  * (fat_attn_splitkv_workspace_bytes) exceeds it return FAT_ERR_INVALID_ARG
  * and launch nothing.  The first call on a device looks up the array's
  * device address (cudaGetSymbolAddress); make that first call before any
- * stream capture.  Nothing in the array needs to start at zero (each call
+ * stream capture.  If the lookup fails, that call returns FAT_ERR_LAUNCH and
+ * the next call on the device tries again.  Nothing in the array needs to
+ * start at zero (each call
  * writes every entry it reads), but all calls share it and it keeps the last
  * call's contents: calls whose work overlaps on the device race with each
  * other, so serialise them (for example on one stream).

@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -395,8 +396,8 @@ constexpr size_t kNoAllocScratchBytes = FAT_NOALLOC_SCRATCH_BYTES;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
 struct NoAllocScratch {
-  std::once_flag once;
-  void* ptr = nullptr;  // device address of g_noalloc_scratch on this device
+  std::mutex m;
+  std::atomic<void*> ptr{nullptr};  // device address of g_noalloc_scratch on this device
 };
 NoAllocScratch g_noalloc[kMaxDevices];
 
@@ -411,14 +412,23 @@ int fat_attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, fl
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FAT_ERR_LAUNCH;
   NoAllocScratch& c = g_noalloc[dev];
   // once per device, with that device current: the array's device address
-  // (in host code its name is only a host-side stand-in)
-  std::call_once(c.once, [&] {
-    void* addr = nullptr;
-    if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) == cudaSuccess) c.ptr = addr;
-  });
-  if (!c.ptr) return FAT_ERR_LAUNCH;
+  // (in host code its name is only a host-side stand-in).  Only a successful
+  // lookup is kept; a failed one is tried again by the next call.
+  void* ptr = c.ptr.load(std::memory_order_acquire);
+  if (!ptr) {
+    std::lock_guard<std::mutex> guard(c.m);
+    ptr = c.ptr.load(std::memory_order_relaxed);
+    if (!ptr) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) == cudaSuccess) {
+        c.ptr.store(addr, std::memory_order_release);
+        ptr = addr;
+      }
+    }
+  }
+  if (!ptr) return FAT_ERR_LAUNCH;
   return fat_attn_fwd_splitkv(q, k, v, o, lse, B, H, Nq, Nk, d, causal, scale, X, num_splits,
-                              c.ptr, kNoAllocScratchBytes, stream);
+                              ptr, kNoAllocScratchBytes, stream);
 }
 
 int fat_check_device_error(cudaStream_t stream) {

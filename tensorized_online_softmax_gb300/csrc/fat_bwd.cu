@@ -11,15 +11,18 @@ namespace {
 template <int D>
 int launch_bwd_d(const BwdParams& bp, const float* o, const void* dout, const float* lse, int dev,
                  cudaStream_t stream) {
+  // per device, once, whichever host thread launches first (1 = set up)
+  static std::once_flag once[kMaxDevices];
   static int ready[kMaxDevices];
   auto kern = fat_bwd_kernel<D>;
   const int smem = BwdSmem<D>::kAlloc;
-  if (!ready[dev]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-      return -4;
-    ready[dev] = 1;
-  }
+  std::call_once(once[dev], [&] {
+    ready[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
+                         cudaSuccess
+                     ? 1
+                     : -1;
+  });
+  if (ready[dev] != 1) return -4;
   const long long rows = static_cast<long long>(bp.BH) * bp.Npad;
   const int warps = 8;
   fat_bwd_prep_kernel<D><<<static_cast<unsigned>((rows + warps - 1) / warps), warps * 32, 0,

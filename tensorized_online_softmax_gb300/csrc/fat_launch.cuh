@@ -5,6 +5,8 @@
 
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "fat_fwd_kernel.cuh"
 
 namespace fat {
@@ -14,20 +16,24 @@ constexpr int kMaxDevices = 64;
 // Returns 0 or the fat_status code FAT_ERR_LAUNCH (-4).
 template <int D, int kX, bool kLTensor, int kDt, bool kZT = false>
 int launch_fwd(const FwdParams& fp, int dev, int grid, int splits, cudaStream_t stream) {
-  static int ready[kMaxDevices];  // per device: attributes checked and set
+  // per device, once, whichever host thread launches first: the attribute
+  // check and set-up below (1 = done, -1 = refused)
+  static std::once_flag once[kMaxDevices];
+  static int ready[kMaxDevices];
   auto kern = fat_fwd_kernel<D, kX, kLTensor, kDt, kZT>;
   const int smem = Smem<D, kDt == kDtE4M3, kZT>::kAlloc;
-  if (!ready[dev]) {
+  std::call_once(once[dev], [&] {
     // The warpgroup register split inside the kernel assumes exactly
     // kLaunchRegs registers per thread at launch; anything else could make
     // the register increase wait forever, so refuse to launch.
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess || fa.numRegs != kLaunchRegs) return -4;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-        cudaSuccess)
-      return -4;
-    ready[dev] = 1;
-  }
+    const bool ok =
+        cudaFuncGetAttributes(&fa, kern) == cudaSuccess && fa.numRegs == kLaunchRegs &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
+            cudaSuccess;
+    ready[dev] = ok ? 1 : -1;
+  });
+  if (ready[dev] != 1) return -4;
   kern<<<dim3(grid, splits), kNumThreads, smem, stream>>>(fp);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;
 }

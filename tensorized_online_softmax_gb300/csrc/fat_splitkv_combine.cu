@@ -42,11 +42,14 @@ __global__ void __launch_bounds__(256) splitkv_combine_kernel(const float* __res
 #pragma unroll
     for (int c = 0; c < kCols; ++c) acc[c] = fmaf(w, src[c], acc[c]);
   }
-  const float inv = 1.f / wsum;
+  // a row that no split reaches is empty: O = 0 and LSE = -inf, as the
+  // unsplit kernel writes it
+  const bool empty = !(wsum > 0.f);
+  const float inv = empty ? 0.f : 1.f / wsum;
   float* dst = o + row * D + lane * kCols;
 #pragma unroll
   for (int c = 0; c < kCols; ++c) dst[c] = acc[c] * inv;
-  if (lane == 0) lse[row] = m + __logf(wsum);
+  if (lane == 0) lse[row] = empty ? -INFINITY : m + __logf(wsum);
 }
 
 }  // namespace
