@@ -44,8 +44,8 @@ L2_FLUSH_BYTES = 256 << 20
 MEASURED_TRAFFIC = {
     "workload": "b2h16n8192d128_causal",
     "variant": "tensor",
-    "bytes": 252.452e6 + 104.104e6,
-    "csrc_sha256": "49454eabba38be46700c9ea13ebdbd63600cf417c25dae0a029010aee77c5e27",
+    "bytes": 255.952896e6 + 103.265792e6,
+    "csrc_sha256": "4588662d098e61c7d8c3662dd1752e584cb6f63b6e4c898c81548d309915cc10",
 }
 
 
@@ -268,6 +268,9 @@ def phase_trace(fat, torch, w, dev, variant, l_mode, stream, sm_mhz, peak_tflops
         ideal = 4.0 * 128 * 128 * w.d / flop_per_clk  # PV + S of one 128-row tile
         out["ideal_tensor_cycles"] = ideal
         out["vector_interval_ratio"] = max(0.0, 1.0 - ideal / period)
+    # the same at the nominal dense bf16 rate of one SM, 8192 flop per cycle
+    # (one 128 x 128 x 16 tcgen05 MMA per 64 cycles)
+    out["nominal_tensor_cycles"] = 4.0 * 128 * 128 * w.d / 8192
     return out
 
 
@@ -307,6 +310,60 @@ def time_variant(fat, torch, w, dev, args, variant, flush, stream, l_mode="vecto
     yield [s.elapsed_time(e) for s, e in zip(starts, ends)]
 
 
+def paired_times(fat, torch, w, dev, arms, pairs, flush, stream):
+    """Device times (ms) of `pairs` launches of each arm, interleaved launch by
+    launch (arm 0, arm 1, ..., then again) so that clock drift and box-to-box
+    differences cancel in the ratios; L2 flushed before each launch.  arms:
+    list of (variant, l_mode)."""
+    out = (torch.empty((w.B, w.H, w.N, w.d), dtype=torch.float32, device=dev["q"].device),
+           torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev["q"].device))
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(pairs)] for _ in arms]
+    with torch.cuda.stream(stream):
+        for i in range(pairs + 3):
+            for a, (variant, l_mode) in enumerate(arms):
+                flush.zero_()
+                if i >= 3:
+                    ev[a][i - 3][0].record(stream)
+                fat.attn_fwd(dev["q"], dev["k"], dev["v"], w.causal, w.scale, w.X,
+                             variant=variant, l_mode=l_mode, out=out, stream=stream)
+                if i >= 3:
+                    ev[a][i - 3][1].record(stream)
+        stream.synchronize()
+    return [[s.elapsed_time(e) for s, e in arm] for arm in ev]
+
+
+def sustained_run(fat, torch, w, dev, flush, stream, gpu_index, seconds=2.0, est_ms=1.0):
+    """The timed step (L2 flush + launch) back to back for about `seconds`, with
+    nvidia-smi sampling the clocks throughout (tens of samples, where the
+    timed region of a few steps gets one): TFLOP/s over that run, the clock
+    record, and device time x median SM clock per step."""
+    n = max(20, int(seconds * 1e3 / max(est_ms, 1e-3)))
+    out = (torch.empty((w.B, w.H, w.N, w.d), dtype=torch.float32, device=dev["q"].device),
+           torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev["q"].device))
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    sampler = ClockSampler(gpu_index)
+    sampler.start()
+    time.sleep(0.3)  # the sampler's first line
+    with torch.cuda.stream(stream):
+        for i in range(n):
+            flush.zero_()
+            starts[i].record(stream)
+            fat.attn_fwd(dev["q"], dev["k"], dev["v"], w.causal, w.scale, w.X, out=out,
+                         stream=stream)
+            ends[i].record(stream)
+        stream.synchronize()
+    clocks = sampler.stop()
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    avg = sum(ms) / n
+    res = {"steps": n, "ms_per_step": avg, "value": w.flops / (avg * 1e-3) / 1e12,
+           "unit": "TFLOP/s", "clocks": clocks}
+    if clocks.get("sm_mhz"):
+        res["kcycles_per_step_at_median_mhz"] = avg * 1e-3 * clocks["sm_mhz"] * 1e6 / 1e3
+    return res
+
+
 def run_all(args):
     """One JSON line per workload (results tables): both softmax variants for
     bf16, the tensorized one for e4m3, and split-KV decode shapes with their
@@ -325,24 +382,27 @@ def run_all(args):
             continue
         inp = gen.make_inputs(w)
         q, k, v = (inp[n].to(device) for n in ("q", "k", "v"))
+        out = (torch.empty((w.B, w.H, w.N, w.d), dtype=torch.float32, device=device),
+               torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=device))
+        kw = {}
+        if w.dtype == "e4m3":
+            kw = dict(dtype="e4m3", descales=(inp["q_descale"], inp["k_descale"], inp["v_descale"]))
         arms = {}
-        if w.dtype == "bf16":
-            for variant in ("tensor", "vec"):
-                ms = timeit(lambda: fat.attn_fwd(q, k, v, w.causal, w.scale, w.X, variant=variant),
-                            steps)
-                arms[variant] = {"ms": ms, "tflops": w.flops / ms / 1e9}
-        else:
-            ds = (inp["q_descale"], inp["k_descale"], inp["v_descale"])
-            for variant in ("tensor", "vec"):
-                ms = timeit(lambda: fat.attn_fwd(q, k, v, w.causal, w.scale, w.X, variant=variant,
-                                                 dtype="e4m3", descales=ds), steps)
-                arms[variant] = {"ms": ms, "tflops": w.flops / ms / 1e9}
+        sampler = ClockSampler(0)
+        sampler.start()
+        for variant in ("tensor", "vec"):
+            ms = timeit(lambda: fat.attn_fwd(q, k, v, w.causal, w.scale, w.X, variant=variant,
+                                             out=out, **kw), steps)
+            arms[variant] = {"ms": ms, "tflops": w.flops / ms / 1e9}
+        clocks = sampler.stop()
         peak = peaks["bf16_tflops"] * (2.0 if w.dtype == "e4m3" else 1.0)
         print(json.dumps({"workload": name, "dtype": w.dtype, "causal": w.causal, "X": w.X,
                           "arms": arms, "peak_tflops": peak,
                           "peak_source": peaks["source"] + (" bf16 x 2 (fp8 nominal ratio)"
                                                             if w.dtype == "e4m3" else " bf16"),
-                          "frac_tensor": arms["tensor"]["tflops"] / peak}), flush=True)
+                          "frac_tensor": arms["tensor"]["tflops"] / peak,
+                          "tensor_speedup_vs_vec": arms["vec"]["ms"] / arms["tensor"]["ms"],
+                          "clocks": clocks}), flush=True)
     for B, H, Nq, Nk, d in ((8, 32, 1, 16384, 128), (4, 32, 16, 32768, 128)):
         g = torch.Generator().manual_seed(2000 + Nq)
         q = torch.randn((B, H, Nq, d), generator=g).to(torch.bfloat16).to(device)
@@ -491,6 +551,10 @@ def main():
     ap.add_argument("--no-ablation", action="store_true", help="skip timing the vec variant")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--pairs", type=int, default=200,
+                    help="interleaved tensorized / vec launches of each arm for the ablation ratio")
+    ap.add_argument("--sustain-s", type=float, default=2.0,
+                    help="seconds of back-to-back steps with the clocks sampled (0: skip)")
     ap.add_argument("--all", action="store_true",
                     help="one line per workload (results tables) instead of the benchmark line")
     ap.add_argument("--sweep", action="store_true",
@@ -565,12 +629,22 @@ def main():
 
     ablation = None
     if not args.no_ablation and w.dtype == "bf16":
-        vt, _, _ = timed("vec", False)
+        # tensorized against the vector softmax: launches interleaved pair by
+        # pair, at least 200 of each
+        pairs = max(args.pairs, args.steps)
+        pt, pv = paired_times(fat, torch, w, dev, [("tensor", "vector"), ("vec", "vector")],
+                              pairs, flush, stream)
+        t_avg, v_avg = sum(pt) / pairs, sum(pv) / pairs
+        ratios = sorted(b / a for a, b in zip(pt, pv))
         lt, _, _ = timed("tensor", False, "tensor")
-        v_avg = sum(vt) / len(vt)
         l_avg = sum(lt) / len(lt)
-        ablation = {"vec_value": w.flops / (v_avg * 1e-3) / 1e12, "vec_ms_per_step": v_avg,
-                    "tensor_speedup_vs_vec": v_avg / avg_ms,
+        ablation = {"pairs": pairs,
+                    "tensor_value_paired": w.flops / (t_avg * 1e-3) / 1e12,
+                    "vec_value": w.flops / (v_avg * 1e-3) / 1e12, "vec_ms_per_step": v_avg,
+                    "tensor_speedup_vs_vec": v_avg / t_avg,
+                    "tensor_speedup_vs_vec_p10_p50_p90": [
+                        ratios[len(ratios) // 10], ratios[len(ratios) // 2],
+                        ratios[(9 * len(ratios)) // 10]],
                     "tensor_lsum_value": w.flops / (l_avg * 1e-3) / 1e12,
                     "tensor_lsum_ms_per_step": l_avg}
         if w.X == 128:
@@ -614,9 +688,14 @@ def main():
         e2e = {"value": w.flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
+    sustained = None
+    if rank == 0 and w.dtype == "bf16" and args.sustain_s > 0:
+        sustained = sustained_run(fat, torch, w, dev, flush, stream, local, args.sustain_s,
+                                  est_ms=avg_ms + 0.05)
+
     traces = None
     if w.dtype == "bf16" and w.N >= 2048:
-        mhz = (clocks or {}).get("sm_mhz")
+        mhz = ((sustained or {}).get("clocks") or {}).get("sm_mhz") or (clocks or {}).get("sm_mhz")
         traces = {"tensor": phase_trace(fat, torch, w, dev, "tensor", "vector", stream, mhz,
                                         peaks["bf16_tflops"]),
                   "vec": phase_trace(fat, torch, w, dev, "vec", "vector", stream, mhz,
@@ -639,7 +718,7 @@ def main():
                          "traffic": measured_traffic(w.name, "tensor"),
                          "peak_source": f"{peaks['source']} bf16 dense (burst)"},
             "ablation": ablation, "phase_trace": traces, "e2e": e2e, "cpu_baseline": cpu,
-            "gpu_launches": args.steps, "clocks": clocks,
+            "gpu_launches": args.steps, "clocks": clocks, "sustained": sustained,
             "wall_s_timed_region": wall,
         }
         print(json.dumps(line), flush=True)
