@@ -186,7 +186,8 @@ struct Smem {
   static constexpr int bQFree = bMReady + 2;         // every S MMA of an item has read Q
   static constexpr int bOFree = bQFree + 1;          // 8 arrivals: the epilogue has read O
   static constexpr int bDecided = bOFree + 1;        // 4 arrivals: set 0's detector done
-  static constexpr int bStageFree = bDecided + 1;    // 2 arrivals: O staging read by TMA
+  static constexpr int bStaged = bDecided + 1;       // 8 arrivals: a pass's O is staged
+  static constexpr int bStageFree = bStaged + 1;     // its stores have read the staging
   static constexpr int bListReady = bStageFree + 1;  // once: every first pass detected
   static constexpr int kNumBars = bListReady + 1;
   static constexpr int kRed = (kBars + 8 * kNumBars + 15) & ~15;  // float [2 sets][2 parity][4 warps]
@@ -198,13 +199,28 @@ struct Smem {
   static constexpr int kDefer = kMisc + 64;          // int [kMaxDeferred]: flagged items
   static constexpr int kBytes = kDefer + 4 * kMaxDeferred;
   static constexpr int kAlloc = kBytes + 1024;       // slack for 1024-byte alignment
-  // The epilogue stages O (fp32, 128 x D) in the V ring when it fits there,
-  // so that the next item's Q and K tiles can load meanwhile; otherwise from
-  // the start of the K ring (which then waits for the staging as well).
-  static constexpr int kStageBytes = kBlockM * D * 4;
-  static constexpr bool kStageInK = kVStages * kTile < kStageBytes;
-  static constexpr int kStage = kStageInK ? kK : kV;
-  static_assert(kStage + kStageBytes <= kOnes, "O staging overlaps the ones tile");
+  // The epilogue stages O (fp32, 128 x D) in the V ring, idle once O is
+  // final, as 16 KB boxes of 32 columns x 128 rows (128-byte swizzled) for
+  // the TMA tensor stores that the V producer issues.  Where the ring has
+  // room, the boxes skip the stage of the next pass's first V tile, so that
+  // tile loads while the last pass's O is still being written out.
+  static constexpr int kBoxes = D / 32;
+  static constexpr int kBoxesPerStage = kTile / 16384;
+  static constexpr bool kStageSkipsFirst = (kVStages - 1) * kBoxesPerStage >= kBoxes;
+  static_assert(kVStages * kTile >= kBlockM * D * 4, "O staging does not fit the V ring");
+  // offset of box b when the next pass's first V tile goes to stage v0
+  __device__ __forceinline__ static int box(int b, int v0) {
+    if constexpr (kStageSkipsFirst)
+      return kV + ((v0 + 1 + b / kBoxesPerStage) % kVStages) * kTile +
+             (b % kBoxesPerStage) * 16384;
+    return kV + b * 16384;
+  }
+  // whether V stage st holds part of that staging
+  __device__ __forceinline__ static bool holds_o(int st, int v0) {
+    if constexpr (kStageSkipsFirst)
+      return st != v0 && ((st - v0 - 1 + kVStages) % kVStages) * kBoxesPerStage < kBoxes;
+    return st * kBoxesPerStage < kBoxes;
+  }
   static_assert(kK % 1024 == 0 && kV % 1024 == 0 && kOnes % 1024 == 0, "tiles 1 KB aligned");
   static_assert(kAlloc <= 227 * 1024, "shared memory budget");
 };
@@ -673,18 +689,23 @@ __device__ __forceinline__ bool softmax_role(const FwdParams& p, uint8_t* smem, 
     __syncwarp();
     if (lane == 0) mbar_arrive(bar(L::bDecided));
   }
+  // the last pass's stores must have read their staging before this pass
+  // stages over it (long since, unless that pass was short)
+  if (ok && epi > 0)
+    ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bStageFree), (epi - 1) & 1, p, abort_flag));
   if (ok) {
     tc_fence_after();
     // epilogue: O / l, this set's half of the columns, staged in shared
     // memory as 128-byte-swizzled boxes of 32 columns x 128 rows for the TMA
     // store below
     const float inv_l = l_full > 0.f ? p.v_scale / l_full : 0.f;  // an empty row gets O = 0
+    const int v0 = (it0 + n_kv) % L::kVStages;  // the next pass's first V stage
 #pragma unroll
     for (int k = 0; k < kHalfD / 32; ++k) {
       uint32_t ov[32];
       tmem_ld32(o_taddr + set * kHalfD + 32 * k, ov);
       tmem_wait_ld(ov);
-      const uint32_t box = sb + L::kStage + (set * (kHalfD / 32) + k) * 16384 + r * 128;
+      const uint32_t box = sb + L::box(set * (kHalfD / 32) + k, v0) + r * 128;
       if (row_g < p.Nq) {  // (rows past N_q are clipped by the store anyway)
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc)
@@ -699,38 +720,19 @@ __device__ __forceinline__ bool softmax_role(const FwdParams& p, uint8_t* smem, 
   tc_fence_before();
   __syncwarp();
   if (lane == 0) mbar_arrive(bar(L::bOFree));
-  if (ok) {
-    fence_async_shared();
-    if (row_g < p.Nq && set == 0) {
-      const size_t out_row = (static_cast<size_t>(split) * (p.B * p.H) + bh) * p.Nq + row_g;
-      const float lsum = kLTensor ? l_full + delta_full : l_full;
-      (p.lse_part ? p.lse_part : p.lse)[out_row] =
-          l_full > 0.f ? (M_fin - kKappa + __log2f(lsum)) * kLn2 : -INFINITY;
-    }
+  if (ok && row_g < p.Nq && set == 0) {
+    const size_t out_row = (static_cast<size_t>(split) * (p.B * p.H) + bh) * p.Nq + row_g;
+    const float lsum = kLTensor ? l_full + delta_full : l_full;
+    (p.lse_part ? p.lse_part : p.lse)[out_row] =
+        l_full > 0.f ? (M_fin - kKappa + __log2f(lsum)) * kLn2 : -INFINITY;
   }
-  // One thread of the set stores its boxes once all four warps have staged
-  // their rows (rows past N_q are clipped by the tensor map), waits until the
-  // copy has read shared memory and signals that the staging area is free
-  // (the producer whose ring it overlaps waits for that).  Every warp of the
-  // set joins this barrier; a warp that gave up vetoes the store.
-  const bool veto = named_bar_or(kBarSet + set, 128, !ok);
-  if (q == 0 && lane == 0) {
-    if (!veto) {
-      const int row_block = p.o_part ? split * (p.B * p.H) + bh : bh;
-      // (fallback pass: the first pass's store of this tile, long since
-      // issued by this thread, must have landed before this one overwrites
-      // it)
-      if constexpr (kExact) bulk_wait_all();
-#pragma unroll
-      for (int k = 0; k < kHalfD / 32; ++k) {
-        const int b = set * (kHalfD / 32) + k;
-        tma_store_3d(&p.tm_o, sb + L::kStage + b * 16384, b * 32, m0, row_block);
-      }
-      bulk_commit();
-      bulk_wait_read();
-    }
-    mbar_arrive(bar(L::bStageFree));
-  }
+  // The staged boxes go to the async proxy, whose stores the V producer
+  // issues once all eight warps have arrived (every warp arrives, aborted or
+  // not; the producer stores nothing after an abort).  The softmax warps go
+  // straight on to the next pass.
+  fence_async_shared();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar(L::bStaged));
   if (tr && r == 0 && set == 0 && p.trace != nullptr && blockIdx.x == 0)
     p.trace[kTraceWords - 1] = static_cast<unsigned long long>(clock64());
   tc_fence_before();
@@ -839,7 +841,8 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
     mbar_init(bar(L::bQFree), 1);
     mbar_init(bar(L::bOFree), kSoftmaxWarps);
     mbar_init(bar(L::bDecided), kSoftmaxWarps / 2);
-    mbar_init(bar(L::bStageFree), 2);
+    mbar_init(bar(L::bStaged), kSoftmaxWarps);
+    mbar_init(bar(L::bStageFree), 1);
     mbar_init(bar(L::bListReady), 1);
     misc[1] = 0;
     misc[2] = 0;
@@ -913,9 +916,43 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
         const int empty = is_k ? L::bKEmpty : (SV == kSBufs ? L::bOReady : L::bVEmpty);
         const int ring = is_k ? L::kK : L::kV;
         const CUtensorMap* tm = is_k ? &p.tm_k : &p.tm_v;
-        // the ring that holds the staged O of the last pass refills only once
-        // that has been read
-        const bool waits_stage = !is_k || L::kStageInK;
+        // (V producer) the O of the last pass, staged in the V ring by the
+        // softmax warps: it is stored from here -- so no softmax warp waits
+        // for the store to read its staging -- and the ring stages that hold
+        // it refill only once the stores have read them
+        struct Pending {
+          int m0, bh, v0;
+          bool exact;
+        } pend{0, 0, 0, false};
+        bool has_pend = false;      // a pass whose O is yet to be stored
+        bool read_pending = false;  // stores issued whose shared-memory reads are not waited for
+        int staged_v0 = 0;          // first V stage of the pass after the stored one
+        int stored = 0;             // passes whose staging has been taken
+        auto store_staged = [&]() -> bool {
+          if (!wait_bounded(bar(L::bStaged), stored & 1, p, abort_flag)) return false;
+          ++stored;
+          has_pend = false;
+          if (*abort_flag) return false;
+          // (a fallback pass rewrites a tile stored before: that store must
+          // have landed first)
+          if (pend.exact) bulk_wait_all();
+          const int row_block = p.o_part ? split * BH + pend.bh : pend.bh;
+#pragma unroll
+          for (int b = 0; b < L::kBoxes; ++b)
+            tma_store_3d(&p.tm_o, sb + L::box(b, pend.v0), b * 32, pend.m0, row_block);
+          bulk_commit();
+          read_pending = true;
+          staged_v0 = pend.v0;
+          return true;
+        };
+        // once the stores have read the staging: its stages may refill, and
+        // the next pass may stage over it
+        auto release_staging = [&]() {
+          if (!read_pending) return;
+          bulk_wait_read();
+          read_pending = false;
+          mbar_arrive(bar(L::bStageFree));
+        };
         int issued = is_k ? k_pre : 0;  // tiles issued (the first K tiles during set-up)
         int q_issued = 1;               // Q tiles issued (the first during set-up)
         int seq = 0, it_base = 0;
@@ -958,11 +995,14 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
                 }
               }
             }
-            if (waits_stage && seq > 0 &&
-                !(ok = wait_bounded(bar(L::bStageFree), (seq - 1) & 1, p, abort_flag)))
-              break;
             for (int jj = issued - it_base; jj < w.n_kv; ++jj) {
               const int it = it_base + jj, st = it % S;
+              if (!is_k) {
+                // the last pass's O is stored before its stages are reused
+                // (after this pass's first V tile when the staging skips it)
+                if (has_pend && (jj > 0 || !L::kStageSkipsFirst) && !(ok = store_staged())) break;
+                if (read_pending && L::holds_o(st, staged_v0)) release_staging();
+              }
               if (is_k && L::kKFreeOnS) {
                 // K stage st is free once S_{it - S} has completed
                 if (it >= S && !(ok = wait_bounded(bar(L::bSFull + (it - S) % kSBufs),
@@ -978,9 +1018,18 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
               issued = it + 1;
             }
             if (!ok) break;
+            if (!is_k) {
+              if (has_pend && !(ok = store_staged())) break;
+              release_staging();
+              pend = {w.m0, w.bh, (it_base + w.n_kv) % SV, phase == 1};
+              has_pend = true;
+            }
             it_base += w.n_kv;
           }
         }
+        // the block's last pass; every store must have completed before exit
+        if (!is_k && ok && has_pend) store_staged();
+        if (!is_k) bulk_wait_all();
         if (*abort_flag) {
           // let every copy already issued land before the block can exit
           if (is_k) wait_drain(bar(L::bQFull), (q_issued - 1) & 1);
