@@ -422,7 +422,7 @@ def run_all(args):
 
 
 def event_timer(torch, device):
-    """fn, steps -> mean device time (ms) of fn over `steps` calls, each
+    """fn, steps -> median device time (ms) of fn over `steps` calls, each
     preceded by an L2 flush, after 3 untimed calls."""
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
 
@@ -430,7 +430,7 @@ def event_timer(torch, device):
         for _ in range(3):
             flush.zero_()
             fn()
-        tot = 0.0
+        ts = []
         for _ in range(steps):
             flush.zero_()
             s0, s1 = torch.cuda.Event(True), torch.cuda.Event(True)
@@ -438,8 +438,8 @@ def event_timer(torch, device):
             fn()
             s1.record()
             s1.synchronize()
-            tot += s0.elapsed_time(s1)
-        return tot / steps
+            ts.append(s0.elapsed_time(s1))
+        return statistics.median(ts)
 
     return timeit
 
