@@ -45,7 +45,7 @@ MEASURED_TRAFFIC = {
     "workload": "b2h16n8192d128_causal",
     "variant": "tensor",
     "bytes": 253.007616e6 + 102.856448e6,
-    "csrc_sha256": "1947867ffa69e96086d91f23f44dc656ce63c2257a57eccc22f0a67c8a95ba54",
+    "csrc_sha256": "10ab29d2c8170c8896ce85bbb32514a1225e436ca3e151ab2a4463714c35c1f8",
 }
 
 

@@ -15,13 +15,17 @@
 //
 //   warp 9      TMA producer of Q (once per item) and K_j, through an mbarrier ring;
 //   warp 10     TMA producer of V_j, through its own ring, so neither stream
-//               waits for a slot of the other (K runs three tiles ahead).
-//   warp 8      MMA issuer (one thread): S_j = Q K_j^T into buffer j % 3,
-//               O += P_j V_j, and (row sum on the tensor pipe) l_j = P_j 1.
+//               waits for a slot of the other (K runs three tiles ahead); it
+//               also issues the TMA stores of each item's O, which the
+//               softmax warps stage in the V ring.
+//   warp 8      MMA issuer (the whole warp, one elected lane per MMA group):
+//               S_j = Q K_j^T into buffer j % 3, O += P_j V_j, and (row sum on
+//               the tensor pipe) l_j = P_j 1.  The tensor pipe queues only a
+//               few MMAs, so this loop is kept short.
 //   warps 0-7   softmax in two sets of four: set w / 4 takes every other K/V
 //               tile; warp w owns TMEM lanes 32 (w % 4) .. +31 (one row per
 //               thread): row maximum, X-row tile maximum, O rescale,
-//               P = exp2(Z).
+//               P = exp2(Z); at the end of an item, O / l and LSE.
 //
 // TMEM (512 columns x 128 lanes, fp32): score buffers [0,128), [128,256),
 // [256,384); O at [384, 384 + D).  P_j overwrites the scores it came from
