@@ -333,6 +333,54 @@ def paired_times(fat, torch, w, dev, arms, pairs, flush, stream):
     return [[s.elapsed_time(e) for s, e in arm] for arm in ev]
 
 
+def other_configs(fat, torch, device, flush, stream, steps, peaks):
+    """The other workloads of the benchmark's config list, tensorized and vec
+    launches interleaved (`steps` of each, L2 flushed before each): TFLOP/s,
+    fraction of the dense peak (fp8: 2x bf16, the nominal ratio) and the
+    tensorized / vec ratio, with the clocks of the whole measurement."""
+    from tensorized_online_softmax_gb300 import inputs as gen
+
+    names = ("b4h16n2048d128", "b4h16n2048d128_causal", "stress_b1h32n16384d64",
+             "fp8_b4h16n4096d128")
+    sampler = ClockSampler(device.index or 0)
+    sampler.start()
+    out = {}
+    for name in names:
+        w = gen.WORKLOADS[name]
+        inp = gen.make_inputs(w)
+        q, k, v = (inp[n].to(device) for n in ("q", "k", "v"))
+        o = torch.empty((w.B, w.H, w.N, w.d), dtype=torch.float32, device=device)
+        lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=device)
+        kw = {}
+        if w.dtype == "e4m3":
+            kw = dict(dtype="e4m3", descales=(inp["q_descale"], inp["k_descale"], inp["v_descale"]))
+        ts = {"tensor": [], "vec": []}
+        with torch.cuda.stream(stream):
+            for i in range(steps + 3):
+                for variant in ("tensor", "vec"):
+                    flush.zero_()
+                    e0 = torch.cuda.Event(enable_timing=True)
+                    e1 = torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    fat.attn_fwd(q, k, v, w.causal, w.scale, w.X, variant=variant, out=(o, lse),
+                                 stream=stream, **kw)
+                    e1.record(stream)
+                    if i >= 3:
+                        ts[variant].append((e0, e1))
+            stream.synchronize()
+        ms = {a: statistics.median(s_.elapsed_time(e_) for s_, e_ in ts[a]) for a in ts}
+        peak = peaks["bf16_tflops"] * (2.0 if w.dtype == "e4m3" else 1.0)
+        out[name] = {"dtype": w.dtype, "causal": w.causal, "X": w.X,
+                     "tensor_tflops": w.flops / ms["tensor"] / 1e9,
+                     "vec_tflops": w.flops / ms["vec"] / 1e9,
+                     "tensor_ms": ms["tensor"], "vec_ms": ms["vec"],
+                     "frac_tensor": w.flops / ms["tensor"] / 1e9 / peak,
+                     "tensor_speedup_vs_vec": ms["vec"] / ms["tensor"]}
+    out["clocks"] = sampler.stop()
+    out["steps_per_arm"] = steps
+    return out
+
+
 def sustained_run(fat, torch, w, dev, flush, stream, gpu_index, seconds=2.0, est_ms=1.0):
     """The timed step (L2 flush + launch) back to back for about `seconds`, with
     nvidia-smi sampling the clocks throughout (tens of samples, where the
@@ -555,6 +603,8 @@ def main():
                     help="interleaved tensorized / vec launches of each arm for the ablation ratio")
     ap.add_argument("--sustain-s", type=float, default=2.0,
                     help="seconds of back-to-back steps with the clocks sampled (0: skip)")
+    ap.add_argument("--other-steps", type=int, default=20,
+                    help="launches per arm of each other workload in the line (0: skip)")
     ap.add_argument("--all", action="store_true",
                     help="one line per workload (results tables) instead of the benchmark line")
     ap.add_argument("--sweep", action="store_true",
@@ -693,6 +743,10 @@ def main():
         sustained = sustained_run(fat, torch, w, dev, flush, stream, local, args.sustain_s,
                                   est_ms=avg_ms + 0.05)
 
+    others = None
+    if rank == 0 and args.other_steps > 0 and args.workload == DEFAULT_WORKLOAD:
+        others = other_configs(fat, torch, device, flush, stream, args.other_steps, peaks)
+
     traces = None
     if w.dtype == "bf16" and w.N >= 2048:
         mhz = ((sustained or {}).get("clocks") or {}).get("sm_mhz") or (clocks or {}).get("sm_mhz")
@@ -719,6 +773,7 @@ def main():
                          "peak_source": f"{peaks['source']} bf16 dense (burst)"},
             "ablation": ablation, "phase_trace": traces, "e2e": e2e, "cpu_baseline": cpu,
             "gpu_launches": args.steps, "clocks": clocks, "sustained": sustained,
+            "other_configs": others,
             "wall_s_timed_region": wall,
         }
         print(json.dumps(line), flush=True)
