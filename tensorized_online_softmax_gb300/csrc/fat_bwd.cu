@@ -1,8 +1,9 @@
-// Backward-pass launchers: the D / LSE preparation and the fused kernel for
-// d = 64 and d = 128 (see fat_bwd_kernel.cuh).
+// Backward-pass launchers: the D / LSE preparation and the fused kernel:
+// fat_bwd_kernel for d = 128, fat_bwd_q2_kernel (a second Q stage) for d = 64.
 #include <cuda_runtime.h>
 
 #include "fat_bwd_kernel.cuh"
+#include "fat_bwd_q2_kernel.cuh"
 #include "fat_launch.cuh"
 
 namespace fat {
@@ -14,8 +15,14 @@ int launch_bwd_d(const BwdParams& bp, const float* o, const void* dout, const fl
   // per device, once, whichever host thread launches first (1 = set up)
   static std::once_flag once[kMaxDevices];
   static int ready[kMaxDevices];
-  auto kern = fat_bwd_kernel<D>;
-  const int smem = BwdSmem<D>::kAlloc;
+  auto kern = [] {
+    if constexpr (D == 64) return fat_bwd_q2_kernel<D>;
+    else return fat_bwd_kernel<D>;
+  }();
+  const int smem = [] {
+    if constexpr (D == 64) return BwdSmemQ2<D>::kAlloc;
+    else return BwdSmem<D>::kAlloc;
+  }();
   std::call_once(once[dev], [&] {
     ready[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
                          cudaSuccess
