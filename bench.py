@@ -39,8 +39,9 @@ L2_FLUSH_BYTES = 256 << 20
 
 # DRAM bytes (read + write) of one launch of the headline kernel from one
 # ncu capture (dram__bytes_read.sum + dram__bytes_write.sum).  The hash guards
-# it: the number is reported only while the CUDA sources hash to the value
-# they had when the capture was taken, and as null once they change.
+# it: the number is reported only while the forward kernel's sources
+# (FWD_SOURCES below) hash to the value they had when the capture was taken,
+# and as null once they change.
 MEASURED_TRAFFIC = {
     "workload": "b2h16n8192d128_causal",
     "variant": "tensor",
