@@ -13,6 +13,8 @@
 //                           tensor reduce-adds
 //
 // with D_i = sum_d dO_id O_id formed beforehand (fat_bwd_prep_kernel).
+// This schedule serves d = 128; d = 64, whose tiles leave room for a second
+// Q stage, runs fat_bwd_q2_kernel (fat_bwd_q2_kernel.cuh) instead.
 // One CTA per 128-key block of one (b, h); it walks the query blocks that
 // see those keys (all of them, or those at or after the diagonal when
 // causal).  Warps: 0-7 form P^T and dS^T (warp w: key rows 32 (w % 4) ..,
