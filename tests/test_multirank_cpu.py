@@ -45,3 +45,19 @@ def test_two_rank_timing_takes_the_slowest_rank():
 def test_single_rank_is_identity():
     assert bench.max_over_ranks(12.5, None) == 12.5
     assert bench.whole_job_tflops(1, 2e12, 5, 1000.0) == pytest.approx(10.0)
+
+
+def test_traffic_record_follows_the_forward_kernel_sources():
+    """The per-launch DRAM traffic in the bench line is reported only while the
+    forward kernel's sources are those of the capture: every listed source
+    exists, and the record is found for the headline workload and variant
+    only."""
+    d = os.path.join(bench.ROOT, "tensorized_online_softmax_gb300", "csrc")
+    for name in bench.FWD_SOURCES:
+        assert os.path.isfile(os.path.join(d, name)), name
+    assert len(bench.csrc_sha256()) == 64
+    rec = bench.MEASURED_TRAFFIC
+    if rec["csrc_sha256"] == bench.csrc_sha256():
+        assert bench.measured_traffic(rec["workload"], rec["variant"]) == rec["bytes"]
+    assert bench.measured_traffic(rec["workload"], "vec") is None
+    assert bench.measured_traffic("no_such_workload", rec["variant"]) is None
