@@ -46,7 +46,7 @@ MEASURED_TRAFFIC = {
     "workload": "b2h16n8192d128_causal",
     "variant": "tensor",
     "bytes": 253.007616e6 + 102.856448e6,
-    "csrc_sha256": "5705cd5dcd4fe83d1d132ea58076576999474505ab8a97a6eec5796a459ffe2c",
+    "csrc_sha256": "16754c34263816e3e6a01e680971241713fe556ea579def2e2cd9b8917e1e63e",
 }
 
 

@@ -21,7 +21,9 @@
 //   warp 8      MMA issuer (the whole warp, one elected lane per MMA group):
 //               S_j = Q K_j^T into buffer j % 3, O += P_j V_j, and (row sum on
 //               the tensor pipe) l_j = P_j 1.  The tensor pipe queues only a
-//               few MMAs, so this loop is kept short.
+//               few MMAs, so this loop is kept short.  At d = 64 warp 8
+//               issues only the S MMAs and warp 11 the P V MMAs (and row
+//               sums), so that P V goes in as soon as P is ready.
 //   warps 0-7   softmax in two sets of four: set w / 4 takes every other K/V
 //               tile; warp w owns TMEM lanes 32 (w % 4) .. +31 (one row per
 //               thread): row maximum, X-row tile maximum, O rescale,
@@ -49,6 +51,7 @@ constexpr int kSoftmaxWarps = 8;
 constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;    // Q and K
 constexpr int kLoadVWarp = 10;  // V; warp 11 completes the third warpgroup
+constexpr int kPvWarp = 11;     // (d = 64) issues O += P V while warp 8 issues S = Q K^T
 constexpr int kNumThreads = 384;
 // Register budget: 384 threads launch with kLaunchRegs each; the MMA/TMA
 // warpgroup drops to kCtrlRegs and the two softmax warpgroups rise to
@@ -193,7 +196,10 @@ struct Smem {
   static constexpr int bStaged = bDecided + 1;       // 8 arrivals: a pass's O is staged
   static constexpr int bStageFree = bStaged + 1;     // its stores have read the staging
   static constexpr int bListReady = bStageFree + 1;  // once: every first pass detected
-  static constexpr int kNumBars = bListReady + 1;
+  // (d = 64: two MMA issuers) the P V issuer's drain after an abort
+  static constexpr bool kTwoIssuers = D == 64;
+  static constexpr int bDrainPv = bListReady + 1;
+  static constexpr int kNumBars = bListReady + 1 + (kTwoIssuers ? 1 : 0);
   static constexpr int kRed = (kBars + 8 * kNumBars + 15) & ~15;  // float [2 sets][2 parity][4 warps]
   static constexpr int kMRow = kRed + 64;            // float [2 sets][128 rows]: offsets
   static constexpr int kFin = kMRow + 1024;          // float [2 epilogues][4][2 sets][128 rows]
@@ -769,6 +775,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
   constexpr int SK = L::kKStages;
   constexpr int SV = L::kVStages;
   constexpr bool kTensor = kX > 0;
+  constexpr bool kTwoIssuers = L::kTwoIssuers;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -840,6 +847,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
     }
     mbar_init(bar(L::bOFinal), 1);
     mbar_init(bar(L::bDrain), 1);
+    if constexpr (L::kTwoIssuers) mbar_init(bar(L::bDrainPv), 1);
     mbar_init(bar(L::bMReady + 0), kSoftmaxWarps / 2);
     mbar_init(bar(L::bMReady + 1), kSoftmaxWarps / 2);
     mbar_init(bar(L::bQFree), 1);
@@ -1042,7 +1050,149 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
         }
       }
       __syncwarp();
-    } else if (warp == kMmaWarp) {
+    } else if (warp == kMmaWarp || (kTwoIssuers && warp == kPvWarp)) {
+      if constexpr (kTwoIssuers) {
+      // =================== MMA issuers ===================
+      // Warp 8 issues S_it = Q K_it^T into buffer it % 3 once O += P_{it-3} V
+      // (the buffer's last reader) has completed; warp 11 issues O += P_it V
+      // once P~_it and V_it are there.  Two issuers, so that neither waits
+      // behind the other's queue: the P V MMAs go in as soon as P~ is ready.
+      // Each warp issues with one elected lane; each commit tracks only its
+      // own warp's MMAs.
+      const bool pv_role = warp == kPvWarp;
+      constexpr uint32_t kFmt = kDt == kDtBf16 ? 1u : 0u;
+      constexpr uint32_t idesc_s = idesc_f32acc<kFmt>(kBlockM, kBlockN, false);
+      constexpr uint32_t idesc_pv = idesc_f32acc<kFmt>(kBlockM, D, true);
+      constexpr uint32_t idesc_rs = idesc_f32acc<kFmt>(kBlockM, 16, false);
+      const uint64_t ones_desc = sdesc_sw128(sb + L::kOnes, 16, 1024);
+      const uint64_t q_desc = sdesc_sw128(sb + L::kQ, 16, 1024);
+      const uint64_t k_desc = sdesc_sw128(sb + L::kK, 16, 1024);
+      const uint64_t v_desc = sdesc_sw128(sb + L::kV, 16384, 1024);
+      const uint64_t zbias_desc = sdesc_plain(sb + L::kZBias, 128, 256);
+      const uint64_t zones_desc = sdesc_plain(sb + L::kZOnes, 128, 256);
+      struct Ring {  // a slot of an n-deep ring and the parity of its phase
+        int slot = 0;
+        uint32_t phase = 0;
+        __device__ __forceinline__ void next(int n) {
+          if (++slot == n) {
+            slot = 0;
+            phase ^= 1u;
+          }
+        }
+      };
+      auto issue_s = [&](int buf, int kst) {
+        const uint64_t kd = k_desc + static_cast<uint32_t>((kst * L::kTile) >> 4);
+        const uint32_t d_t = tmem + buf * kBlockN;
+#pragma unroll
+        for (int g = 0; g < D / L::kMmaK / 4; ++g)
+          mma_ss_x4<kE4M3, 2>(d_t, q_desc + g * 1024, kd + g * 1024, idesc_s, g > 0);
+        if constexpr (kZT)
+          mma_ss<false>(d_t, zbias_desc + static_cast<uint32_t>((buf * 4096) >> 4), zones_desc,
+                        idesc_s, 1u);
+      };
+      auto issue_pv = [&](int buf, int vst, bool acc) {
+        const uint64_t vd = v_desc + static_cast<uint32_t>((vst * L::kTile) >> 4);
+#pragma unroll
+        for (int g = 0; g < kBlockN / L::kMmaK / 4; ++g)
+          mma_ts_x4<kE4M3, 8, (L::kPvStep >> 4)>(
+              tmem + kOCol, tmem + buf * kBlockN + g * 32,
+              vd + static_cast<uint32_t>(g * 4 * (L::kPvStep >> 4)), idesc_pv, acc || g > 0);
+      };
+      auto issue_rs = [&](int buf) {
+#pragma unroll
+        for (int g = 0; g < kBlockN / L::kMmaK; ++g)
+          mma_ts<kE4M3>(tmem + buf * kBlockN + 64, tmem + buf * kBlockN + g * 8, ones_desc,
+                        idesc_rs, g > 0);
+      };
+      auto wait_all = [&](uint32_t b, uint32_t par) -> bool {
+        return __all_sync(0xffffffffu, wait_bounded(b, par, p, abort_flag));
+      };
+      Ring buf_r, k_r, v_r;   // score buffer, K stage (S role), V stage (P V role)
+      Ring free_r;            // (S role) the buffer's previous tile, three back
+      int s_total = 0;        // (S role) S tiles issued so far
+      bool ok = true;
+      int seq = 0;
+#pragma unroll 1
+      for (int phase = 0; phase < 2 && ok; ++phase) {
+        int count = 0;
+        if (phase == 1) {
+          if (!(ok = wait_all(bar(L::bListReady), 0))) break;
+          count = min(static_cast<int>(misc[2]), kMaxDeferred);
+        }
+#pragma unroll 1
+        for (int k = 0; ok; ++k, ++seq) {
+          const int idx = phase == 0 ? fwd_item_at(p, k) : (k < count ? deferred[k] : -1);
+          if (idx < 0) break;
+          const int n_kv_t = item(idx).n_kv;
+          const bool trc = seq == 0 && p.trace != nullptr && blockIdx.x == 0;
+          if (!pv_role) {
+            if (!(ok = wait_all(bar(L::bQFull), seq & 1))) break;
+            // (kZT) the bias tiles are zero again once the last item's
+            // detector has run
+            if (kZT && seq > 0 && !(ok = wait_all(bar(L::bDecided), (seq - 1) & 1))) break;
+#pragma unroll 1
+            for (int jj = 0; jj < n_kv_t; ++jj) {
+              if (s_total >= kSBufs) {
+                // O += P~ V of the buffer's last tile has read it (and, with
+                // the tensor row sum, its row sum has been read)
+                if (!(ok = wait_all(bar(L::bOReady + free_r.slot), free_r.phase))) break;
+                if (kLTensor &&
+                    !(ok = wait_all(bar(L::bLFree + free_r.slot), free_r.phase))) break;
+                free_r.next(kSBufs);
+              }
+              if (!(ok = wait_all(bar(L::bKFull + k_r.slot), k_r.phase))) break;
+              tc_fence_after();
+              issue_s(buf_r.slot, k_r.slot);
+              mma_commit(bar(L::bSFull + buf_r.slot));
+              if constexpr (!L::kKFreeOnS) mma_commit(bar(L::bKEmpty + k_r.slot));
+              if (trc && lane == 0 && jj >= kSBufs) trace_at(p, 4, 0, jj - kSBufs);
+              buf_r.next(kSBufs);
+              k_r.next(SK);
+              ++s_total;
+            }
+            if (!ok) break;
+            // every S MMA of the item issued: Q is free once they have completed
+            mma_commit(bar(L::bQFree));
+          } else {
+#pragma unroll 1
+            for (int j = 0; j < n_kv_t; ++j) {
+              const bool v_ok = mbar_test_wait(bar(L::bVFull + v_r.slot), v_r.phase);
+              const bool p_ok = mbar_test_wait(bar(L::bPFull + buf_r.slot), buf_r.phase);
+              if (__ballot_sync(0xffffffffu, v_ok && p_ok) != 0xffffffffu) {
+                if (!(ok = wait_all(bar(L::bVFull + v_r.slot), v_r.phase))) break;
+                if (!(ok = wait_all(bar(L::bPFull + buf_r.slot), buf_r.phase))) break;
+              }
+              // the first O = P V of an item overwrites O: the last epilogue
+              // must have read it
+              if (j == 0 && seq > 0 && !(ok = wait_all(bar(L::bOFree), (seq - 1) & 1))) break;
+              if (trc && lane == 0) trace_at(p, 3, 0, j);
+              tc_fence_after();
+              if (kLTensor) {
+                issue_rs(buf_r.slot);
+                mma_commit(bar(L::bRsFull + buf_r.slot));
+              }
+              issue_pv(buf_r.slot, v_r.slot, j > 0);
+              if (SV != kSBufs) mma_commit(bar(L::bVEmpty + v_r.slot));
+              mma_commit(bar(L::bOReady + buf_r.slot));
+              buf_r.next(kSBufs);
+              v_r.next(SV);
+            }
+            if (!ok) break;
+            mma_commit(bar(L::bOFinal));
+          }
+        }
+      }
+      if (ok) {
+        // the last item's "Q read" is waited for by no one else
+        if (!pv_role && seq > 0) wait_drain(bar(L::bQFree), (seq - 1) & 1);
+      } else {
+        // every MMA this warp issued must finish before TMEM can be released
+        const uint32_t db = bar(pv_role ? L::bDrainPv : L::bDrain);
+        mma_commit(db);
+        wait_drain(db, 0);
+      }
+      __syncwarp();
+      } else {
       // =================== MMA issuer ===================
       // The whole warp runs this code with warp-uniform values; one elected
       // lane issues each MMA and commit.
@@ -1216,6 +1366,7 @@ __global__ void __launch_bounds__(kNumThreads, 1) fat_fwd_kernel(const __grid_co
         wait_drain(bar(L::bDrain), 0);
       }
       __syncwarp();
+      }
     }
     __syncthreads();
     tc_fence_after();
