@@ -417,10 +417,44 @@ def sustained_run(fat, torch, w, dev, flush, stream, gpu_index, seconds=2.0, est
     return res
 
 
+DECODE_SHAPES = ((8, 32, 1, 16384, 128), (4, 32, 16, 32768, 128))  # B, H, Nq, Nk, d
+
+
+def decode_lines(fat, torch, device, timeit, peaks, steps):
+    """Split-KV decode shapes, one JSON line each, with their HBM roofline (K
+    and V read once: 2 * B * H * Nk * d * 2 bytes)."""
+    for B, H, Nq, Nk, d in DECODE_SHAPES:
+        g = torch.Generator().manual_seed(2000 + Nq)
+        q = torch.randn((B, H, Nq, d), generator=g).to(torch.bfloat16).to(device)
+        k = torch.randn((B, H, Nk, d), generator=g).to(torch.bfloat16).to(device)
+        v = torch.randn((B, H, Nk, d), generator=g).to(torch.bfloat16).to(device)
+        splits = fat.load_library().fat_attn_splitkv_default_splits(B, H, Nq, Nk)
+        ws = torch.empty(fat.load_library().fat_attn_splitkv_workspace_bytes(B, H, Nq, d, splits),
+                         dtype=torch.uint8, device=device)
+        ms = timeit(lambda: fat.attn_fwd_splitkv(q, k, v, False, None, 128, splits, workspace=ws),
+                    steps)
+        kv_bytes = 2.0 * B * H * Nk * d * 2
+        print(json.dumps({"workload": f"decode_b{B}h{H}q{Nq}k{Nk}d{d}", "splits": splits,
+                          "ms": ms, "tflops": 4.0 * B * H * Nq * Nk * d / ms / 1e9,
+                          "hbm_gbs": kv_bytes / ms / 1e6, "hbm_peak_gbs": peaks["hbm_gbs"],
+                          "frac_hbm": kv_bytes / ms / 1e6 / peaks["hbm_gbs"]}), flush=True)
+
+
+def run_decode(args):
+    """Only the split-KV decode lines of --all."""
+    import torch
+
+    import tensorized_online_softmax_gb300 as fat
+
+    device = torch.device("cuda", 0)
+    decode_lines(fat, torch, device, event_timer(torch, device), load_peaks(),
+                 max(1, min(args.steps, 100)))
+
+
 def run_all(args):
     """One JSON line per workload (results tables): both softmax variants for
-    bf16, the tensorized one for e4m3, and split-KV decode shapes with their
-    HBM roofline (K and V read once: 2 * B * H * Nk * d * 2 bytes)."""
+    bf16, the tensorized one for e4m3, the split-KV decode shapes
+    (decode_lines) and the backward pass."""
     import torch
 
     import tensorized_online_softmax_gb300 as fat
@@ -456,21 +490,7 @@ def run_all(args):
                           "frac_tensor": arms["tensor"]["tflops"] / peak,
                           "tensor_speedup_vs_vec": arms["vec"]["ms"] / arms["tensor"]["ms"],
                           "clocks": clocks}), flush=True)
-    for B, H, Nq, Nk, d in ((8, 32, 1, 16384, 128), (4, 32, 16, 32768, 128)):
-        g = torch.Generator().manual_seed(2000 + Nq)
-        q = torch.randn((B, H, Nq, d), generator=g).to(torch.bfloat16).to(device)
-        k = torch.randn((B, H, Nk, d), generator=g).to(torch.bfloat16).to(device)
-        v = torch.randn((B, H, Nk, d), generator=g).to(torch.bfloat16).to(device)
-        splits = fat.load_library().fat_attn_splitkv_default_splits(B, H, Nq, Nk)
-        ws = torch.empty(fat.load_library().fat_attn_splitkv_workspace_bytes(B, H, Nq, d, splits),
-                         dtype=torch.uint8, device=device)
-        ms = timeit(lambda: fat.attn_fwd_splitkv(q, k, v, False, None, 128, splits, workspace=ws),
-                    steps)
-        kv_bytes = 2.0 * B * H * Nk * d * 2
-        print(json.dumps({"workload": f"decode_b{B}h{H}q{Nq}k{Nk}d{d}", "splits": splits,
-                          "ms": ms, "tflops": 4.0 * B * H * Nq * Nk * d / ms / 1e9,
-                          "hbm_gbs": kv_bytes / ms / 1e6, "hbm_peak_gbs": peaks["hbm_gbs"],
-                          "frac_hbm": kv_bytes / ms / 1e6 / peaks["hbm_gbs"]}), flush=True)
+    decode_lines(fat, torch, device, timeit, peaks, steps)
     run_bwd(args, BWD_WORKLOADS, steps)
 
 
@@ -616,6 +636,8 @@ def main():
                     help="the pages' fp16 / fp8 sweep, one line per shape")
     ap.add_argument("--bwd", action="store_true",
                     help="time the backward pass on --workload (bf16) only, one line")
+    ap.add_argument("--decode", action="store_true",
+                    help="only the split-KV decode lines of --all")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.bwd:
@@ -626,6 +648,9 @@ def main():
         return
     if args.all:
         run_all(args)
+        return
+    if args.decode:
+        run_decode(args)
         return
 
     from tensorized_online_softmax_gb300 import inputs as gen
