@@ -20,9 +20,11 @@
 // causal).  Warps: 0-7 form P^T and dS^T (warp w: key rows 32 (w % 4) ..,
 // query columns 64 (w / 4) ..) and then stage the block's dQ partial from
 // TMEM in shared memory; 8 issues the MMAs; 9 loads K and V once and Q, dO,
-// log2(e) LSE and D per query block with TMA; 10 adds each staged dQ
+// -log2(e) LSE and -scale D per query block with TMA; 10 adds each staged dQ
 // partial into global dQ with TMA reduce-adds.
 #pragma once
+
+#include <climits>
 
 #include "fat_fwd_kernel.cuh"
 
@@ -34,8 +36,8 @@ struct BwdParams {
   CUtensorMap tm_v;
   CUtensorMap tm_do;
   CUtensorMap tm_dq;  // fp32 [B*H, N, d], boxes of 32 columns x 128 rows, 128-byte swizzle
-  const float* lse2;  // [B*H][Npad] log2(e) * LSE; +inf for rows >= N
-  const float* dvec;  // [B*H][Npad] D; 0 for rows >= N
+  const float* lse2;  // [B*H][Npad] -log2(e) * LSE; -inf for rows >= N
+  const float* dvec;  // [B*H][Npad] -scale * D; 0 for rows >= N
   float* dq;          // fp32 [B*H, N, d], zero on entry, accumulated by TMA reduce-adds
   float* dk;          // fp32 [B*H, N, d]
   float* dv;          // fp32 [B*H, N, d]
@@ -62,6 +64,63 @@ struct BwdColDQ {
   static constexpr int value = 256 + 3 * D <= 512 ? 256 + 2 * D : kBwdColDP;
 };
 
+// Two fp32 pairs from shared memory (16-byte aligned address).
+__device__ __forceinline__ void ld_shared_2xf2(uint32_t addr, uint64_t& a, uint64_t& b) {
+  asm volatile("ld.shared.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "r"(addr));
+}
+
+// P^T of one 32-column chunk of a thread's key row, in place over its scores
+// s (fp32 bits): exp2(c S^T - log2(e) LSE) with -log2(e) LSE of the chunk's
+// 32 queries at nlse (shared memory), one f32x2 FMA per pair of columns;
+// pk receives the bf16 pairs for TMEM.  kMasked: columns below lim (causal)
+// are zero; callers pass lim = INT_MAX for a key row past N.
+template <bool kMasked>
+__device__ __forceinline__ void bwd_p_chunk(uint32_t (&s)[32], uint32_t (&pk)[16], uint32_t nlse,
+                                            uint64_t c2, int col0, int lim) {
+#pragma unroll
+  for (int i4 = 0; i4 < 8; ++i4) {
+    uint64_t nl[2];
+    ld_shared_2xf2(nlse + 16 * i4, nl[0], nl[1]);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = 4 * i4 + 2 * h;
+      float z0, z1;
+      f2_unpack(f2_fma(f2_pack(__uint_as_float(s[i]), __uint_as_float(s[i + 1])), c2, nl[h]), z0,
+                z1);
+      float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
+      if constexpr (kMasked) {
+        p0 = col0 + i >= lim ? p0 : 0.f;
+        p1 = col0 + i + 1 >= lim ? p1 : 0.f;
+      }
+      s[i] = __float_as_uint(p0);
+      s[i + 1] = __float_as_uint(p1);
+      pk[2 * i4 + h] = pack_bf16x2(p0, p1);
+    }
+  }
+}
+
+// dS^T of one 32-column chunk: P^T (fp32 bits, p) times
+// scale dP^T - scale D, with -scale D of the chunk's queries at nsd (shared
+// memory): one f32x2 FMA and one f32x2 multiply per pair of columns; dsk
+// receives the bf16 pairs.
+__device__ __forceinline__ void bwd_ds_chunk(const uint32_t (&p)[32], const uint32_t (&dp)[32],
+                                             uint32_t (&dsk)[16], uint32_t nsd, uint64_t sc2) {
+#pragma unroll
+  for (int i4 = 0; i4 < 8; ++i4) {
+    uint64_t nd[2];
+    ld_shared_2xf2(nsd + 16 * i4, nd[0], nd[1]);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = 4 * i4 + 2 * h;
+      const uint64_t u =
+          f2_fma(f2_pack(__uint_as_float(dp[i]), __uint_as_float(dp[i + 1])), sc2, nd[h]);
+      float d0, d1;
+      f2_unpack(f2_mul(f2_pack(__uint_as_float(p[i]), __uint_as_float(p[i + 1])), u), d0, d1);
+      dsk[2 * i4 + h] = pack_bf16x2(d0, d1);
+    }
+  }
+}
+
 template <int D>
 struct BwdSmem {
   static constexpr int kTile = 128 * D * 2;  // one 128 x D bf16 tile
@@ -73,10 +132,10 @@ struct BwdSmem {
   // the dQ partial of a query block: fp32, 128-byte-swizzled boxes of 32
   // columns x 128 rows (16 KB each), the layout of the dQ tensor map
   static constexpr int kDQ = kDS + 32768;
-  static constexpr int kLse = kDQ + 128 * D * 4;  // log2(e) LSE of the query block (128 fp32)
-  static constexpr int kDvec = kLse + 512;   // D of the query block (128 fp32)
+  static constexpr int kLse = kDQ + 128 * D * 4;  // -log2(e) LSE of the query block (128 fp32)
+  static constexpr int kDvec = kLse + 512;   // -scale D of the query block (128 fp32)
   static constexpr int kBars = kDvec + 512;
-  // bQFull / bQFree: Q with log2(e) LSE and D; bOFull / bOFree: dO;
+  // bQFull / bQFree: Q with -log2(e) LSE and -scale D; bOFull / bOFree: dO;
   // bSFull, bDPFull: S^T, dP^T in TMEM; bPReady: P^T in TMEM, bDSReady: dS^T
   // in shared memory (8 arrivals each); bSHeld + w % 4: both warps of those
   // key rows hold their scores (2 arrivals); bStaged: the dQ partial is in
@@ -176,7 +235,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
         tma_load_3d(sb + L::kV + a * 16384, &p.tm_v, bar(L::bKV), a * 64, jb * 128, bh);
       }
       // dO of block t once dV of block t - 1 has read the previous one; Q,
-      // log2(e) LSE and D once dK of block t - 1 has (D is read while dS is
+      // -log2(e) LSE and -scale D once dK of block t - 1 has (D is read while dS is
       // formed, which dK waits for, so it travels with Q)
       int issued_o = 0, issued_q = 0;
       for (int t = 0; t < n_q; ++t) {
@@ -300,7 +359,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
     const int key = jb * 128 + r;
     const bool row_ok = key < p.N;
     const uint32_t lane_base = static_cast<uint32_t>(qw * 32) << 16;
-    const float c = p.c;
+    const uint64_t c2 = f2_pack(p.c, p.c);
+    const uint64_t sc2 = f2_pack(p.scale, p.scale);
     bool ok = true;
     for (int t = 0; t < n_q; ++t) {
       const int ib = q_block(t);
@@ -320,32 +380,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
       if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bSHeld + qw), t & 1, p, abort_flag))))
         break;
       tc_fence_after();
-      // causal: query ib * 128 + col sees this key iff col >= lim
-      const int lim = p.causal ? key - ib * 128 : -1;
+      // causal: query ib * 128 + col sees this key iff col >= lim (none for
+      // a key row past N)
+      const int lim = !row_ok ? INT_MAX : p.causal ? key - ib * 128 : -1;
       // P^T = exp2(c S^T - log2(e) LSE), kept in fp32 (over the scores'
       // registers) for dS^T and stored as bf16 over the scores' columns
-      // (columns 16 k .. for the 32-column chunk k)
+      // (columns 16 k .. for the 32-column chunk k); the mask only where
+      // this thread's columns 64 hf .. need it
+      const bool masked = lim > 64 * hf;
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
         const int k = 2 * hf + kk;  // 32-column chunk of the block's queries
         uint32_t pk[16];
-#pragma unroll
-        for (int i4 = 0; i4 < 8; ++i4) {
-          const float4 l4 = ld_shared_v4(sb + L::kLse + (32 * k + 4 * i4) * 4);
-          const float l2[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i = 4 * i4 + e;
-            const bool keep = row_ok && 32 * k + i >= lim;
-            const float pf =
-                keep ? ex2_approx(fmaf(__uint_as_float(s[kk][i]), c, -l2[e])) : 0.f;
-            s[kk][i] = __float_as_uint(pf);
-          }
-          pk[2 * i4] = pack_bf16x2(__uint_as_float(s[kk][4 * i4]),
-                                   __uint_as_float(s[kk][4 * i4 + 1]));
-          pk[2 * i4 + 1] = pack_bf16x2(__uint_as_float(s[kk][4 * i4 + 2]),
-                                       __uint_as_float(s[kk][4 * i4 + 3]));
-        }
+        if (masked)
+          bwd_p_chunk<true>(s[kk], pk, sb + L::kLse + 128 * k, c2, 32 * k, lim);
+        else
+          bwd_p_chunk<false>(s[kk], pk, sb + L::kLse + 128 * k, c2, 32 * k, lim);
         tmem_st16(tmem + lane_base + kBwdColS + 16 * k, pk);
       }
       tmem_wait_st();
@@ -365,19 +415,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
         tmem_ld32(tmem + lane_base + kBwdColDP + 32 * k, dp);
         tmem_wait_ld(dp);
         uint32_t dk[16];
-#pragma unroll
-        for (int i4 = 0; i4 < 8; ++i4) {
-          const float4 d4 = ld_shared_v4(sb + L::kDvec + (32 * k + 4 * i4) * 4);
-          const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
-          float dsv[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i = 4 * i4 + e;
-            dsv[e] = __uint_as_float(s[kk][i]) * (__uint_as_float(dp[i]) - dd[e]) * p.scale;
-          }
-          dk[2 * i4] = pack_bf16x2(dsv[0], dsv[1]);
-          dk[2 * i4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
-        }
+        bwd_ds_chunk(s[kk], dp, dk, sb + L::kDvec + 128 * k, sc2);
         const uint32_t row = sb + L::kDS + (k >> 1) * 16384 + r * 128;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
@@ -449,13 +487,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
   if (warp == kBwdMmaWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-// D_i = sum_d dO_id O_id and log2(e) LSE_i for every row, padded to whole
-// 128-row blocks (D = 0, log2(e) LSE = +inf past N, so those queries weigh
-// nothing); one warp per row.
+// -scale D_i (D_i = sum_d dO_id O_id) and -log2(e) LSE_i for every row,
+// padded to whole 128-row blocks (0 and -inf past N, so those queries weigh
+// nothing), in the forms the elementwise warps use: exp2(c S + (-log2(e)
+// LSE)) and P (scale dP + (-scale D)), one f32x2 FMA per pair; one warp per
+// row.
 template <int D>
 __global__ void fat_bwd_prep_kernel(const float* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                                     const float* __restrict__ lse, float* __restrict__ lse2,
-                                    float* __restrict__ dvec, int N, int Npad, long long rows) {
+                                    float* __restrict__ dvec, int N, int Npad, long long rows,
+                                    float scale) {
   const long long row = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -476,8 +517,8 @@ __global__ void fat_bwd_prep_kernel(const float* __restrict__ o, const __nv_bflo
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
   if (lane == 0) {
-    dvec[row] = n < N ? acc : 0.f;
-    lse2[row] = n < N ? lse[bh * N + n] * kLog2e : INFINITY;
+    dvec[row] = n < N ? -scale * acc : 0.f;
+    lse2[row] = n < N ? -(lse[bh * N + n] * kLog2e) : -INFINITY;
   }
 }
 

@@ -1,6 +1,6 @@
 // The backward pass with a second Q stage, for d = 64: the same five
 // tcgen05 MMAs per 128 x 128 tile and the same roles as fat_bwd_kernel, in
-// another order.  Q (with its log2(e) LSE and D) is double-buffered, so Sᵀ of
+// another order.  Q (with its -log2(e) LSE and -scale D) is double-buffered, so Sᵀ of
 // the next query block is issued right after dV of this one and runs while
 // the softmax warps form dSᵀ; they find it ready once they have.  Between the
 // two the softmax warps stage the last block's dQ partial, and the reduce
@@ -24,15 +24,15 @@ struct BwdSmemQ2 {
   static constexpr int kQ = 2 * kTile;       // [2 slots] by the parity of the query block
   static constexpr int kDO = 4 * kTile;
   static constexpr int kDS = 5 * kTile;      // dS^T: 128 keys x 128 queries bf16 (32 KB)
-  static constexpr int kLse = kDS + 32768;   // [2 slots] log2(e) LSE of the query block (128 fp32)
-  static constexpr int kDvec = kLse + 1024;  // [2 slots] D of the query block (128 fp32)
+  static constexpr int kLse = kDS + 32768;   // [2 slots] -log2(e) LSE of the query block (128 fp32)
+  static constexpr int kDvec = kLse + 1024;  // [2 slots] -scale D of the query block (128 fp32)
   // the dQ partial: fp32 as 128-byte-swizzled boxes of 32 columns x 128
   // rows (16 KB each, the layout of the dQ tensor map)
   static constexpr int kBoxes = D / 32;
   static constexpr int kX = kDvec + 1024;
   static constexpr int kBars = kX + kBoxes * 16384;
   __device__ __forceinline__ static int box(int b) { return kX + b * 16384; }
-  // bQFull / bQFree + slot: Q with log2(e) LSE and D; bOFull / bOFree: dO;
+  // bQFull / bQFree + slot: Q with -log2(e) LSE and -scale D; bOFull / bOFree: dO;
   // bSFull, bDPFull: S^T, dP^T in TMEM; bPReady: P^T in TMEM, bDSReady: dS^T
   // in shared memory (8 arrivals each); bSHeld + w % 4: both warps of those
   // key rows hold their scores (2 arrivals); bDQFull: the dQ partial in
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_q2_kernel(const __grid
         tma_load_3d(sb + L::kK + a * 16384, &p.tm_k, bar(L::bKV), a * 64, jb * 128, bh);
         tma_load_3d(sb + L::kV + a * 16384, &p.tm_v, bar(L::bKV), a * 64, jb * 128, bh);
       }
-      // Q of block t (with log2(e) LSE and D) into slot t % 2 once dK of
+      // Q of block t (with -log2(e) LSE and -scale D) into slot t % 2 once dK of
       // block t - 2 has read that slot (D is read while dS^T is formed,
       // which dK waits for, so it travels with Q); dO of block t once dV of
       // block t - 1 has read the previous one
@@ -278,7 +278,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_q2_kernel(const __grid
     const int key = jb * 128 + r;
     const bool row_ok = key < p.N;
     const uint32_t lane_base = static_cast<uint32_t>(qw * 32) << 16;
-    const float c = p.c;
+    const uint64_t c2 = f2_pack(p.c, p.c);
+    const uint64_t sc2 = f2_pack(p.scale, p.scale);
     // the dQ partial of block u (query rows 32 qw .., columns D/2 hf ..) out
     // of TMEM and into its staging boxes, once the reduce-adds of block u - 1
     // have read them
@@ -333,32 +334,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_q2_kernel(const __grid
       if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bSHeld + qw), t & 1, p, abort_flag))))
         break;
       tc_fence_after();
-      // causal: query ib * 128 + col sees this key iff col >= lim
-      const int lim = p.causal ? key - ib * 128 : -1;
+      // causal: query ib * 128 + col sees this key iff col >= lim (none for
+      // a key row past N)
+      const int lim = !row_ok ? INT_MAX : p.causal ? key - ib * 128 : -1;
       // P^T = exp2(c S^T - log2(e) LSE), kept in fp32 (over the scores'
       // registers) for dS^T and stored as bf16 over the scores' columns
-      // (columns 16 k .. for the 32-column chunk k)
+      // (columns 16 k .. for the 32-column chunk k); the mask only where
+      // this thread's columns 64 hf .. need it
+      const bool masked = lim > 64 * hf;
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
         const int k = 2 * hf + kk;  // 32-column chunk of the block's queries
         uint32_t pk[16];
-#pragma unroll
-        for (int i4 = 0; i4 < 8; ++i4) {
-          const float4 l4 = ld_shared_v4(lse_s + (32 * k + 4 * i4) * 4);
-          const float l2[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i = 4 * i4 + e;
-            const bool keep = row_ok && 32 * k + i >= lim;
-            const float pf =
-                keep ? ex2_approx(fmaf(__uint_as_float(s[kk][i]), c, -l2[e])) : 0.f;
-            s[kk][i] = __float_as_uint(pf);
-          }
-          pk[2 * i4] = pack_bf16x2(__uint_as_float(s[kk][4 * i4]),
-                                   __uint_as_float(s[kk][4 * i4 + 1]));
-          pk[2 * i4 + 1] = pack_bf16x2(__uint_as_float(s[kk][4 * i4 + 2]),
-                                       __uint_as_float(s[kk][4 * i4 + 3]));
-        }
+        if (masked)
+          bwd_p_chunk<true>(s[kk], pk, lse_s + 128 * k, c2, 32 * k, lim);
+        else
+          bwd_p_chunk<false>(s[kk], pk, lse_s + 128 * k, c2, 32 * k, lim);
         tmem_st16(tmem + lane_base + kBwdColS + 16 * k, pk);
       }
       tmem_wait_st();
@@ -384,19 +375,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_q2_kernel(const __grid
         uint32_t dp[32];
         tmem_ld32(tmem + lane_base + kBwdColDP + 32 * k, dp);
         tmem_wait_ld(dp);
-#pragma unroll
-        for (int i4 = 0; i4 < 8; ++i4) {
-          const float4 d4 = ld_shared_v4(dvec_s + (32 * k + 4 * i4) * 4);
-          const float dd[4] = {d4.x, d4.y, d4.z, d4.w};
-          float dsv[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i = 4 * i4 + e;
-            dsv[e] = __uint_as_float(s[kk][i]) * (__uint_as_float(dp[i]) - dd[e]) * p.scale;
-          }
-          dsk[kk][2 * i4] = pack_bf16x2(dsv[0], dsv[1]);
-          dsk[kk][2 * i4 + 1] = pack_bf16x2(dsv[2], dsv[3]);
-        }
+        bwd_ds_chunk(s[kk], dp, dsk[kk], dvec_s + 128 * k, sc2);
       }
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
