@@ -369,13 +369,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_q2_kernel(const __grid
         break;
       tc_fence_after();
       uint32_t dsk[2][16];
+      uint32_t dp[2][32];
+      tmem_ld32(tmem + lane_base + kBwdColDP + 64 * hf, dp[0]);
+      tmem_ld32(tmem + lane_base + kBwdColDP + 64 * hf + 32, dp[1]);
+      tmem_wait_ld(dp[0]);
+      tmem_wait_ld(dp[1]);
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
         const int k = 2 * hf + kk;
-        uint32_t dp[32];
-        tmem_ld32(tmem + lane_base + kBwdColDP + 32 * k, dp);
-        tmem_wait_ld(dp);
-        bwd_ds_chunk(s[kk], dp, dsk[kk], dvec_s + 128 * k, sc2);
+        bwd_ds_chunk(s[kk], dp[kk], dsk[kk], dvec_s + 128 * k, sc2);
       }
 #pragma unroll
       for (int kk = 0; kk < 2; ++kk) {
