@@ -21,7 +21,10 @@
 // query columns 64 (w / 4) ..) and then stage the block's dQ partial from
 // TMEM in shared memory; 8 issues the MMAs; 9 loads K and V once and Q, dO,
 // -log2(e) LSE and -scale D per query block with TMA; 10 adds each staged dQ
-// partial into global dQ with TMA reduce-adds.
+// partial into global dQ with TMA reduce-adds.  Q and dO swap their two
+// shared-memory slots every query block, so that the next Q loads as soon as
+// dV has read dO rather than after dK, and dQ is issued before dK: the
+// softmax warps wait for the dQ partial, the next dO for dK.
 #pragma once
 
 #include <climits>
@@ -126,15 +129,20 @@ struct BwdSmem {
   static constexpr int kTile = 128 * D * 2;  // one 128 x D bf16 tile
   static constexpr int kK = 0;
   static constexpr int kV = kTile;
-  static constexpr int kQ = 2 * kTile;
-  static constexpr int kDO = 3 * kTile;
+  // [2 slots] Q of query block t in slot t % 2, dO of block t in the other:
+  // the next Q goes where dO was as soon as dV has read it, the next dO where
+  // Q was once dK has read that
+  static constexpr int kSlot = 2 * kTile;
   static constexpr int kDS = 4 * kTile;      // dS^T: 128 keys x 128 queries bf16 (32 KB)
   // the dQ partial of a query block: fp32, 128-byte-swizzled boxes of 32
   // columns x 128 rows (16 KB each), the layout of the dQ tensor map
   static constexpr int kDQ = kDS + 32768;
-  static constexpr int kLse = kDQ + 128 * D * 4;  // -log2(e) LSE of the query block (128 fp32)
-  static constexpr int kDvec = kLse + 512;   // -scale D of the query block (128 fp32)
-  static constexpr int kBars = kDvec + 512;
+  // [2 slots by t % 2] -log2(e) LSE and -scale D of the query block (128
+  // fp32 each): the next block's arrive with its Q while dS^T of this one
+  // still reads D
+  static constexpr int kLse = kDQ + 128 * D * 4;
+  static constexpr int kDvec = kLse + 1024;
+  static constexpr int kBars = kDvec + 1024;
   // bQFull / bQFree: Q with -log2(e) LSE and -scale D; bOFull / bOFree: dO;
   // bSFull, bDPFull: S^T, dP^T in TMEM; bPReady: P^T in TMEM, bDSReady: dS^T
   // in shared memory (8 arrivals each); bSHeld + w % 4: both warps of those
@@ -146,7 +154,9 @@ struct BwdSmem {
                        kNumBars = 19;
   static constexpr int kMisc = kBars + 8 * kNumBars;  // u32: tmem base, abort
   static constexpr int kBytes = kMisc + 16;
-  static constexpr int kAlloc = kBytes + 1024;
+  // no room to align the base by hand: the dynamic shared memory must start
+  // 1024-byte aligned (the kernel checks and stops with an error otherwise)
+  static constexpr int kAlloc = kBytes;
   static_assert(kAlloc <= 227 * 1024, "shared memory budget");
 };
 
@@ -156,9 +166,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
   constexpr int kAtoms = D / 64;  // 128-byte column slabs of a tile
   constexpr int kColDQ = BwdColDQ<D>::value;
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* smem = smem_raw;
   const uint32_t sb = smem_u32(smem);
+  if (sb & 1023u) {  // (uniform over the block: no barrier has been used yet)
+    if (threadIdx.x == 0) atomicOr(p.error_word, 1u);
+    return;
+  }
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(smem + L::kMisc);
@@ -234,25 +247,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
         tma_load_3d(sb + L::kK + a * 16384, &p.tm_k, bar(L::bKV), a * 64, jb * 128, bh);
         tma_load_3d(sb + L::kV + a * 16384, &p.tm_v, bar(L::bKV), a * 64, jb * 128, bh);
       }
-      // dO of block t once dV of block t - 1 has read the previous one; Q,
-      // -log2(e) LSE and -scale D once dK of block t - 1 has (D is read while dS is
-      // formed, which dK waits for, so it travels with Q)
+      // Q of block t (with -log2(e) LSE and -scale D: D is read while dS^T
+      // is formed, so it travels with Q) into slot t % 2 once dV of block
+      // t - 1 has read dO of block t - 1 there; dO of block t into the other
+      // slot once dK of block t - 1 has read Q of block t - 1 there
       int issued_o = 0, issued_q = 0;
       for (int t = 0; t < n_q; ++t) {
         const int ib = q_block(t);
+        const int s = t & 1;
         if (t > 0 && !wait_bounded(bar(L::bOFree), (t - 1) & 1, p, abort_flag)) break;
-        mbar_arrive_expect_tx(bar(L::bOFull), L::kTile);
-        for (int a = 0; a < kAtoms; ++a)
-          tma_load_3d(sb + L::kDO + a * 16384, &p.tm_do, bar(L::bOFull), a * 64, ib * 128, bh);
-        issued_o = t + 1;
-        if (t > 0 && !wait_bounded(bar(L::bQFree), (t - 1) & 1, p, abort_flag)) break;
         mbar_arrive_expect_tx(bar(L::bQFull), L::kTile + 1024);
         for (int a = 0; a < kAtoms; ++a)
-          tma_load_3d(sb + L::kQ + a * 16384, &p.tm_q, bar(L::bQFull), a * 64, ib * 128, bh);
+          tma_load_3d(sb + L::kSlot + s * L::kTile + a * 16384, &p.tm_q, bar(L::bQFull), a * 64,
+                      ib * 128, bh);
         const size_t row0 = static_cast<size_t>(bh) * p.Npad + ib * 128;
-        bulk_load(sb + L::kLse, p.lse2 + row0, 512, bar(L::bQFull));
-        bulk_load(sb + L::kDvec, p.dvec + row0, 512, bar(L::bQFull));
+        bulk_load(sb + L::kLse + s * 512, p.lse2 + row0, 512, bar(L::bQFull));
+        bulk_load(sb + L::kDvec + s * 512, p.dvec + row0, 512, bar(L::bQFull));
         issued_q = t + 1;
+        if (t > 0 && !wait_bounded(bar(L::bQFree), (t - 1) & 1, p, abort_flag)) break;
+        mbar_arrive_expect_tx(bar(L::bOFull), L::kTile);
+        for (int a = 0; a < kAtoms; ++a)
+          tma_load_3d(sb + L::kSlot + (s ^ 1) * L::kTile + a * 16384, &p.tm_do, bar(L::bOFull),
+                      a * 64, ib * 128, bh);
+        issued_o = t + 1;
       }
       if (*abort_flag) {
         // let the copies already issued land before the CTA can exit
@@ -269,13 +286,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
     constexpr uint32_t idesc_ab_mn = idesc_f32acc<1u>(128, D, true, true); // A, B MN-major
     const uint64_t k_kmaj = sdesc_sw128(sb + L::kK, 16, 1024);
     const uint64_t v_kmaj = sdesc_sw128(sb + L::kV, 16, 1024);
-    const uint64_t q_kmaj = sdesc_sw128(sb + L::kQ, 16, 1024);
-    const uint64_t do_kmaj = sdesc_sw128(sb + L::kDO, 16, 1024);
+    const uint64_t slot_kmaj = sdesc_sw128(sb + L::kSlot, 16, 1024);
     const uint64_t ds_kmaj = sdesc_sw128(sb + L::kDS, 16, 1024);
-    const uint64_t q_mn = sdesc_sw128(sb + L::kQ, 16384, 1024);
-    const uint64_t do_mn = sdesc_sw128(sb + L::kDO, 16384, 1024);
+    const uint64_t slot_mn = sdesc_sw128(sb + L::kSlot, 16384, 1024);
     const uint64_t k_mn = sdesc_sw128(sb + L::kK, 16384, 1024);
     const uint64_t ds_mn = sdesc_sw128(sb + L::kDS, 16384, 1024);
+    // Q of block t in slot t % 2, dO in the other (descriptor units)
+    constexpr uint32_t kSlot1 = static_cast<uint32_t>(L::kTile >> 4);
     // K step kk (16 elements) of a K-major operand: 128-byte slab kk / 4,
     // 32-byte step kk % 4 within its rows; of an MN-major one: 16 rows
     auto kstep = [](int kk) -> uint32_t { return ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4; };
@@ -285,13 +302,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
       return __all_sync(0xffffffffu, wait_bounded(bar(b), phase & 1, p, abort_flag));
     };
     for (int t = 0; ok && t < n_q; ++t) {
+      const uint32_t q_slot = (t & 1) * kSlot1, do_slot = ((t & 1) ^ 1) * kSlot1;
       // S^T = K Q^T (its columns last held P^T of block t - 1, which the dV
       // MMAs issued before this one read)
       if (!(ok = wait_all(L::bQFull, t))) break;
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
-        mma_ss<false>(tmem + kBwdColS, k_kmaj + kstep(kk), q_kmaj + kstep(kk), idesc_sq, kk > 0);
+        mma_ss<false>(tmem + kBwdColS, k_kmaj + kstep(kk), slot_kmaj + q_slot + kstep(kk),
+                      idesc_sq, kk > 0);
       mma_commit(bar(L::bSFull));
       // dP^T = V dO^T (when the dQ partial shares its columns, once the
       // previous one has left them)
@@ -300,7 +319,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
-        mma_ss<false>(tmem + kBwdColDP, v_kmaj + kstep(kk), do_kmaj + kstep(kk), idesc_sq, kk > 0);
+        mma_ss<false>(tmem + kBwdColDP, v_kmaj + kstep(kk), slot_kmaj + do_slot + kstep(kk),
+                      idesc_sq, kk > 0);
       mma_commit(bar(L::bDPFull));
       // dV += P^T dO: P^T (bf16, two per column) from TMEM, 8 columns per K
       // step, while the softmax warps still form dS^T
@@ -308,25 +328,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
       tc_fence_after();
 #pragma unroll
       for (int g = 0; g < 8; ++g)
-        mma_ts<false>(tmem + kBwdColDV, tmem + kBwdColS + g * 8, do_mn + mnstep(g), idesc_b_mn,
-                      t > 0 || g > 0);
+        mma_ts<false>(tmem + kBwdColDV, tmem + kBwdColS + g * 8, slot_mn + do_slot + mnstep(g),
+                      idesc_b_mn, t > 0 || g > 0);
+      // dO's slot takes the next Q once these have completed
       mma_commit(bar(L::bOFree));
-      // dK += dS^T Q
       if (!(ok = wait_all(L::bDSReady, t))) break;
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        mma_ss<false>(tmem + kBwdColDV + D, ds_kmaj + kstep(kk), q_mn + mnstep(kk), idesc_b_mn,
-                      t > 0 || kk > 0);
-      mma_commit(bar(L::bQFree));
       // dQ partial = dS K (over dP^T, which the softmax warps have read, or in
-      // its own columns once the previous partial has left them)
+      // its own columns once the previous partial has left them), before dK:
+      // the softmax warps wait for it
       if (kColDQ != kBwdColDP && t > 0 && !(ok = wait_all(L::bDQFree, t - 1))) break;
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk)
         mma_ss<false>(tmem + kColDQ, ds_mn + mnstep(kk), k_mn + mnstep(kk), idesc_ab_mn, kk > 0);
       mma_commit(bar(L::bDQFull));
+      // dK += dS^T Q
+      tc_fence_after();
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ss<false>(tmem + kBwdColDV + D, ds_kmaj + kstep(kk), slot_mn + q_slot + mnstep(kk),
+                      idesc_b_mn, t > 0 || kk > 0);
+      // Q's slot takes the next dO once these have completed
+      mma_commit(bar(L::bQFree));
     }
     if (ok) {
       mma_commit(bar(L::bFinal));
@@ -364,6 +387,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
     bool ok = true;
     for (int t = 0; t < n_q; ++t) {
       const int ib = q_block(t);
+      const uint32_t lse_s = sb + L::kLse + (t & 1) * 512;
+      const uint32_t dvec_s = sb + L::kDvec + (t & 1) * 512;
       if (!(ok = __all_sync(0xffffffffu, wait_bounded(bar(L::bSFull), t & 1, p, abort_flag))))
         break;
       tc_fence_after();
@@ -393,9 +418,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
         const int k = 2 * hf + kk;  // 32-column chunk of the block's queries
         uint32_t pk[16];
         if (masked)
-          bwd_p_chunk<true>(s[kk], pk, sb + L::kLse + 128 * k, c2, 32 * k, lim);
+          bwd_p_chunk<true>(s[kk], pk, lse_s + 128 * k, c2, 32 * k, lim);
         else
-          bwd_p_chunk<false>(s[kk], pk, sb + L::kLse + 128 * k, c2, 32 * k, lim);
+          bwd_p_chunk<false>(s[kk], pk, lse_s + 128 * k, c2, 32 * k, lim);
         tmem_st16(tmem + lane_base + kBwdColS + 16 * k, pk);
       }
       tmem_wait_st();
@@ -415,7 +440,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
         tmem_ld32(tmem + lane_base + kBwdColDP + 32 * k, dp);
         tmem_wait_ld(dp);
         uint32_t dk[16];
-        bwd_ds_chunk(s[kk], dp, dk, sb + L::kDvec + 128 * k, sc2);
+        bwd_ds_chunk(s[kk], dp, dk, dvec_s + 128 * k, sc2);
         const uint32_t row = sb + L::kDS + (k >> 1) * 16384 + r * 128;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
