@@ -197,6 +197,62 @@ def cpu_oracle_sample(w, inp, budget_s: float = 10.0):
                       f"({t_total:.1f} s)"}
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the record."""
+    import subprocess
+
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def run_cpu_all(args):
+    """The oracle as it stands, timed on this host's cores on every benchmark
+    workload (whole heads until about --cpu-budget seconds of work have run),
+    and on one thread for the two smallest; one JSON line per measurement.
+    Needs no GPU."""
+    import oracle
+    from tensorized_online_softmax_gb300 import inputs as gen
+
+    model, cores = cpu_model(), oracle.available_cores()
+    names = ["tiny", "b4h16n2048d128", "b4h16n2048d128_causal", DEFAULT_WORKLOAD,
+             "stress_b1h32n16384d64", "fp8_b4h16n4096d128"]
+    for name in names:
+        w = gen.WORKLOADS[name]
+        inp = gen.make_inputs(w)
+        q64, k64, v64 = (gen.widened(inp, n) for n in ("q", "k", "v"))
+        flops_head = w.flops / (w.B * w.H)
+        for threads in ([0, 1] if name in ("tiny", "b4h16n2048d128") else [0]):
+            done, t_total, heads = 0.0, 0.0, 0
+            for bh in range(w.B * w.H):
+                b, h = divmod(bh, w.H)
+                qs, ks, vs = (t[b:b + 1, h:h + 1].numpy() for t in (q64, k64, v64))
+                t0 = time.perf_counter()
+                oracle.attn_fwd(qs, ks, vs, w.causal, w.scale, nthreads=threads)
+                t_total += time.perf_counter() - t0
+                done += flops_head
+                heads += 1
+                if t_total >= args.cpu_budget:
+                    break
+            print(json.dumps({
+                "cpu_oracle": name, "threads": threads if threads else cores, "cores": cores,
+                "cpu_model": model, "value": done / t_total / 1e12, "unit": "TFLOP/s",
+                "gflops_per_s": done / t_total / 1e9, "heads": heads, "of_heads": w.B * w.H,
+                "seconds": t_total, "seconds_per_head": t_total / heads,
+                "dtype": "f64", "kind": "oracle"}), flush=True)
+
+
 def run_reference(args, w):
     """The CPU oracle as the reference arm (rank 0 only)."""
     world, rank, _ = dist_setup()
@@ -646,8 +702,15 @@ def main():
                     help="time the backward pass on --workload (bf16) only, one line")
     ap.add_argument("--decode", action="store_true",
                     help="only the split-KV decode lines of --all")
+    ap.add_argument("--cpu-all", action="store_true",
+                    help="time the CPU oracle on every workload (no GPU), one line each")
+    ap.add_argument("--cpu-budget", type=float, default=5.0,
+                    help="seconds of oracle work per --cpu-all line")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.cpu_all:
+        run_cpu_all(args)
+        return
     if args.bwd:
         run_bwd(args, [args.workload], max(1, args.steps))
         return
