@@ -517,9 +517,7 @@ int fat_attn_bwd(const void* q, const void* k, const void* v, const float* o, co
   bp.poll_limit = 0;
   bp.timeout_ns = 4000000000ull;
   bp.error_word = g_dev[dev].error_word;
-  if (cudaMemsetAsync(dq, 0, static_cast<size_t>(BH) * N * d * sizeof(float), stream) !=
-      cudaSuccess)
-    return FAT_ERR_LAUNCH;
+  // (dQ is cleared by the preparation kernel, ahead of the fused kernel's adds)
   const int st = fat::launch_bwd(bp, d, o, dout, lse, dev, stream);
   if (st != 0) return st == -1 ? FAT_ERR_UNSUPPORTED : FAT_ERR_LAUNCH;
   return FAT_OK;

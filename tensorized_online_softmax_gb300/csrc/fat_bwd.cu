@@ -31,11 +31,11 @@ int launch_bwd_d(const BwdParams& bp, const float* o, const void* dout, const fl
   });
   if (ready[dev] != 1) return -4;
   const long long rows = static_cast<long long>(bp.BH) * bp.Npad;
-  const int warps = 8;
-  fat_bwd_prep_kernel<D><<<static_cast<unsigned>((rows + warps - 1) / warps), warps * 32, 0,
-                           stream>>>(o, static_cast<const __nv_bfloat16*>(dout), lse,
-                                     const_cast<float*>(bp.lse2), const_cast<float*>(bp.dvec),
-                                     bp.N, bp.Npad, rows, bp.scale);
+  constexpr int kRowsPerBlock = kPrepWarps * kPrepRows;
+  fat_bwd_prep_kernel<D><<<static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock),
+                           kPrepWarps * 32, 0, stream>>>(
+      o, static_cast<const __nv_bfloat16*>(dout), lse, const_cast<float*>(bp.lse2),
+      const_cast<float*>(bp.dvec), bp.dq, bp.N, bp.Npad, rows, bp.scale);
   if (cudaGetLastError() != cudaSuccess) return -4;
   kern<<<bp.BH * bp.n_blocks, kBwdThreads, smem, stream>>>(bp);
   return cudaGetLastError() == cudaSuccess ? 0 : -4;

@@ -41,7 +41,8 @@ struct BwdParams {
   CUtensorMap tm_dq;  // fp32 [B*H, N, d], boxes of 32 columns x 128 rows, 128-byte swizzle
   const float* lse2;  // [B*H][Npad] -log2(e) * LSE; -inf for rows >= N
   const float* dvec;  // [B*H][Npad] -scale * D; 0 for rows >= N
-  float* dq;          // fp32 [B*H, N, d], zero on entry, accumulated by TMA reduce-adds
+  float* dq;          // fp32 [B*H, N, d], cleared by the preparation kernel, then
+                      // accumulated by TMA reduce-adds
   float* dk;          // fp32 [B*H, N, d]
   float* dv;          // fp32 [B*H, N, d]
   int BH, N, Npad, causal, n_blocks;
@@ -515,35 +516,78 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
 // -scale D_i (D_i = sum_d dO_id O_id) and -log2(e) LSE_i for every row,
 // padded to whole 128-row blocks (0 and -inf past N, so those queries weigh
 // nothing), in the forms the elementwise warps use: exp2(c S + (-log2(e)
-// LSE)) and P (scale dP + (-scale D)), one f32x2 FMA per pair; one warp per
-// row.
+// LSE)) and P (scale dP + (-scale D)), one f32x2 FMA per pair; and dQ's rows
+// cleared for the reduce-adds that follow, in the same pass over the rows.
+// Each warp takes kPrepRows consecutive rows and issues all of their loads
+// before it reduces any, so that enough bytes are in flight to keep HBM busy.
+constexpr int kPrepRows = 4;
+constexpr int kPrepWarps = 8;
 template <int D>
-__global__ void fat_bwd_prep_kernel(const float* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
-                                    const float* __restrict__ lse, float* __restrict__ lse2,
-                                    float* __restrict__ dvec, int N, int Npad, long long rows,
-                                    float scale) {
-  const long long row = static_cast<long long>(blockIdx.x) * (blockDim.x / 32) + (threadIdx.x >> 5);
+__global__ void __launch_bounds__(kPrepWarps * 32)
+    fat_bwd_prep_kernel(const float* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
+                        const float* __restrict__ lse, float* __restrict__ lse2,
+                        float* __restrict__ dvec, float* __restrict__ dq, int N, int Npad,
+                        long long rows, float scale) {
+  static_assert(D == 64 || D == 128, "head dimension");
+  constexpr int kCols = D / 32;  // columns per lane: 2 or 4
   const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const long long bh = row / Npad;
-  const int n = static_cast<int>(row - bh * Npad);
-  float acc = 0.f;
-  if (n < N) {
-    const size_t base = (static_cast<size_t>(bh) * N + n) * D;
+  const long long row0 =
+      (static_cast<long long>(blockIdx.x) * kPrepWarps + (threadIdx.x >> 5)) * kPrepRows;
+  float ov[kPrepRows][kCols];
+  __nv_bfloat162 dv2[kPrepRows][kCols / 2];
+  size_t base[kPrepRows];
+  bool live[kPrepRows];
 #pragma unroll
-    for (int i = lane * 4; i < D; i += 128) {
-      const float4 ov = *reinterpret_cast<const float4*>(o + base + i);
-      const __nv_bfloat162 d01 = *reinterpret_cast<const __nv_bfloat162*>(dout + base + i);
-      const __nv_bfloat162 d23 = *reinterpret_cast<const __nv_bfloat162*>(dout + base + i + 2);
-      acc += ov.x * __low2float(d01) + ov.y * __high2float(d01) + ov.z * __low2float(d23) +
-             ov.w * __high2float(d23);
+  for (int r = 0; r < kPrepRows; ++r) {
+    const long long row = row0 + r;
+    const long long bh = row / Npad;
+    const int n = static_cast<int>(row - bh * Npad);
+    live[r] = row < rows && n < N;
+    base[r] = (static_cast<size_t>(bh) * N + n) * D + lane * kCols;
+#pragma unroll
+    for (int c = 0; c < kCols; ++c) ov[r][c] = 0.f;
+#pragma unroll
+    for (int c = 0; c < kCols / 2; ++c) dv2[r][c] = __floats2bfloat162_rn(0.f, 0.f);
+    if (live[r]) {
+      if constexpr (kCols == 4) {
+        const float4 a = *reinterpret_cast<const float4*>(o + base[r]);
+        ov[r][0] = a.x; ov[r][1] = a.y; ov[r][2] = a.z; ov[r][3] = a.w;
+      } else {
+        const float2 a = *reinterpret_cast<const float2*>(o + base[r]);
+        ov[r][0] = a.x; ov[r][1] = a.y;
+      }
+#pragma unroll
+      for (int c = 0; c < kCols / 2; ++c)
+        dv2[r][c] = *reinterpret_cast<const __nv_bfloat162*>(dout + base[r] + 2 * c);
     }
   }
+  float acc[kPrepRows];
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) {
-    dvec[row] = n < N ? -scale * acc : 0.f;
-    lse2[row] = n < N ? -(lse[bh * N + n] * kLog2e) : -INFINITY;
+  for (int r = 0; r < kPrepRows; ++r) {
+    acc[r] = 0.f;
+#pragma unroll
+    for (int c = 0; c < kCols / 2; ++c)
+      acc[r] += ov[r][2 * c] * __low2float(dv2[r][c]) + ov[r][2 * c + 1] * __high2float(dv2[r][c]);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+    for (int r = 0; r < kPrepRows; ++r) acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], off);
+#pragma unroll
+  for (int r = 0; r < kPrepRows; ++r) {
+    const long long row = row0 + r;
+    if (live[r]) {
+      if constexpr (kCols == 4)
+        *reinterpret_cast<float4*>(dq + base[r]) = make_float4(0.f, 0.f, 0.f, 0.f);
+      else
+        *reinterpret_cast<float2*>(dq + base[r]) = make_float2(0.f, 0.f);
+    }
+    if (lane == r && row < rows) {
+      const long long bh = row / Npad;
+      const int n = static_cast<int>(row - bh * Npad);
+      dvec[row] = n < N ? -scale * acc[r] : 0.f;
+      lse2[row] = n < N ? -(lse[bh * N + n] * kLog2e) : -INFINITY;
+    }
   }
 }
 
