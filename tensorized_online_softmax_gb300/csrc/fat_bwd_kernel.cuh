@@ -248,6 +248,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
         tma_load_3d(sb + L::kK + a * 16384, &p.tm_k, bar(L::bKV), a * 64, jb * 128, bh);
         tma_load_3d(sb + L::kV + a * 16384, &p.tm_v, bar(L::bKV), a * 64, jb * 128, bh);
       }
+      // -log2(e) LSE and -scale D come from the preparation kernel, which may
+      // still be running (programmatic dependent launch)
+      grid_dep_wait();
       // Q of block t (with -log2(e) LSE and -scale D: D is read while dS^T
       // is formed, so it travels with Q) into slot t % 2 once dV of block
       // t - 1 has read dO of block t - 1 there; dO of block t into the other
@@ -361,6 +364,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
     __syncwarp();
   } else if (warp == kBwdReduceWarp) {
     // =================== dQ reduce-adds ===================
+    grid_dep_wait();  // dQ is cleared by the preparation kernel
     for (int t = 0; t < n_q; ++t) {
       if (!__all_sync(0xffffffffu, wait_bounded(bar(L::bStaged), t & 1, p, abort_flag))) break;
       if (lane == 0) {
@@ -530,6 +534,9 @@ __global__ void __launch_bounds__(kPrepWarps * 32)
                         long long rows, float scale) {
   static_assert(D == 64 || D == 128, "head dimension");
   constexpr int kCols = D / 32;  // columns per lane: 2 or 4
+  // the fused kernel may start its set-up (it waits for this grid before it
+  // reads anything written here)
+  grid_dep_launch();
   const int lane = threadIdx.x & 31;
   const long long row0 =
       (static_cast<long long>(blockIdx.x) * kPrepWarps + (threadIdx.x >> 5)) * kPrepRows;

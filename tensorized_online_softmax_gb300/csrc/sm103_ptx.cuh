@@ -415,6 +415,19 @@ __device__ __forceinline__ void tmem_wait_st() {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+// Wait until the grids this one depends on (the previous kernel in the stream,
+// when this one was launched with programmatic stream serialisation) have
+// completed and their memory is visible; returns at once otherwise.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the dependent grid start launching (its blocks still wait for this
+// grid's completion wherever they call grid_dep_wait).
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // arithmetic
 // ---------------------------------------------------------------------------
 // 2^x on the MUFU unit (flushes subnormal results to zero; 2^-inf = 0).
