@@ -510,7 +510,15 @@ int fat_attn_bwd(const void* q, const void* k, const void* v, const float* o, co
     long long g = (48ll << 20) / per_head;
     if (g < 1) g = 1;
     if (g > BH) g = BH;
-    bp.group_heads = static_cast<int>(g);
+    if (d == 128) {
+      // balanced groups (bwd_work_item)
+      bp.group_heads = fat::bwd_group_heads(bh, static_cast<int>(g));
+      bp.group_extra = fat::bwd_group_extra(bh, static_cast<int>(g));
+    } else {
+      // the d = 64 kernel's own order: groups of g heads, the last one smaller
+      bp.group_heads = static_cast<int>(g);
+      bp.group_extra = 0;
+    }
   }
   bp.c = scale * fat::kLog2e;
   bp.scale = scale;

@@ -46,7 +46,10 @@ struct BwdParams {
   float* dk;          // fp32 [B*H, N, d]
   float* dv;          // fp32 [B*H, N, d]
   int BH, N, Npad, causal, n_blocks;
-  int group_heads;    // causal: heads whose blocks are ordered together
+  int group_heads;    // causal: heads per group of blocks ordered together ...
+  int group_extra;    // ... the first group_extra groups holding one more
+                      // (d = 128; the d = 64 kernel takes groups of
+                      // group_heads, the last one smaller)
   float c;            // log2(e) * scale
   float scale;
   unsigned long long poll_limit;
@@ -181,25 +184,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) fat_bwd_kernel(const __grid_co
 
   // work item: key block jb of head bh.  The blocks of a head re-read its Q
   // and dO and add into its dQ, so heads run a few at a time, as many as keep
-  // those in L2: without a mask every block does the same work and a head's
-  // blocks are simply consecutive; causal blocks go in groups of
-  // group_heads heads, the first key blocks (which see the most query blocks)
-  // first within a group.
+  // those in L2 (bwd_work_item in fat_schedule.h: balanced groups of heads
+  // when causal, the first key blocks first within a group).
   int jb, bh;
-  {
-    const int idx = static_cast<int>(blockIdx.x);
-    if (p.causal) {
-      const int per = p.group_heads * p.n_blocks;
-      const int g = idx / per;
-      const int rem = idx - g * per;
-      const int gh = min(p.group_heads, p.BH - g * p.group_heads);
-      jb = rem / gh;
-      bh = g * p.group_heads + rem % gh;
-    } else {
-      jb = idx % p.n_blocks;
-      bh = idx / p.n_blocks;
-    }
-  }
+  bwd_work_item(static_cast<int>(blockIdx.x), p.n_blocks, p.causal != 0, p.group_heads,
+                p.group_extra, jb, bh);
   const int ib0 = p.causal ? jb : 0;
   const int n_q = p.n_blocks - ib0;
   // query block of step t: causal blocks start at their diagonal; the others
