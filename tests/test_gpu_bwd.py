@@ -132,6 +132,27 @@ def test_full_size_sampled_bwd(cuda_device, shape):
                                                           np.abs(w).mean())
 
 
+@pytest.mark.parametrize("causal", [False, True], ids=["full", "causal"])
+def test_full_size_whole_tensor_bwd_b4h16n2048(cuda_device, causal):
+    """The B4 H16 N2048 d128 benchmark shape (64 heads, 16 key blocks each, the
+    launch the benchmark times): every element of dq, dk and dv against the
+    oracle, with the oracle's own O and LSE as the forward's outputs, at the
+    full-size bars of the sampled test."""
+    B, H, N, d = 4, 16, 2048, 128
+    q, k, v, do = _inputs(B, H, N, d, seed=4242 + int(causal))
+    scale = d ** -0.5
+    dq_r, dk_r, dv_r, o_r, lse_r = attn_bwd(_f64(q), _f64(k), _f64(v), _f64(do), causal, scale)
+    o = torch.from_numpy(o_r).float().cuda()
+    lse = torch.from_numpy(lse_r).float().cuda()
+    dq, dk, dv = fat.attn_bwd(q.cuda(), k.cuda(), v.cuda(), o, lse, do.cuda(), causal, scale)
+    torch.cuda.synchronize()
+    for name, got, ref in (("dq", dq, dq_r), ("dk", dk, dk_r), ("dv", dv, dv_r)):
+        err = np.abs(_f64(got) - ref)
+        assert np.isfinite(err).all(), name
+        assert err.max() <= 1e-2 * np.abs(ref).max(), (name, err.max(), np.abs(ref).max())
+        assert err.mean() <= 4e-3 * np.abs(ref).mean(), (name, err.mean(), np.abs(ref).mean())
+
+
 def test_bwd_argument_errors(cuda_device):
     q, k, v, do = (t.cuda() for t in _inputs(1, 1, 256, 64, seed=5))
     o, lse = fat.attn_fwd(q, k, v, False, 0.125, 64)
