@@ -32,7 +32,9 @@ int launch_bwd_d(const BwdParams& bp, const float* o, const void* dout, const fl
   if (ready[dev] != 1) return -4;
   const long long rows = static_cast<long long>(bp.BH) * bp.Npad;
   constexpr int kRowsPerBlock = kPrepWarps * kPrepRows;
-  fat_bwd_prep_kernel<D><<<static_cast<unsigned>((rows + kRowsPerBlock - 1) / kRowsPerBlock),
+  const long long prep_blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
+  if (prep_blocks > 0x7fffffffll) return -1;  // (beyond any device memory; nothing launched)
+  fat_bwd_prep_kernel<D><<<static_cast<unsigned>(prep_blocks),
                            kPrepWarps * 32, 0, stream>>>(
       o, static_cast<const __nv_bfloat16*>(dout), lse, const_cast<float*>(bp.lse2),
       const_cast<float*>(bp.dvec), bp.dq, bp.N, bp.Npad, rows, bp.scale);
