@@ -16,6 +16,11 @@ NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-std=c++17", "-lineinfo",
     "-Xcompiler", "-fPIC",
+    # the per-device launch state sits in function-local statics of kernel
+    # templates; without this GCC marks them unique across every loaded
+    # library, so a second copy of this library in one process would find
+    # another copy's state and skip its own kernel set-up
+    "-Xcompiler", "-fno-gnu-unique",
 ]
 
 
@@ -25,8 +30,10 @@ def translation_units():
 
 
 def _sources():
+    # (this file too: a change of flags rebuilds)
     return (glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cuh"))
-            + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(ROOT, "include", "*.h")))
+            + glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(ROOT, "include", "*.h"))
+            + [os.path.abspath(__file__)])
 
 
 def nvcc_path() -> str | None:
