@@ -40,6 +40,16 @@ def test_library_exports_every_declared_symbol(lib):
         assert re.search(rf"\bT {name}$", out, flags=re.M), name
 
 
+def test_no_symbol_is_unique_across_loaded_libraries(lib):
+    # each loaded copy of the library must keep its own kernel launch state
+    # (function-local statics of the kernel templates); GCC's STB_GNU_UNIQUE
+    # binding would merge them across copies, so the build turns it off
+    out = subprocess.run(["nm", "-D", _build.LIB_PATH], capture_output=True, text=True).stdout
+    # (nm marks a unique global "u"; "U" is an undefined symbol)
+    unique = [line for line in out.splitlines() if re.search(r"\su\s", line)]
+    assert out.strip() and not unique, unique[:5]
+
+
 def test_status_strings(lib):
     for code, name in [(0, "FAT_OK"), (-1, "FAT_ERR_INVALID_ARG"), (-2, "FAT_ERR_UNSUPPORTED"),
                        (-3, "FAT_ERR_ALIGNMENT"), (-4, "FAT_ERR_LAUNCH"),
